@@ -1,0 +1,281 @@
+"""Pins for the fp64 oracle: checks against something other than the oracle.
+
+Each ``pin_*`` function takes an :class:`oracle.Oracle` and raises
+AssertionError when the oracle disagrees with what the pages or the
+mathematics fix. They are used twice: on the real oracle
+(``test_oracle_pins.py``) and on deliberately broken copies of it
+(``test_oracle_mutations.py``), where at least one pin must fail.
+
+What each pin compares against:
+
+* exact rational arithmetic (``fractions.Fraction``) on tiny inputs, a method
+  that does no floating-point rounding at all;
+* a library routine: ``torch.matmul`` in float64, whose lower triangle scaled
+  by 1/sqrt(HS) is the causal score ("llm.c dev/cuda/trimat_forward.cu",
+  the referee computes q.k only for t2 <= t), and X @ W.T for the dense layer
+  ("DietCode ... test_local_padding", Y[i, j] += X[i, k] * W[j, k]);
+* closed forms (all-ones, one-hot, small integers whose sums are exact);
+* invariants: mask positions and counts, causality under perturbation, head
+  permutation, zero padding along the reduction axis (local padding), row
+  independence, transposition.
+"""
+from __future__ import annotations
+
+import math
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+from causal_attention_score_gb300 import synth
+
+MASK_NAN = 0
+MASK_NEG_INF = 1
+
+
+# ---------------------------------------------------------------- helpers --
+
+def _u16_to_f32(u: np.ndarray) -> np.ndarray:
+    return (u.astype(np.uint32) << 16).view(np.float32)
+
+
+def _bits_of(values: np.ndarray) -> np.ndarray:
+    """bf16 patterns of float values that are exactly representable in bf16."""
+    f = np.asarray(values, dtype=np.float32)
+    bits = f.view(np.uint32)
+    if np.any(bits & 0xFFFF):
+        raise ValueError("value not exactly representable in bf16")
+    return (bits >> 16).astype(np.uint16)
+
+
+def _qkv_from_parts(Q: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:
+    """Pack float arrays Q, K, V of shape (B, T, NH, HS) into (B, T, 3, NH, HS) bf16 bits."""
+    qkv = np.stack([Q, K, V], axis=2)
+    return _bits_of(qkv)
+
+
+def _random_qkv(B, T, NH, HS, seed, dist="uniform"):
+    shape = synth.TrimulShape(B=B, T=T, C=NH * HS, NH=NH)
+    t = synth.trimul_input(shape, seed=seed, dist=dist)
+    return synth.bf16_bits(t).reshape(-1)
+
+
+def _split_qk(qkv_u16, B, T, NH, HS):
+    f = _u16_to_f32(qkv_u16).astype(np.float64).reshape(B, T, 3, NH, HS)
+    Q = f[:, :, 0].transpose(0, 2, 1, 3)  # (B, NH, T, HS)
+    K = f[:, :, 1].transpose(0, 2, 1, 3)
+    return Q, K
+
+
+# ------------------------------------------------------- score product pins --
+
+def pin_trimul_exact_rational(o):
+    """Brute force in exact rationals on tiny inputs, then one division by sqrt(HS)."""
+    for (B, T, NH, HS, seed) in [(2, 7, 2, 8, 3), (1, 5, 1, 16, 4), (1, 1, 3, 8, 5)]:
+        C = NH * HS
+        qkv = _random_qkv(B, T, NH, HS, seed)
+        f = _u16_to_f32(qkv).reshape(B, T, 3, NH, HS)
+        out = o.trimul(qkv, B, T, C, NH, MASK_NAN)
+        root = math.sqrt(HS)
+        for b in range(B):
+            for h in range(NH):
+                for t in range(T):
+                    for t2 in range(T):
+                        got = out[b, h, t, t2]
+                        if t2 > t:
+                            assert math.isnan(got), (b, h, t, t2, got)
+                            continue
+                        exact = sum((Fraction(float(f[b, t, 0, h, d])) * Fraction(float(f[b, t2, 1, h, d]))
+                                     for d in range(HS)), Fraction(0))
+                        want = float(exact) / root
+                        assert abs(got - want) <= 1e-14 * (1.0 + abs(want)), (b, h, t, t2, got, want)
+
+
+def pin_trimul_matmul_identity(o):
+    """The unmasked triangle equals the lower half of a full Q K^T (torch fp64) / sqrt(HS)."""
+    for (B, T, NH, HS, seed, dist) in [(2, 37, 3, 24, 11, "normal"), (1, 130, 2, 64, 12, "uniform")]:
+        C = NH * HS
+        qkv = _random_qkv(B, T, NH, HS, seed, dist)
+        Q, K = _split_qk(qkv, B, T, NH, HS)
+        full = torch.matmul(torch.from_numpy(Q), torch.from_numpy(K).transpose(-1, -2)).numpy()
+        want = full / math.sqrt(HS)
+        out = o.trimul(qkv, B, T, C, NH, MASK_NAN)
+        lower = np.tril(np.ones((T, T), dtype=bool))
+        got_l = out[..., lower]
+        want_l = want[..., lower]
+        assert np.all(np.isfinite(got_l))
+        assert np.max(np.abs(got_l - want_l) / (1.0 + np.abs(want_l))) <= 1e-12
+        assert np.all(np.isnan(out[..., ~lower]))
+
+
+def pin_trimul_closed_forms(o):
+    """All-ones rows give sqrt(HS); one-hot rows give delta / sqrt(HS)."""
+    for HS in (4, 16, 64, 128, 256):
+        B, T, NH = 1, 6, 2
+        ones = np.ones((B, T, NH, HS), dtype=np.float32)
+        qkv = _qkv_from_parts(ones, ones, ones * 2)
+        out = o.trimul(qkv, B, T, NH * HS, NH, MASK_NAN)
+        lower = np.tril(np.ones((T, T), dtype=bool))
+        # HS / sqrt(HS) == sqrt(HS): exact for perfect squares, within one ulp otherwise.
+        want = math.sqrt(HS)
+        err = np.abs(out[..., lower] - want)
+        if math.isqrt(HS) ** 2 == HS:
+            assert np.all(err == 0.0), (HS, out[..., lower][:4])
+        else:
+            assert np.all(err <= 2 * np.spacing(want)), HS
+    # one-hot: Q[t] = e_{t mod HS}, K[t2] = e_{(t2 + 1) mod HS}
+    B, T, NH, HS = 1, 9, 1, 4
+    Q = np.zeros((B, T, NH, HS), np.float32)
+    K = np.zeros((B, T, NH, HS), np.float32)
+    for t in range(T):
+        Q[0, t, 0, t % HS] = 1.0
+        K[0, t, 0, (t + 1) % HS] = 1.0
+    out = o.trimul(_qkv_from_parts(Q, K, np.zeros_like(Q)), B, T, NH * HS, NH, MASK_NAN)
+    for t in range(T):
+        for t2 in range(t + 1):
+            want = 0.5 if (t % HS) == ((t2 + 1) % HS) else 0.0  # 1/sqrt(4)
+            assert out[0, 0, t, t2] == want, (t, t2, out[0, 0, t, t2])
+
+
+def pin_trimul_integer_exact(o):
+    """Small-integer inputs: every sum is exact; compare with int64 arithmetic."""
+    rng = np.random.default_rng(7)
+    for (B, T, NH, HS) in [(2, 11, 2, 64), (1, 8, 3, 16), (1, 5, 1, 4)]:
+        ints = rng.integers(-4, 5, size=(B, T, 3, NH, HS)).astype(np.int64)
+        qkv = _bits_of(ints.astype(np.float32))
+        out = o.trimul(qkv, B, T, NH * HS, NH, MASK_NAN)
+        Qi = ints[:, :, 0].transpose(0, 2, 1, 3)
+        Ki = ints[:, :, 1].transpose(0, 2, 1, 3)
+        dots = np.einsum("bhtd,bhsd->bhts", Qi, Ki)  # exact int64
+        root = math.isqrt(HS)  # 8, 4, 2: exact divisions
+        for t in range(T):
+            for t2 in range(t + 1):
+                assert np.array_equal(out[:, :, t, t2], dots[:, :, t, t2] / root)
+
+
+def pin_trimul_index_roles(o):
+    """Query rows index t, key rows index t2, keys sit C after the queries, V is ignored,
+    heads and batches are kept apart. Built so that any swap changes the value."""
+    B, T, NH, HS = 2, 6, 3, 16
+    Q = np.zeros((B, T, NH, HS), np.float32)
+    K = np.zeros((B, T, NH, HS), np.float32)
+    V = np.full((B, T, NH, HS), 96.0, np.float32)
+    for b in range(B):
+        for t in range(T):
+            for h in range(NH):
+                Q[b, t, h, 0] = t + 1
+                Q[b, t, h, 1] = h + 1
+                K[b, t, h, 0] = 1.0
+                K[b, t, h, 1] = (b + 1) * (t + 1)
+    out = o.trimul(_qkv_from_parts(Q, K, V), B, T, NH * HS, NH, MASK_NAN)
+    for b in range(B):
+        for h in range(NH):
+            for t in range(T):
+                for t2 in range(t + 1):
+                    want = ((t + 1) + (h + 1) * (b + 1) * (t2 + 1)) / 4.0
+                    assert out[b, h, t, t2] == want, (b, h, t, t2, out[b, h, t, t2], want)
+
+
+def pin_trimul_mask_and_causality(o):
+    """Mask count T(T-1)/2 per head at exactly t2 > t; -inf mode; causality under perturbation."""
+    B, T, NH, HS = 2, 19, 2, 8
+    C = NH * HS
+    qkv = _random_qkv(B, T, NH, HS, 21)
+    out = o.trimul(qkv, B, T, C, NH, MASK_NAN)
+    upper = np.triu(np.ones((T, T), dtype=bool), k=1)
+    nan = np.isnan(out)
+    assert nan.sum() == B * NH * T * (T - 1) // 2
+    assert np.array_equal(nan, np.broadcast_to(upper, out.shape))
+    out_inf = o.trimul(qkv, B, T, C, NH, MASK_NEG_INF)
+    assert np.all(out_inf[..., upper] == -np.inf)
+    assert np.array_equal(out_inf[..., ~upper], out[..., ~upper])
+    # changing key row s touches only column s at rows t >= s
+    s = 7
+    pert = qkv.reshape(B, T, 3, NH, HS).copy()
+    pert[:, s, 1] = _bits_of(np.full((B, NH, HS), 0.75, np.float32))
+    out_p = o.trimul(pert.reshape(-1), B, T, C, NH, MASK_NAN)
+    changed = ~((out_p == out) | (np.isnan(out_p) & np.isnan(out)))
+    allowed = np.zeros((T, T), dtype=bool)
+    allowed[s:, s] = True
+    assert not np.any(changed & ~allowed)
+    assert np.any(changed[..., s:, s])
+    # permuting the heads of the input permutes the heads of the output
+    perm = [1, 0]
+    permuted = qkv.reshape(B, T, 3, NH, HS)[:, :, :, perm].copy().reshape(-1)
+    out_h = o.trimul(permuted, B, T, C, NH, MASK_NAN)
+    assert np.array_equal(np.nan_to_num(out_h), np.nan_to_num(out[:, perm]))
+
+
+def pin_trimul_rows(o):
+    """Sampled rows agree with the full tensor."""
+    B, T, NH, HS = 2, 23, 3, 8
+    qkv = _random_qkv(B, T, NH, HS, 31)
+    full = o.trimul(qkv, B, T, NH * HS, NH, MASK_NAN)
+    bht = np.array([[0, 0, 0], [1, 2, 22], [0, 1, 11], [1, 0, 5]])
+    rows = o.trimul_rows(qkv, B, T, NH * HS, NH, bht, MASK_NAN)
+    for i, (b, h, t) in enumerate(bht):
+        assert np.array_equal(np.nan_to_num(rows[i], nan=7.0), np.nan_to_num(full[b, h, t], nan=7.0))
+
+
+# ------------------------------------------------------------ dense pins --
+
+def _dense_random(M, I, H, seed):
+    X, W = synth.dense_input(synth.DenseShape(M=M, I=I, H=H), seed=seed)
+    return synth.bf16_bits(X).reshape(-1), synth.bf16_bits(W).reshape(-1)
+
+
+def pin_dense_exact_rational(o):
+    M, I, H = 3, 5, 4
+    x, w = _dense_random(M, I, H, 41)
+    xf, wf = _u16_to_f32(x).reshape(M, I), _u16_to_f32(w).reshape(H, I)
+    Y = o.dense(x, w, M, I, H)
+    for i in range(M):
+        for j in range(H):
+            exact = sum((Fraction(float(xf[i, k])) * Fraction(float(wf[j, k])) for k in range(I)),
+                        Fraction(0))
+            assert abs(Y[i, j] - float(exact)) <= 1e-15 * (1 + abs(float(exact)))
+
+
+def pin_dense_matmul_identity(o):
+    for (M, I, H, seed) in [(37, 45, 29, 42), (130, 770, 70, 43)]:
+        x, w = _dense_random(M, I, H, seed)
+        xf = torch.from_numpy(_u16_to_f32(x).astype(np.float64).reshape(M, I))
+        wf = torch.from_numpy(_u16_to_f32(w).astype(np.float64).reshape(H, I))
+        want = (xf @ wf.T).numpy()
+        Y = o.dense(x, w, M, I, H)
+        assert np.max(np.abs(Y - want) / (1 + np.abs(want))) <= 1e-12
+
+
+def pin_dense_integer_exact(o):
+    rng = np.random.default_rng(9)
+    M, I, H = 17, 770, 13
+    Xi = rng.integers(-4, 5, size=(M, I)).astype(np.int64)
+    Wi = rng.integers(-4, 5, size=(H, I)).astype(np.int64)
+    Y = o.dense(_bits_of(Xi.astype(np.float32)), _bits_of(Wi.astype(np.float32)), M, I, H)
+    assert np.array_equal(Y, (Xi @ Wi.T).astype(np.float64))
+
+
+def pin_dense_local_padding(o):
+    """Zero columns appended along I change nothing; rows are independent;
+    swapping X and W transposes Y."""
+    M, I, H = 9, 13, 6
+    x, w = _dense_random(M, I, H, 44)
+    Y = o.dense(x, w, M, I, H)
+    pad = 19
+    xp = np.concatenate([x.reshape(M, I), np.zeros((M, pad), np.uint16)], axis=1)
+    wp = np.concatenate([w.reshape(H, I), np.zeros((H, pad), np.uint16)], axis=1)
+    assert np.array_equal(o.dense(xp.reshape(-1), wp.reshape(-1), M, I + pad, H), Y)
+    one = o.dense(x.reshape(M, I)[4:5].reshape(-1), w, 1, I, H)
+    assert np.array_equal(one[0], Y[4])
+    rows = o.dense_rows(x, w, M, I, H, np.array([8, 0, 4]))
+    assert np.array_equal(rows, Y[[8, 0, 4]])
+    Yt = o.dense(w, x, H, I, M)
+    assert np.array_equal(Yt, Y.T)
+
+
+TRIMUL_PINS = [pin_trimul_exact_rational, pin_trimul_matmul_identity, pin_trimul_closed_forms,
+               pin_trimul_integer_exact, pin_trimul_index_roles, pin_trimul_mask_and_causality,
+               pin_trimul_rows]
+DENSE_PINS = [pin_dense_exact_rational, pin_dense_matmul_identity, pin_dense_integer_exact,
+              pin_dense_local_padding]
+ALL_PINS = TRIMUL_PINS + DENSE_PINS
