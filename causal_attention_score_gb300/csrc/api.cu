@@ -1,0 +1,230 @@
+// C ABI of libcsa_gb300.so: argument validation, per-device facts, tensor-map
+// encoding through the runtime's driver entry point, and the device status
+// word that bounded waits report into. The compute lives in
+// trimul_sm103a.cu and dense_sm103a.cu.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "csa.h"
+#include "csa_internal.h"
+
+// Per device: [0] = first error code recorded by a kernel, [1] = wait site.
+__device__ int g_csa_status[2];
+
+namespace csa {
+namespace {
+
+thread_local std::string t_last_error;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+bool g_dev_ready[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+std::atomic<uint64_t> g_wait_limit_ns{0};
+std::atomic<int> g_inject{0};
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
+
+int set_error(int code, const std::string& msg) {
+  t_last_error = msg;
+  return code;
+}
+
+int cuda_error(const char* what, cudaError_t e) {
+  return set_error(CSA_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+}  // namespace
+
+int current_device(DeviceInfo& info, std::string& err) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    err = std::string("cudaGetDevice: ") + cudaGetErrorString(e);
+    return CSA_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) {
+    err = "device ordinal out of range";
+    return CSA_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_dev_ready[dev]) {
+    DeviceInfo d;
+    d.device = dev;
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) ||
+        (e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) ||
+        (e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                    dev))) {
+      err = std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e);
+      return CSA_ERR_CUDA;
+    }
+    d.cc = major * 10 + minor;
+    if (d.cc != 103) {
+      err = "this library is built for sm_103a (GB300); current device is sm_" +
+            std::to_string(d.cc);
+      return CSA_ERR_ARCH;
+    }
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_csa_status)) != cudaSuccess) {
+      err = std::string("cudaGetSymbolAddress(status): ") + cudaGetErrorString(e);
+      return CSA_ERR_CUDA;
+    }
+    d.status_word = static_cast<int*>(p);
+    if (!g_encode) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+        err = "cuTensorMapEncodeTiled entry point unavailable";
+        return CSA_ERR_CUDA;
+      }
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    g_dev[dev] = d;
+    g_dev_ready[dev] = true;
+  }
+  info = g_dev[dev];
+  return CSA_OK;
+}
+
+int encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, const void* addr,
+                 const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                 CUtensorMapSwizzle swizzle, std::string& err) {
+  cuuint64_t d[5], s[4];
+  cuuint32_t b[5], es[5];
+  for (uint32_t i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) s[i] = strides_bytes[i];
+  }
+  CUresult r = g_encode(map, dtype, rank, const_cast<void*>(addr), d, s, b, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    err = "cuTensorMapEncodeTiled failed (code " + std::to_string(static_cast<int>(r)) + ")";
+    return CSA_ERR_ALIGN;
+  }
+  return CSA_OK;
+}
+
+uint64_t wait_limit_ns() {
+  const uint64_t v = g_wait_limit_ns.load();
+  return v ? v : kDefaultWaitLimitNs;
+}
+
+bool take_inject() { return g_inject.exchange(0) != 0; }
+
+}  // namespace csa
+
+using namespace csa;
+
+extern "C" {
+
+csa_status trimul_forward_ex(float* out, const void* qkv, int B, int T, int C, int NH,
+                             uint32_t mask_bits, uint32_t flags, void* stream) {
+  t_last_error.clear();
+  if (!out || !qkv) return set_error(CSA_ERR_NULL, "trimul_forward: null pointer");
+  if (B <= 0 || T <= 0 || C <= 0 || NH <= 0)
+    return set_error(CSA_ERR_SHAPE, "trimul_forward: B, T, C, NH must be >= 1");
+  if (C % NH != 0) return set_error(CSA_ERR_SHAPE, "trimul_forward: C % NH != 0");
+  if (flags & ~CSA_TRIMUL_LOWER_ONLY)
+    return set_error(CSA_ERR_UNSUPPORTED, "trimul_forward: unknown flags");
+  const int HS = C / NH;
+  if (HS % 8 != 0)
+    return set_error(CSA_ERR_ALIGN, "trimul_forward: HS = C/NH must be a multiple of 8");
+  if (HS > 256) return set_error(CSA_ERR_UNSUPPORTED, "trimul_forward: HS > 256");
+  if (reinterpret_cast<uintptr_t>(qkv) % 16 != 0 || reinterpret_cast<uintptr_t>(out) % 4 != 0)
+    return set_error(CSA_ERR_ALIGN, "trimul_forward: qkv must be 16-byte aligned, out 4-byte");
+  DeviceInfo dev;
+  std::string err;
+  int rc = current_device(dev, err);
+  if (rc != CSA_OK) return set_error(rc, err);
+  rc = trimul_launch(out, qkv, B, T, C, NH, mask_bits, flags, static_cast<cudaStream_t>(stream),
+                     dev, err);
+  if (rc != CSA_OK) return set_error(rc, err);
+  return CSA_OK;
+}
+
+csa_status trimul_forward(float* out, const void* qkv, int B, int T, int C, int NH) {
+  return trimul_forward_ex(out, qkv, B, T, C, NH, CSA_MASK_NAN, CSA_TRIMUL_FULL, nullptr);
+}
+
+csa_status dense_xwt_ex(float* Y, const void* X, const void* W, int M, int I, int H,
+                        void* stream) {
+  t_last_error.clear();
+  if (!Y || !X || !W) return set_error(CSA_ERR_NULL, "dense_xwt: null pointer");
+  if (M <= 0 || I <= 0 || H <= 0)
+    return set_error(CSA_ERR_SHAPE, "dense_xwt: M, I, H must be >= 1");
+  if (reinterpret_cast<uintptr_t>(X) % 2 || reinterpret_cast<uintptr_t>(W) % 2 ||
+      reinterpret_cast<uintptr_t>(Y) % 4)
+    return set_error(CSA_ERR_ALIGN, "dense_xwt: X, W need 2-byte and Y 4-byte alignment");
+  DeviceInfo dev;
+  std::string err;
+  int rc = current_device(dev, err);
+  if (rc != CSA_OK) return set_error(rc, err);
+  rc = dense_launch(Y, X, W, M, I, H, static_cast<cudaStream_t>(stream), dev, err);
+  if (rc != CSA_OK) return set_error(rc, err);
+  return CSA_OK;
+}
+
+csa_status dense_xwt(float* Y, const void* X, const void* W, int M, int I, int H) {
+  return dense_xwt_ex(Y, X, W, M, I, H, nullptr);
+}
+
+csa_status csa_get_status(void* stream) {
+  t_last_error.clear();
+  DeviceInfo dev;
+  std::string err;
+  int rc = current_device(dev, err);
+  if (rc != CSA_OK) return set_error(rc, err);
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_error("csa_get_status: cudaStreamSynchronize", e);
+  int host[2] = {0, 0};
+  e = cudaMemcpy(host, dev.status_word, sizeof host, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_error("csa_get_status: read status", e);
+  if (host[0] != 0) {
+    const int zero[2] = {0, 0};
+    e = cudaMemcpy(dev.status_word, zero, sizeof zero, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_error("csa_get_status: clear status", e);
+    t_last_error = "device wait ran out at site " + std::to_string(host[1]);
+    return host[0];
+  }
+  return CSA_OK;
+}
+
+const char* csa_status_string(csa_status s) {
+  switch (s) {
+    case CSA_OK: return "ok";
+    case CSA_ERR_NULL: return "null pointer";
+    case CSA_ERR_SHAPE: return "invalid shape";
+    case CSA_ERR_ALIGN: return "alignment or stride requirement not met";
+    case CSA_ERR_UNSUPPORTED: return "unsupported size or flag";
+    case CSA_ERR_ARCH: return "device is not sm_103";
+    case CSA_ERR_LAUNCH: return "kernel launch failed";
+    case CSA_ERR_TIMEOUT: return "device-side wait ran out";
+    case CSA_ERR_CUDA: return "CUDA call failed";
+    default: return "unknown status";
+  }
+}
+
+const char* csa_last_error(void) { return t_last_error.c_str(); }
+
+const char* csa_version(void) { return "0.1.0 sm_103a"; }
+
+void csa_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns); }
+
+void csa_debug_inject(int enable) { g_inject.store(enable ? 1 : 0); }
+
+}  // extern "C"

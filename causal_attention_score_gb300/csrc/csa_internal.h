@@ -1,0 +1,41 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <string>
+
+#include "csa.h"
+
+namespace csa {
+
+// Per-device facts, queried once per device and cached.
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+  int cc = 0;              // major * 10 + minor
+  int max_smem_optin = 0;  // bytes of dynamic shared memory a block may opt into
+  int* status_word = nullptr;  // device address of the [code, site] status pair
+};
+
+// Fills `info` for the current device. Returns CSA_OK, CSA_ERR_CUDA or CSA_ERR_ARCH.
+int current_device(DeviceInfo& info, std::string& err);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+int encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, const void* addr,
+                 const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                 CUtensorMapSwizzle swizzle, std::string& err);
+
+uint64_t wait_limit_ns();
+bool take_inject();
+
+// Kernel launchers; each validates what is specific to its kernel.
+int trimul_launch(float* out, const void* qkv, int B, int T, int C, int NH, uint32_t mask_bits,
+                  uint32_t flags, cudaStream_t stream, const DeviceInfo& dev, std::string& err);
+
+int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
+                 cudaStream_t stream, const DeviceInfo& dev, std::string& err);
+
+}  // namespace csa

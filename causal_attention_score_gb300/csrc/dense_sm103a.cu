@@ -1,0 +1,432 @@
+// Ragged dense layer on sm_103a: Y[M, H] = X[M, I] W[H, I]^T, bf16 in, fp32 out.
+//
+// The workload is the dense layer of "DietCode tests/codegen/
+// test_1_local_padding.py" (test_local_padding docstring), whose point is
+// "local padding": the bounds checks of an imperfectly tiled product belong
+// only to the Fetch stage (out-of-range elements become zeros) and the
+// Writeback stage (out-of-range results are not stored); the Compute stage
+// then runs over whole tiles with no predicates at all.
+//
+// Design (one persistent launch, one CTA per SM, 9 warps):
+//  - tiles of 128 x BN outputs (BN = 64, 128 or 256, chosen per shape),
+//    K in blocks of 64; tiles are dealt round-robin to CTAs.
+//  - Fetch, two forms:
+//      * TMA (I*2 % 16 == 0, 16-byte aligned X and W): warp 0 issues 2-D tiled
+//        loads; rows >= M / H and columns >= I are zero-filled by the TMA unit.
+//      * loader warps (any other I, e.g. I = 770 whose 1540-byte rows no
+//        tensor map can describe): warps 0-3 read 4-byte (or 2-byte) pairs
+//        with plain loads, substitute zeros out of range, and write them into
+//        the same 128-byte-swizzled K-major layout the TMA would produce.
+//  - Compute: warp 4 issues tcgen05.mma M=128 N=BN K=16 into one of two TMEM
+//    accumulators; no bounds logic at all.
+//  - Writeback: warps 5-8 read TMEM 32 columns at a time and store 32 x 32
+//    boxes with TMA (clipped at M and H) when Y rows are 16-byte aligned, or
+//    with coalesced predicated plain stores otherwise.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <string>
+
+#include "csa_internal.h"
+#include "sm103a_ptx.cuh"
+
+namespace csa {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kThreads = 288;
+constexpr int kLoaderWarps = 4;
+constexpr int kMmaWarp = 4;
+constexpr int kFirstEpiWarp = 5;
+constexpr int kStoreBufs = 4;
+constexpr int kBoxBytes = 32 * 32 * 4;
+constexpr int kStagingBytes = 4 * kStoreBufs * kBoxBytes;
+
+struct DenseArgs {
+  int M, I, H, BN;
+  int m_tiles, n_tiles, kblocks, stages;
+  long long num_tiles;
+  uint32_t tma_load, tma_store, vec2;
+  uint32_t idesc;
+  const uint16_t* X;
+  const uint16_t* W;
+  float* Y;
+  int* status;
+  unsigned long long wait_limit_ns;
+  uint32_t stage_bytes, off_staging, off_bars, off_misc, tmem_cols;
+};
+
+template <bool kPair>
+__device__ __forceinline__ uint32_t load_pair(const uint16_t* row, int k, int I) {
+  if (kPair) {
+    // I even and 4-byte aligned rows: k is even, so k < I covers both halves.
+    return k < I ? __ldg(reinterpret_cast<const unsigned int*>(row + k)) : 0u;
+  } else {
+    const uint32_t lo = k < I ? __ldg(reinterpret_cast<const unsigned short*>(row + k)) : 0u;
+    const uint32_t hi = k + 1 < I ? __ldg(reinterpret_cast<const unsigned short*>(row + k + 1)) : 0u;
+    return lo | (hi << 16);
+  }
+}
+
+// One loader warp's share of a rows x 64 operand block: rows w, w+4, w+8, ...
+// Each lane handles bf16 columns k, k+1 (k = kb*64 + 2*lane); the warp writes
+// whole 128-byte rows, so the swizzled stores are bank-conflict free.
+template <bool kPair>
+__device__ __forceinline__ void load_block(const uint16_t* src, int nrows, int row_base, int rows,
+                                           int I, int k, uint32_t tile, uint32_t w,
+                                           uint32_t lane) {
+  for (int i0 = 0; i0 < rows / kLoaderWarps; i0 += 8) {
+    uint32_t v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int rl = (i0 + u) * kLoaderWarps + static_cast<int>(w);
+      const int row = row_base + rl;
+      v[u] = row < nrows ? load_pair<kPair>(src + static_cast<size_t>(row) * I, k, I) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint32_t rl = static_cast<uint32_t>((i0 + u) * kLoaderWarps) + w;
+      st_shared_b32(tile + rl * 128u + ((((lane >> 2) ^ (rl & 7u))) << 4) + ((lane & 3u) << 2),
+                    v[u]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    dense_sm103a_kernel(const __grid_constant__ CUtensorMap tmap_x,
+                        const __grid_constant__ CUtensorMap tmap_w,
+                        const __grid_constant__ CUtensorMap tmap_y, const DenseArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = lane_id();
+
+  const uint32_t bars = base + a.off_bars;
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  auto empty_bar = [&](int s) { return bars + 8u * (a.stages + s); };
+  auto tfull_bar = [&](int s) { return bars + 8u * (2 * a.stages + s); };
+  auto tempty_bar = [&](int s) { return bars + 8u * (2 * a.stages + 2 + s); };
+  const uint32_t drain_bar = bars + 8u * (2 * a.stages + 4);
+  const uint32_t tmem_slot = base + a.off_misc;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + a.off_misc + 4);
+  auto a_tile = [&](int s) { return base + s * a.stage_bytes; };
+  auto b_tile = [&](int s) { return base + s * a.stage_bytes + kBM * 128u; };
+
+  const Watchdog wd{a.wait_limit_ns, a.status, abort_flag};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(full_bar(s), a.tma_load ? 1u : static_cast<uint32_t>(kLoaderWarps));
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(tfull_bar(s), 1);
+      mbar_init(tempty_bar(s), 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, a.tmem_cols);
+    tmem_relinquish();
+    tc_fence_before_sync();
+  }
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = ld_shared_b32(tmem_slot);
+
+  if (warp < kLoaderWarps) {
+    // ------------------------------------------------------------ Fetch --
+    if (a.tma_load) {
+      if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&tmap_x);
+        tma_prefetch_map(&tmap_w);
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued = 0, issued_parity = 0;
+        const uint32_t tx = static_cast<uint32_t>(kBM + a.BN) * 128u;
+        for (long long tile = blockIdx.x; tile < a.num_tiles && !*abort_flag;
+             tile += gridDim.x) {
+          const int mb = static_cast<int>(tile % a.m_tiles);
+          const int nb = static_cast<int>(tile / a.m_tiles);
+          bool ok = true;
+          for (int kb = 0; kb < a.kblocks; ++kb) {
+            if (!mbar_wait(empty_bar(stage), phase ^ 1u, wd, kSiteProducerEmpty)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(full_bar(stage), tx);
+            tma_load_2d(a_tile(stage), &tmap_x, full_bar(stage), kb * kBK, mb * kBM);
+            tma_load_2d(b_tile(stage), &tmap_w, full_bar(stage), kb * kBK, nb * a.BN);
+            issued |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+            if (++stage == a.stages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+        }
+        if (*abort_flag) {
+          for (int s = 0; s < a.stages; ++s) {
+            if (!(issued & (1u << s))) continue;
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_test(full_bar(s), (issued_parity >> s) & 1u) &&
+                   globaltimer_ns() - t0 < a.wait_limit_ns) {
+            }
+          }
+        }
+      }
+    } else {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (long long tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
+        const int mb = static_cast<int>(tile % a.m_tiles);
+        const int nb = static_cast<int>(tile / a.m_tiles);
+        bool ok = true;
+        for (int kb = 0; kb < a.kblocks; ++kb) {
+          if (!mbar_wait_warp(empty_bar(stage), phase ^ 1u, wd, kSiteLoaderEmpty)) {
+            ok = false;
+            break;
+          }
+          const int k = kb * kBK + 2 * static_cast<int>(lane);
+          if (a.vec2) {
+            load_block<true>(a.X, a.M, mb * kBM, kBM, a.I, k, a_tile(stage), warp, lane);
+            load_block<true>(a.W, a.H, nb * a.BN, a.BN, a.I, k, b_tile(stage), warp, lane);
+          } else {
+            load_block<false>(a.X, a.M, mb * kBM, kBM, a.I, k, a_tile(stage), warp, lane);
+            load_block<false>(a.W, a.H, nb * a.BN, a.BN, a.I, k, b_tile(stage), warp, lane);
+          }
+          fence_proxy_async_smem();  // generic smem writes -> visible to tcgen05.mma
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full_bar(stage));
+          if (++stage == a.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------- Compute --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (long long tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, wd, kSiteMmaTmemEmpty)) break;
+        tc_fence_after_sync();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * a.BN);
+        bool ok = true;
+        for (int kb = 0; kb < a.kblocks; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, wd, kSiteMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint32_t off = static_cast<uint32_t>(k) * 32u;
+            umma_bf16(d, umma_desc_k_sw128(a_tile(stage) + off),
+                      umma_desc_k_sw128(b_tile(stage) + off), a.idesc,
+                      (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          umma_commit(empty_bar(stage));
+          if (++stage == a.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(tfull_bar(acc));
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      umma_commit(drain_bar);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_test(drain_bar, 0) && globaltimer_ns() - t0 < a.wait_limit_ns) {
+      }
+    }
+  } else {
+    // -------------------------------------------------------- Writeback --
+    const int q = static_cast<int>(warp & 3u);
+    const uint32_t staging =
+        base + a.off_staging + (warp - kFirstEpiWarp) * kStoreBufs * kBoxBytes;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    uint32_t buf = 0;
+    const int chunks = a.BN / 32;
+    for (long long tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
+      const int mb = static_cast<int>(tile % a.m_tiles);
+      const int nb = static_cast<int>(tile / a.m_tiles);
+      if (!mbar_wait_warp(tfull_bar(acc), acc_phase, wd, kSiteEpilogueFull)) break;
+      tc_fence_after_sync();
+      const uint32_t tcol = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                            static_cast<uint32_t>(acc * a.BN);
+      const int row0 = mb * kBM + q * 32;
+      for (int c = 0; c < chunks; ++c) {
+        uint32_t v[32];
+        tmem_ld_32cols(tcol + static_cast<uint32_t>(c * 32), v);
+        if (c == chunks - 1) {
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(acc));
+        }
+        const int col0 = nb * a.BN + c * 32;
+        if (row0 >= a.M || col0 >= a.H) continue;
+        if (lane == 0) bulk_wait_read<kStoreBufs - 1>();
+        __syncwarp();
+        const uint32_t box = staging + buf * kBoxBytes;
+        buf = (buf + 1u) & (kStoreBufs - 1u);
+        stage_row_sw128(box, lane, v);
+        if (a.tma_store) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmap_y, box, col0, row0);
+            bulk_commit();
+          }
+        } else {
+          __syncwarp();
+          const int col = col0 + static_cast<int>(lane);
+          float* ycol = a.Y + static_cast<size_t>(row0) * a.H + col;
+          for (int rr = 0; rr < 32; ++rr) {
+            const uint32_t val = staged_elem_sw128(box, static_cast<uint32_t>(rr), lane);
+            if (row0 + rr < a.M && col < a.H)
+              ycol[static_cast<size_t>(rr) * a.H] = __uint_as_float(val);
+          }
+        }
+      }
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, a.tmem_cols);
+  }
+}
+
+// Tile width along H: the largest BN whose wave count times tile cost is
+// smallest (tile cost ~ BN plus a fixed per-tile overhead).
+int choose_bn(int M, int H, int sms) {
+  const int m_tiles = (M + kBM - 1) / kBM;
+  int best = 64;
+  long long best_cost = -1;
+  for (int bn : {256, 128, 64}) {
+    const long long tiles = static_cast<long long>(m_tiles) * ((H + bn - 1) / bn);
+    const long long waves = (tiles + sms - 1) / sms;
+    const long long cost = waves * (bn + 32);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+}  // namespace
+
+int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
+                 cudaStream_t stream, const DeviceInfo& dev, std::string& err) {
+  const uintptr_t px = reinterpret_cast<uintptr_t>(X), pw = reinterpret_cast<uintptr_t>(W),
+                  py = reinterpret_cast<uintptr_t>(Y);
+  if (px % 2 || pw % 2 || py % 4) {
+    err = "dense_xwt: X and W must be 2-byte aligned and Y 4-byte aligned";
+    return CSA_ERR_ALIGN;
+  }
+  DenseArgs a{};
+  a.M = M;
+  a.I = I;
+  a.H = H;
+  a.BN = choose_bn(M, H, dev.sm_count);
+  a.m_tiles = (M + kBM - 1) / kBM;
+  a.n_tiles = (H + a.BN - 1) / a.BN;
+  a.kblocks = (I + kBK - 1) / kBK;
+  a.num_tiles = static_cast<long long>(a.m_tiles) * a.n_tiles;
+  a.tma_load = ((static_cast<long long>(I) * 2) % 16 == 0 && px % 16 == 0 && pw % 16 == 0) ? 1u : 0u;
+  a.tma_store = ((static_cast<long long>(H) * 4) % 16 == 0 && py % 16 == 0) ? 1u : 0u;
+  a.vec2 = (I % 2 == 0 && px % 4 == 0 && pw % 4 == 0) ? 1u : 0u;
+  a.idesc = idesc_bf16_f32(kBM, a.BN);
+  a.X = static_cast<const uint16_t*>(X);
+  a.W = static_cast<const uint16_t*>(W);
+  a.Y = Y;
+  a.status = dev.status_word;
+  a.wait_limit_ns = wait_limit_ns();
+  a.tmem_cols = static_cast<uint32_t>(2 * a.BN);
+
+  a.stage_bytes = static_cast<uint32_t>(kBM + a.BN) * 128u;
+  const int fixed = kStagingBytes + 1024 + 1024;
+  a.stages = std::min(4, (dev.max_smem_optin - fixed) / static_cast<int>(a.stage_bytes));
+  if (a.stages < 2) {
+    err = "dense_xwt: not enough shared memory";
+    return CSA_ERR_UNSUPPORTED;
+  }
+  a.off_staging = static_cast<uint32_t>(a.stages) * a.stage_bytes;
+  a.off_bars = a.off_staging + kStagingBytes;
+  a.off_misc = a.off_bars + 8u * static_cast<uint32_t>(2 * a.stages + 5);
+  const size_t smem = a.off_misc + 16 + 1024;
+
+  CUtensorMap map_x, map_w, map_y;
+  std::memset(&map_x, 0, sizeof map_x);
+  std::memset(&map_w, 0, sizeof map_w);
+  std::memset(&map_y, 0, sizeof map_y);
+  if (a.tma_load) {
+    const uint64_t dx[2] = {static_cast<uint64_t>(I), static_cast<uint64_t>(M)};
+    const uint64_t dw[2] = {static_cast<uint64_t>(I), static_cast<uint64_t>(H)};
+    const uint64_t st[1] = {static_cast<uint64_t>(I) * 2};
+    const uint32_t bx[2] = {kBK, kBM};
+    const uint32_t bw[2] = {kBK, static_cast<uint32_t>(a.BN)};
+    int rc = encode_tiled(&map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, dx, st, bx,
+                          CU_TENSOR_MAP_SWIZZLE_128B, err);
+    if (rc != CSA_OK) return rc;
+    rc = encode_tiled(&map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, dw, st, bw,
+                      CU_TENSOR_MAP_SWIZZLE_128B, err);
+    if (rc != CSA_OK) return rc;
+  }
+  if (a.tma_store) {
+    const uint64_t dy[2] = {static_cast<uint64_t>(H), static_cast<uint64_t>(M)};
+    const uint64_t st[1] = {static_cast<uint64_t>(H) * 4};
+    const uint32_t by[2] = {32, 32};
+    int rc = encode_tiled(&map_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, Y, dy, st, by,
+                          CU_TENSOR_MAP_SWIZZLE_128B, err);
+    if (rc != CSA_OK) return rc;
+  }
+
+  cudaError_t e = cudaFuncSetAttribute(dense_sm103a_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) {
+    err = std::string("dense_xwt: cudaFuncSetAttribute: ") + cudaGetErrorString(e);
+    return CSA_ERR_LAUNCH;
+  }
+  const long long grid = std::min<long long>(a.num_tiles, dev.sm_count);
+  dense_sm103a_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(map_x, map_w,
+                                                                               map_y, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    err = std::string("dense_xwt: launch: ") + cudaGetErrorString(e);
+    return CSA_ERR_LAUNCH;
+  }
+  return CSA_OK;
+}
+
+}  // namespace csa

@@ -1,0 +1,436 @@
+// Causal triangular score product on sm_103a.
+//
+//   out[b][h][t][t2] = (Q[b][h][t][:] . K[b][h][t2][:]) * (1/sqrt(HS))  for t2 <= t
+//   out[b][h][t][t2] = mask                                            for t2 > t
+//
+// as defined by the CPU referee of "llm.c dev/cuda/trimat_forward.cu"
+// (trimul_cpu, Chapter I), reading Q and K in place from the packed
+// (B, T, 3, NH, HS) tensor (trimul_global's q/k pointers, Chapter II) with no
+// permute pass.
+//
+// Design (one persistent launch, one CTA per SM, 6 warps):
+//  - tile space: for every (b, h) the ceil(T/128)^2 output tiles of 128 x 128;
+//    tiles with t2-tile <= t-tile are "lower" (MMA + epilogue), the others are
+//    "fill" tiles that only receive the mask pattern. In lower-only mode the
+//    fill tiles are not enumerated at all. Tiles are dealt round-robin to CTAs.
+//  - warp 0 (one lane): TMA producer. A 4-D tensor map (HS, 3*NH, T, B) over
+//    the packed QKV addresses the query of head h at index h and its key at
+//    NH + h; rows past T and columns past HS arrive zero-filled. Q and K tiles
+//    land in a multi-stage ring in the 128-byte-swizzled K-major layout.
+//  - warp 1 (one lane): tcgen05.mma issuer, M=128 N=128 K=16, bf16 x bf16 ->
+//    fp32 into one of two TMEM accumulators (256 columns), so the epilogue of
+//    one tile overlaps the MMA of the next.
+//  - warps 2..5: epilogue. Each warp owns 32 rows (its TMEM lane quarter):
+//    tcgen05.ld 32 columns, multiply by 1/sqrt(HS), write the mask above the
+//    diagonal on diagonal tiles, stage through swizzled shared memory and
+//    issue 32 x 32 TMA stores (clipped at T). Fill tiles are TMA-stored from a
+//    resident 4 KB mask box. When T % 4 != 0 the output rows are not 16-byte
+//    aligned, so the same staged data is written with coalesced plain stores.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <string>
+
+#include "csa_internal.h"
+#include "sm103a_ptx.cuh"
+
+namespace csa {
+namespace {
+
+constexpr int kTile = 128;          // output tile edge
+constexpr int kChunkElems = 64;     // bf16 per 128-byte swizzle row
+constexpr int kChunkBytes = kTile * 128;  // one 128-row x 64-element operand chunk
+constexpr int kThreads = 192;
+constexpr int kStoreBufs = 4;       // staging boxes per epilogue warp
+constexpr int kBoxBytes = 32 * 32 * 4;
+constexpr int kStagingBytes = 4 * kStoreBufs * kBoxBytes;
+constexpr int kTmemCols = 2 * kTile;
+constexpr uint32_t kIdesc = idesc_bf16_f32(kTile, kTile);
+
+struct TrimulArgs {
+  int T, NH, BH, Tt;
+  int kchunks, ksteps, stages;
+  long long num_tiles;
+  float scale;
+  uint32_t mask_bits;
+  uint32_t lower_only;
+  uint32_t tma_store;
+  float* out;
+  int* status;
+  unsigned long long wait_limit_ns;
+  int inject;
+  uint32_t stage_bytes, off_staging, off_mask, off_bars, off_misc;
+};
+
+__device__ __forceinline__ void decode_tile(long long id, const TrimulArgs& a, int& bh, int& ti,
+                                            int& tj) {
+  if (!a.lower_only) {
+    const long long per = static_cast<long long>(a.Tt) * a.Tt;
+    bh = static_cast<int>(id / per);
+    const int r = static_cast<int>(id - static_cast<long long>(bh) * per);
+    ti = r / a.Tt;
+    tj = r - ti * a.Tt;
+  } else {
+    const long long per = static_cast<long long>(a.Tt) * (a.Tt + 1) / 2;
+    bh = static_cast<int>(id / per);
+    const int r = static_cast<int>(id - static_cast<long long>(bh) * per);
+    int i = static_cast<int>((sqrtf(8.0f * static_cast<float>(r) + 1.0f) - 1.0f) * 0.5f);
+    while ((i + 1) * (i + 2) / 2 <= r) ++i;
+    while (i * (i + 1) / 2 > r) --i;
+    ti = i;
+    tj = r - i * (i + 1) / 2;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    trimul_sm103a_kernel(const __grid_constant__ CUtensorMap tmap_qkv,
+                         const __grid_constant__ CUtensorMap tmap_out, const TrimulArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = lane_id();
+
+  const uint32_t bars = base + a.off_bars;
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  auto empty_bar = [&](int s) { return bars + 8u * (a.stages + s); };
+  auto tfull_bar = [&](int s) { return bars + 8u * (2 * a.stages + s); };
+  auto tempty_bar = [&](int s) { return bars + 8u * (2 * a.stages + 2 + s); };
+  const uint32_t drain_bar = bars + 8u * (2 * a.stages + 4);
+  const uint32_t tmem_slot = base + a.off_misc;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + a.off_misc + 4);
+  const uint32_t mask_box = base + a.off_mask;
+  auto q_chunk = [&](int s, int kc) { return base + s * a.stage_bytes + kc * kChunkBytes; };
+  auto k_chunk = [&](int s, int kc) {
+    return base + s * a.stage_bytes + (a.kchunks + kc) * kChunkBytes;
+  };
+
+  const Watchdog wd{a.wait_limit_ns, a.status, abort_flag};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(tfull_bar(s), 1);
+      mbar_init(tempty_bar(s), 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  // The resident mask box that fill tiles are stored from.
+  for (uint32_t w = threadIdx.x; w < kBoxBytes / 4; w += kThreads)
+    st_shared_b32(mask_box + 4u * w, a.mask_bits);
+  fence_proxy_async_smem();
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+    tc_fence_before_sync();
+  }
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = ld_shared_b32(tmem_slot);
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      tma_prefetch_map(&tmap_qkv);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_parity = 0;  // per-stage: loads that may be in flight
+      bool injected = false;
+      const uint32_t tx = static_cast<uint32_t>(a.kchunks) * 2u * kChunkBytes;
+      for (long long tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
+        int bh, ti, tj;
+        decode_tile(tile, a, bh, ti, tj);
+        if (tj > ti) continue;
+        if (!mbar_wait(empty_bar(stage), phase ^ 1u, wd, kSiteProducerEmpty)) break;
+        const int b = bh / a.NH, h = bh - b * a.NH;
+        mbar_arrive_expect_tx(full_bar(stage), tx);
+        if (a.inject && blockIdx.x == 0 && !injected) {
+          injected = true;  // withhold this tile's loads: its consumer's wait must run out
+          issued &= ~(1u << stage);
+        } else {
+          for (int kc = 0; kc < a.kchunks; ++kc) {
+            tma_load_4d(q_chunk(stage, kc), &tmap_qkv, full_bar(stage), kc * kChunkElems, h,
+                        ti * kTile, b);
+            tma_load_4d(k_chunk(stage, kc), &tmap_qkv, full_bar(stage), kc * kChunkElems,
+                        a.NH + h, tj * kTile, b);
+          }
+          issued |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        }
+        if (++stage == a.stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (*abort_flag) {
+        // Let every load still in flight land before shared memory goes away.
+        const Watchdog drain{a.wait_limit_ns, a.status, abort_flag};
+        for (int s = 0; s < a.stages; ++s) {
+          if (!(issued & (1u << s))) continue;
+          const uint32_t par = (issued_parity >> s) & 1u;
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_test(full_bar(s), par) && globaltimer_ns() - t0 < drain.limit_ns) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (long long tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
+        int bh, ti, tj;
+        decode_tile(tile, a, bh, ti, tj);
+        if (tj > ti) continue;
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, wd, kSiteMmaTmemEmpty)) break;
+        tc_fence_after_sync();
+        if (!mbar_wait(full_bar(stage), phase, wd, kSiteMmaFull)) break;
+        tc_fence_after_sync();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kTile);
+        for (int k = 0; k < a.ksteps; ++k) {
+          const uint32_t off = static_cast<uint32_t>(k & 3) * 32u;  // 16 bf16 = 32 B along K
+          const uint64_t ad = umma_desc_k_sw128(q_chunk(stage, k >> 2) + off);
+          const uint64_t bd = umma_desc_k_sw128(k_chunk(stage, k >> 2) + off);
+          umma_bf16(d, ad, bd, kIdesc, k > 0 ? 1u : 0u);
+        }
+        umma_commit(empty_bar(stage));  // operands consumed -> slot free
+        umma_commit(tfull_bar(acc));    // accumulator ready -> epilogue
+        if (++stage == a.stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // All MMAs of this thread complete before TMEM can be released.
+      umma_commit(drain_bar);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_test(drain_bar, 0) && globaltimer_ns() - t0 < a.wait_limit_ns) {
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue --
+    const int q = static_cast<int>(warp & 3u);  // TMEM lane quarter this warp may read
+    const uint32_t staging = base + a.off_staging + (warp - 2u) * kStoreBufs * kBoxBytes;
+    const int T = a.T;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    uint32_t buf = 0;
+    for (long long tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
+      int bh, ti, tj;
+      decode_tile(tile, a, bh, ti, tj);
+      const int row0 = ti * kTile + q * 32;
+      if (tj > ti) {
+        // Fill tile: mask pattern only (full mode).
+        if (row0 >= T) continue;
+        if (a.tma_store) {
+          if (lane == 0) {
+            for (int c = 0; c < 4; ++c) {
+              const int col0 = tj * kTile + c * 32;
+              if (col0 < T) {
+                tma_store_3d(&tmap_out, mask_box, col0, row0, bh);
+                bulk_commit();
+              }
+            }
+          }
+        } else {
+          float* orow = a.out + (static_cast<size_t>(bh) * T + row0) * T;
+          const float m = __uint_as_float(a.mask_bits);
+          for (int rr = 0; rr < 32 && row0 + rr < T; ++rr) {
+            for (int c = 0; c < 4; ++c) {
+              const int col = tj * kTile + c * 32 + static_cast<int>(lane);
+              if (col < T) orow[static_cast<size_t>(rr) * T + col] = m;
+            }
+          }
+        }
+        continue;
+      }
+
+      if (!mbar_wait_warp(tfull_bar(acc), acc_phase, wd, kSiteEpilogueFull)) break;
+      tc_fence_after_sync();
+      const uint32_t tcol =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kTile);
+      const bool diag = (ti == tj);
+      const int r = row0 + static_cast<int>(lane);
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld_32cols(tcol + static_cast<uint32_t>(c * 32), v);
+        if (c == 3) {
+          // This warp's rows of the accumulator are in registers: release it.
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(acc));
+        }
+        const int col0 = tj * kTile + c * 32;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          uint32_t bits = __float_as_uint(__uint_as_float(v[e]) * a.scale);
+          if (diag && col0 + e > r) bits = a.mask_bits;
+          v[e] = bits;
+        }
+        if (row0 >= T || col0 >= T) continue;  // box wholly past the end (tail tile)
+
+        // 0: skip, 1: TMA store, 2: plain stores (all), 3: plain stores, t2 <= t only
+        int mode = a.tma_store ? 1 : 2;
+        if (a.lower_only && diag) {
+          if (col0 > row0 + 31) mode = 0;
+          else if (col0 + 31 > row0) mode = 3;
+        }
+        if (mode == 0) continue;
+
+        if (lane == 0) bulk_wait_read<kStoreBufs - 1>();
+        __syncwarp();
+        const uint32_t box = staging + buf * kBoxBytes;
+        buf = (buf + 1u) & (kStoreBufs - 1u);
+        stage_row_sw128(box, lane, v);
+        if (mode == 1) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tmap_out, box, col0, row0, bh);
+            bulk_commit();
+          }
+        } else {
+          __syncwarp();
+          const int col = col0 + static_cast<int>(lane);
+          float* ocol = a.out + (static_cast<size_t>(bh) * T + row0) * T + col;
+          for (int rr = 0; rr < 32; ++rr) {
+            const int row = row0 + rr;
+            const bool ok = row < T && col < T && (mode == 2 || col <= row);
+            const uint32_t val = staged_elem_sw128(box, static_cast<uint32_t>(rr), lane);
+            if (ok) ocol[static_cast<size_t>(rr) * T] = __uint_as_float(val);
+          }
+        }
+      }
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace
+
+int trimul_launch(float* out, const void* qkv, int B, int T, int C, int NH, uint32_t mask_bits,
+                  uint32_t flags, cudaStream_t stream, const DeviceInfo& dev, std::string& err) {
+  const int HS = C / NH;
+  if (HS % 8 != 0) {
+    err = "trimul_forward: HS = C/NH must be a multiple of 8 (TMA row pitch of a head)";
+    return CSA_ERR_ALIGN;
+  }
+  if (HS > 256) {
+    err = "trimul_forward: HS > 256 is not supported";
+    return CSA_ERR_UNSUPPORTED;
+  }
+  if (reinterpret_cast<uintptr_t>(qkv) % 16 != 0 || reinterpret_cast<uintptr_t>(out) % 4 != 0) {
+    err = "trimul_forward: qkv must be 16-byte aligned and out 4-byte aligned";
+    return CSA_ERR_ALIGN;
+  }
+  const long long BH = static_cast<long long>(B) * NH;
+  if (BH > (1LL << 30) || static_cast<long long>(T) > (1LL << 30)) {
+    err = "trimul_forward: B*NH or T too large";
+    return CSA_ERR_SHAPE;
+  }
+  const bool lower_only = (flags & CSA_TRIMUL_LOWER_ONLY) != 0;
+
+  TrimulArgs a{};
+  a.T = T;
+  a.NH = NH;
+  a.BH = static_cast<int>(BH);
+  a.Tt = (T + kTile - 1) / kTile;
+  a.kchunks = (HS + kChunkElems - 1) / kChunkElems;
+  a.ksteps = (HS + 15) / 16;
+  a.num_tiles = BH * (lower_only ? static_cast<long long>(a.Tt) * (a.Tt + 1) / 2
+                                 : static_cast<long long>(a.Tt) * a.Tt);
+  a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(HS)));
+  a.mask_bits = mask_bits;
+  a.lower_only = lower_only ? 1u : 0u;
+  a.tma_store = (T % 4 == 0 && reinterpret_cast<uintptr_t>(out) % 16 == 0) ? 1u : 0u;
+  a.out = out;
+  a.status = dev.status_word;
+  a.wait_limit_ns = wait_limit_ns();
+  a.inject = take_inject() ? 1 : 0;
+
+  // Shared memory: operand ring | staging boxes | mask box | barriers | misc.
+  a.stage_bytes = static_cast<uint32_t>(a.kchunks) * 2u * kChunkBytes;
+  const int fixed = kStagingBytes + kBoxBytes + 1024 /*bars+misc*/ + 1024 /*align slack*/;
+  const int budget = dev.max_smem_optin - fixed;
+  a.stages = std::min(4, budget / static_cast<int>(a.stage_bytes));
+  if (a.stages < 1) {
+    err = "trimul_forward: not enough shared memory for one operand stage";
+    return CSA_ERR_UNSUPPORTED;
+  }
+  a.off_staging = static_cast<uint32_t>(a.stages) * a.stage_bytes;
+  a.off_mask = a.off_staging + kStagingBytes;
+  a.off_bars = a.off_mask + kBoxBytes;
+  a.off_misc = a.off_bars + 8u * static_cast<uint32_t>(2 * a.stages + 5);
+  const size_t smem = a.off_misc + 16 + 1024;
+
+  CUtensorMap map_qkv, map_out;
+  {
+    const uint64_t dims[4] = {static_cast<uint64_t>(HS), static_cast<uint64_t>(3 * NH),
+                              static_cast<uint64_t>(T), static_cast<uint64_t>(B)};
+    const uint64_t strides[3] = {static_cast<uint64_t>(HS) * 2, static_cast<uint64_t>(C) * 6,
+                                 static_cast<uint64_t>(T) * C * 6};
+    const uint32_t box[4] = {kChunkElems, 1, kTile, 1};
+    int rc = encode_tiled(&map_qkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, qkv, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B, err);
+    if (rc != CSA_OK) return rc;
+  }
+  if (a.tma_store) {
+    const uint64_t dims[3] = {static_cast<uint64_t>(T), static_cast<uint64_t>(T),
+                              static_cast<uint64_t>(BH)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(T) * 4,
+                                 static_cast<uint64_t>(T) * static_cast<uint64_t>(T) * 4};
+    const uint32_t box[3] = {32, 32, 1};
+    int rc = encode_tiled(&map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, out, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B, err);
+    if (rc != CSA_OK) return rc;
+  } else {
+    std::memset(&map_out, 0, sizeof map_out);
+  }
+
+  cudaError_t e = cudaFuncSetAttribute(trimul_sm103a_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) {
+    err = std::string("trimul_forward: cudaFuncSetAttribute: ") + cudaGetErrorString(e);
+    return CSA_ERR_LAUNCH;
+  }
+  const long long grid = std::min<long long>(a.num_tiles, dev.sm_count);
+  trimul_sm103a_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(map_qkv, map_out,
+                                                                                a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    err = std::string("trimul_forward: launch: ") + cudaGetErrorString(e);
+    return CSA_ERR_LAUNCH;
+  }
+  return CSA_OK;
+}
+
+}  // namespace csa

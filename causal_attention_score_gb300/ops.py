@@ -1,0 +1,100 @@
+"""Python binding of the C ABI: argument marshalling only.
+
+Every function checks that the tensors match what the C entry point expects
+(device, dtype, contiguity, size), then passes raw pointers and the current
+torch CUDA stream. All computation happens in the library's kernels.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+from ._lib import CSA_MASK_NAN, CSA_MASK_NEG_INF, CSA_TRIMUL_FULL, CSA_TRIMUL_LOWER_ONLY
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, numel: int) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.numel() != numel:
+        raise ValueError(f"{name} has {t.numel()} elements, expected {numel}")
+
+
+def _mask_bits(mask) -> int:
+    if mask in ("nan", None):
+        return CSA_MASK_NAN
+    if mask in ("-inf", "neg_inf"):
+        return CSA_MASK_NEG_INF
+    return int(mask) & 0xFFFFFFFF
+
+
+def trimul_forward(out: torch.Tensor, qkv: torch.Tensor, B: int, T: int, C: int, NH: int,
+                   mask="nan", lower_only: bool = False, stream=None) -> None:
+    """Causal scores into ``out`` (fp32, (B, NH, T, T)) from packed ``qkv``
+    (bf16, (B, T, 3, NH, HS)); see trimul_forward_ex in include/csa.h."""
+    _need(qkv, "qkv", torch.bfloat16, B * T * 3 * C)
+    _need(out, "out", torch.float32, B * NH * T * T)
+    flags = CSA_TRIMUL_LOWER_ONLY if lower_only else CSA_TRIMUL_FULL
+    rc = _lib.load().trimul_forward_ex(out.data_ptr(), qkv.data_ptr(), B, T, C, NH,
+                                       _mask_bits(mask), flags, _stream_ptr(stream))
+    _lib.check(rc, "trimul_forward")
+
+
+def dense_xwt(Y: torch.Tensor, X: torch.Tensor, W: torch.Tensor, M: int, I: int, H: int,
+              stream=None) -> None:
+    """Y = X W^T into ``Y`` (fp32 [M, H]) from bf16 X [M, I] and W [H, I]."""
+    _need(X, "X", torch.bfloat16, M * I)
+    _need(W, "W", torch.bfloat16, H * I)
+    _need(Y, "Y", torch.float32, M * H)
+    rc = _lib.load().dense_xwt_ex(Y.data_ptr(), X.data_ptr(), W.data_ptr(), M, I, H,
+                                  _stream_ptr(stream))
+    _lib.check(rc, "dense_xwt")
+
+
+def trimul(qkv: torch.Tensor, mask="nan", lower_only: bool = False, stream=None) -> torch.Tensor:
+    """Allocating form: qkv (B, T, 3, NH, HS) bf16 -> scores (B, NH, T, T) fp32."""
+    B, T, three, NH, HS = qkv.shape
+    if three != 3:
+        raise ValueError("qkv must have shape (B, T, 3, NH, HS)")
+    out = torch.empty((B, NH, T, T), dtype=torch.float32, device=qkv.device)
+    trimul_forward(out, qkv, B, T, NH * HS, NH, mask=mask, lower_only=lower_only, stream=stream)
+    return out
+
+
+def dense(X: torch.Tensor, W: torch.Tensor, stream=None) -> torch.Tensor:
+    """Allocating form: X [M, I], W [H, I] bf16 -> Y = X W^T fp32 [M, H]."""
+    M, I = X.shape
+    H, I2 = W.shape
+    if I2 != I:
+        raise ValueError("X and W disagree on I")
+    Y = torch.empty((M, H), dtype=torch.float32, device=X.device)
+    dense_xwt(Y, X, W, M, I, H, stream=stream)
+    return Y
+
+
+def get_status(stream=None) -> int:
+    """Synchronise ``stream`` and return/clear the device status word (0 = ok)."""
+    return int(_lib.load().csa_get_status(_stream_ptr(stream)))
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    _lib.load().csa_set_wait_limit_ns(int(ns))
+
+
+def debug_inject(enable: bool = True) -> None:
+    _lib.load().csa_debug_inject(1 if enable else 0)
+
+
+def version() -> str:
+    return _lib.load().csa_version().decode()

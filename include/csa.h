@@ -1,0 +1,149 @@
+/*
+ * csa.h -- C ABI of the GB300 (sm_103a) causal-attention-score library,
+ * libcsa_gb300.so.
+ *
+ * Two products, each one persistent tcgen05/TMA kernel launch per call:
+ *
+ *  trimul_forward  the causal triangular score product of
+ *                  "llm.c dev/cuda/trimat_forward.cu" (the CPU referee
+ *                  trimul_cpu, Chapter I; the lower-tile skip of trimul_global,
+ *                  Chapter II):
+ *                    out[b][h][t][t2] = (Q[b][h][t][:] . K[b][h][t2][:]) / sqrt(HS)
+ *                                       for t2 <= t, the mask value for t2 > t,
+ *                  with Q[b][h][t][d] = qkv[b][t][0][h][d] and
+ *                       K[b][h][t2][d] = qkv[b][t2][1][h][d].
+ *
+ *  dense_xwt       the dense layer of "DietCode tests/codegen/
+ *                  test_1_local_padding.py" (test_local_padding docstring):
+ *                    Y[i][j] = sum_k X[i][k] * W[j][k]   (Y = X W^T)
+ *                  for any M, I, H >= 1; tails are handled only where data is
+ *                  fetched (zero fill) and written back (clipped), never in the
+ *                  compute stage ("local padding").
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers named as device pointers must point to memory of the current CUDA
+ *    device (cudaMalloc'd or torch-allocated). The caller owns every buffer;
+ *    the library never allocates, frees or retains caller memory.
+ *  - bf16 inputs are passed as `const void*` to raw 16-bit bfloat16 values.
+ *  - Outputs are fp32 and fully overwritten (no read-modify-write).
+ *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ *    stream. Calls are asynchronous on that stream; argument errors are
+ *    returned synchronously before anything is launched.
+ *  - Return value: CSA_OK (0) or a negative csa_status. A failed call launches
+ *    nothing and leaves the output untouched; csa_last_error() then describes it.
+ *  - The library keeps one device status word per device. A kernel whose
+ *    bounded wait ran out records CSA_ERR_TIMEOUT there and returns early
+ *    (its output is then incomplete); csa_get_status() reports and clears it.
+ *  - Thread safety: entry points may be called from several host threads; the
+ *    error string is per thread.
+ */
+#ifndef CSA_GB300_H
+#define CSA_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int csa_status;
+
+#define CSA_OK                 0
+#define CSA_ERR_NULL          -1  /* a required pointer is NULL */
+#define CSA_ERR_SHAPE         -2  /* a size is <= 0, C % NH != 0, or an index overflows */
+#define CSA_ERR_ALIGN         -3  /* a pointer or stride breaks the 16-byte rule below */
+#define CSA_ERR_UNSUPPORTED   -4  /* a size beyond what the kernel implements (HS > 256) */
+#define CSA_ERR_ARCH          -5  /* the current device is not sm_103 (GB300) */
+#define CSA_ERR_LAUNCH        -6  /* the kernel launch failed (see csa_last_error) */
+#define CSA_ERR_TIMEOUT       -7  /* a device-side bounded wait ran out (csa_get_status) */
+#define CSA_ERR_CUDA          -8  /* a CUDA runtime/driver call failed (no device, ...) */
+
+/* Causal mask bit patterns for the upper triangle (t2 > t). The page writes
+ * NAN (the float quiet NaN, 0x7FC00000) and notes -inf would also do. */
+#define CSA_MASK_NAN          0x7FC00000u
+#define CSA_MASK_NEG_INF      0xFF800000u
+
+/* trimul_forward_ex flags. */
+#define CSA_TRIMUL_FULL        0u  /* write every element: scores below, mask above */
+#define CSA_TRIMUL_LOWER_ONLY  1u  /* write only t2 <= t; leave t2 > t untouched
+                                      (what the page's GPU kernels do, tri4's
+                                      "don't write above the diagonal") */
+
+/*
+ * trimul_forward -- causal score product, NaN mask, default stream.
+ *
+ *   out  device, fp32, (B, NH, T, T) contiguous, fully overwritten.
+ *   qkv  device, bf16, (B, T, 3, NH, HS) contiguous, HS = C / NH; read only.
+ *   B, T, C, NH >= 1, C % NH == 0.
+ *
+ * Requirements (else CSA_ERR_ALIGN / CSA_ERR_UNSUPPORTED): qkv and out 16-byte
+ * aligned; HS % 8 == 0 (the TMA row pitch of a head is HS*2 bytes and must be
+ * a multiple of 16); HS <= 256. Any T >= 1 is accepted: rows and columns past
+ * T are zero-filled on fetch and clipped on store. Scores are computed as
+ * fp32 accumulations of exact bf16 products, then multiplied by the fp32
+ * value of 1/sqrt(HS).
+ */
+csa_status trimul_forward(float* out, const void* qkv, int B, int T, int C, int NH);
+
+/*
+ * trimul_forward_ex -- as trimul_forward, with
+ *   mask_bits  the 32-bit pattern written above the diagonal (CSA_MASK_NAN,
+ *              CSA_MASK_NEG_INF or any other pattern);
+ *   flags      CSA_TRIMUL_FULL or CSA_TRIMUL_LOWER_ONLY;
+ *   stream     cudaStream_t (void*), NULL = default stream.
+ */
+csa_status trimul_forward_ex(float* out, const void* qkv, int B, int T, int C, int NH,
+                             uint32_t mask_bits, uint32_t flags, void* stream);
+
+/*
+ * dense_xwt -- Y = X W^T, default stream.
+ *
+ *   Y  device, fp32, [M, H] row-major, fully overwritten.
+ *   X  device, bf16, [M, I] row-major; W device, bf16, [H, I] row-major.
+ *   M, I, H >= 1, any values (no tile-multiple requirement).
+ *
+ * X and W need only 2-byte alignment: when I*2 is a multiple of 16 and both
+ * are 16-byte aligned, tiles are fetched by TMA; otherwise loader warps fetch
+ * them with plain loads. Y is written by TMA when H*4 is a multiple of 16 and
+ * Y is 16-byte aligned (4-byte alignment required otherwise).
+ * Sums are fp32 accumulations of exact bf16 products.
+ */
+csa_status dense_xwt(float* Y, const void* X, const void* W, int M, int I, int H);
+
+/* dense_xwt_ex -- as dense_xwt on `stream` (cudaStream_t as void*). */
+csa_status dense_xwt_ex(float* Y, const void* X, const void* W, int M, int I, int H,
+                        void* stream);
+
+/*
+ * csa_get_status -- synchronises `stream`, then returns and clears the current
+ * device's status word: CSA_OK, or CSA_ERR_TIMEOUT if a kernel's bounded wait
+ * ran out since the last call. Returns CSA_ERR_CUDA if synchronisation fails.
+ */
+csa_status csa_get_status(void* stream);
+
+/* csa_status_string -- static description of a status code (never NULL). */
+const char* csa_status_string(csa_status s);
+
+/* csa_last_error -- text of the last failure on this host thread ("" if none). */
+const char* csa_last_error(void);
+
+/* csa_version -- library version string, e.g. "0.1.0 sm_103a". */
+const char* csa_version(void);
+
+/*
+ * Watchdog controls, for tests of the failure path (no GPU fault involved).
+ *
+ * csa_set_wait_limit_ns -- upper bound, in nanoseconds of %globaltimer, on
+ *   every spin-wait inside the kernels (default 2e9 = 2 s; 0 restores it).
+ * csa_debug_inject -- when nonzero, the next trimul_forward_ex launch withholds
+ *   one tile load, so its consumer's bounded wait runs out and the kernel
+ *   records CSA_ERR_TIMEOUT and returns. Consumed by that launch.
+ */
+void csa_set_wait_limit_ns(uint64_t ns);
+void csa_debug_inject(int enable);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA_GB300_H */

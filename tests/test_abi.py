@@ -1,0 +1,88 @@
+"""The C ABI on the CPU: the library loads, exports every symbol include/csa.h
+declares, and rejects invalid arguments before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from causal_attention_score_gb300 import _lib, build_lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_lib.build()
+    return _lib.load()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "csa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([A-Za-z_]\w*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert {"trimul_forward", "trimul_forward_ex", "dense_xwt", "dense_xwt_ex",
+            "csa_get_status"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in csa.h but not exported"
+        assert n in _lib.SIGNATURES, f"{n} has no ctypes signature in the binding"
+
+
+def test_status_strings(lib):
+    for code in range(-8, 1):
+        assert lib.csa_status_string(code)
+    assert lib.csa_version().decode().endswith("sm_103a")
+
+
+@pytest.mark.parametrize("args,code", [
+    ((None, 16, 1, 1, 8, 1), _lib.CSA_ERR_NULL),
+    ((16, None, 1, 1, 8, 1), _lib.CSA_ERR_NULL),
+    ((16, 16, 0, 1, 8, 1), _lib.CSA_ERR_SHAPE),
+    ((16, 16, 1, 0, 8, 1), _lib.CSA_ERR_SHAPE),
+    ((16, 16, 1, 1, 10, 3), _lib.CSA_ERR_SHAPE),       # C % NH != 0
+    ((16, 16, 1, 1, 12, 1), _lib.CSA_ERR_ALIGN),       # HS = 12
+    ((16, 16, 1, 1, 512, 1), _lib.CSA_ERR_UNSUPPORTED),  # HS = 512
+    ((16, 8, 1, 1, 64, 1), _lib.CSA_ERR_ALIGN),        # qkv not 16-byte aligned
+    ((18, 16, 1, 1, 64, 1), _lib.CSA_ERR_ALIGN),       # out not 4-byte aligned
+])
+def test_trimul_argument_errors(lib, args, code):
+    assert lib.trimul_forward(*args) == code
+    assert lib.csa_last_error()
+
+
+def test_trimul_unknown_flags(lib):
+    assert lib.trimul_forward_ex(16, 16, 1, 1, 64, 1, 0, 8, None) == _lib.CSA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("args,code", [
+    ((None, 16, 16, 1, 1, 1), _lib.CSA_ERR_NULL),
+    ((16, 16, 16, 0, 1, 1), _lib.CSA_ERR_SHAPE),
+    ((16, 16, 16, 1, -1, 1), _lib.CSA_ERR_SHAPE),
+    ((16, 17, 16, 1, 1, 1), _lib.CSA_ERR_ALIGN),
+    ((18, 16, 16, 1, 1, 1), _lib.CSA_ERR_ALIGN),
+])
+def test_dense_argument_errors(lib, args, code):
+    assert lib.dense_xwt(*args) == code
+
+
+def test_no_device_is_an_error_not_a_crash(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    assert lib.trimul_forward(1024, 1024, 1, 64, 128, 2) == _lib.CSA_ERR_CUDA
+    assert lib.dense_xwt(1024, 1024, 1024, 4, 4, 4) == _lib.CSA_ERR_CUDA
+    assert lib.csa_get_status(None) == _lib.CSA_ERR_CUDA
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    import causal_attention_score_gb300 as csa
+    qkv = torch.zeros((1, 4, 3, 1, 8), dtype=torch.bfloat16)
+    out = torch.zeros((1, 1, 4, 4))
+    with pytest.raises(ValueError):
+        csa.trimul_forward(out, qkv, 1, 4, 8, 1)

@@ -1,0 +1,95 @@
+"""Parity of the CUDA ragged dense layer Y = X W^T against the fp64 oracle (GPU)."""
+import numpy as np
+import pytest
+import torch
+
+import causal_attention_score_gb300 as csa
+from causal_attention_score_gb300 import synth
+from gpu_util import assert_close, f32_bits, poisoned
+
+pytestmark = pytest.mark.gpu
+
+# (M, I, H): the ragged case (M % 128 != 0, I % 4 != 0), the page's H = 2304, TMA-able
+# and non-TMA I, odd I (2-byte loads), H % 4 != 0 (plain stores), tiny and tile-edge sizes.
+SHAPES = [
+    (960, 770, 768),
+    (960, 770, 2304),
+    (1, 8, 1),
+    (17, 770, 768),
+    (130, 776, 200),
+    (128, 64, 128),
+    (129, 65, 129),
+    (33, 21, 7),
+    (7, 300, 5),
+    (64, 768, 3072),
+    (300, 1000, 770),
+    (257, 129, 255),
+]
+
+
+def _run(X, W):
+    M, I = X.shape
+    H = W.shape[0]
+    Y = poisoned((M, H))
+    csa.dense_xwt(Y, X.cuda(), W.cuda(), M, I, H)
+    torch.cuda.synchronize()
+    assert csa.get_status() == 0
+    return Y
+
+
+@pytest.mark.parametrize("M,I,H", SHAPES)
+def test_dense_parity(oracle_lib, M, I, H):
+    X, W = synth.dense_input(synth.DenseShape(M=M, I=I, H=H), seed=M + I + H)
+    ref = oracle_lib.dense(synth.bf16_bits(X).reshape(-1), synth.bf16_bits(W).reshape(-1), M, I, H)
+    Y = _run(X, W)
+    assert_close(Y.cpu().numpy(), ref, f"dense{(M, I, H)}")
+
+
+def test_dense_ragged_case(oracle_lib):
+    """The ragged case: X [960, 770], W [768, 770], seed 0, via the allocating helper."""
+    s = synth.DENSE_RAGGED
+    X, W = synth.dense_input(s, seed=0)
+    ref = oracle_lib.dense(synth.bf16_bits(X).reshape(-1), synth.bf16_bits(W).reshape(-1),
+                           s.M, s.I, s.H)
+    Y = csa.dense(X.cuda(), W.cuda())
+    torch.cuda.synchronize()
+    assert_close(Y.cpu().numpy(), ref, "dense ragged")
+
+
+@pytest.mark.parametrize("M,I,H", [(960, 770, 768), (200, 776, 130), (31, 33, 29)])
+def test_dense_integer_inputs_bit_exact(oracle_lib, M, I, H):
+    rng = np.random.default_rng(M)
+    X = torch.from_numpy(rng.integers(-4, 5, size=(M, I)).astype(np.float32)).to(torch.bfloat16)
+    W = torch.from_numpy(rng.integers(-4, 5, size=(H, I)).astype(np.float32)).to(torch.bfloat16)
+    ref = oracle_lib.dense(synth.bf16_bits(X).reshape(-1), synth.bf16_bits(W).reshape(-1), M, I, H)
+    Y = _run(X, W)
+    assert np.array_equal(Y.cpu().numpy().astype(np.float64), ref)
+
+
+def test_dense_row_independence():
+    """One row computed alone equals that row of the full product (no leakage
+    through the zero-filled tile padding)."""
+    X, W = synth.dense_input(synth.DenseShape(M=333, I=770, H=768), seed=5)
+    Y = _run(X, W)
+    for r in (0, 127, 128, 332):
+        y1 = _run(X[r:r + 1].contiguous(), W)
+        assert torch.equal(y1[0], Y[r])
+
+
+def test_dense_sweep(oracle_lib):
+    """All 32 calls of the dynamic-shape sweep (M = 16*T, T ~ U{1..128}, I=768, H=3072),
+    on sampled rows of each call."""
+    xs, W = synth.dense_sweep_inputs(seed=0)
+    Wd = W.cuda()
+    wbits = synth.bf16_bits(W).reshape(-1)
+    H, I = W.shape
+    rng = np.random.default_rng(0)
+    for i, X in enumerate(xs):
+        M = X.shape[0]
+        Y = poisoned((M, H))
+        csa.dense_xwt(Y, X.cuda(), Wd, M, I, H)
+        torch.cuda.synchronize()
+        rows = np.unique(np.concatenate([[0, M - 1], rng.integers(0, M, size=6)]))
+        ref = oracle_lib.dense_rows(synth.bf16_bits(X).reshape(-1), wbits, M, I, H, rows)
+        assert_close(Y[torch.from_numpy(rows).cuda()].cpu().numpy(), ref, f"sweep call {i} M={M}")
+        assert bool(torch.all(torch.isfinite(Y)))
