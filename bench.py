@@ -1,0 +1,485 @@
+"""Benchmark of the hot path: one step = one causal score product on the GPT-2-small
+shape plus one ragged dense layer, the two products of this library.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Workload (seeded synthetic data, resident in HBM before timing):
+  trimul_forward  QKV bf16 (B=8, T=1024, 3, NH=12, HS=64) N(0,1) seed 0 -> fp32 (8, 12, 1024, 1024)
+                  (the shape of the "llm.c dev/cuda/trimat_forward.cu" main);
+  dense_xwt       X [960, 770], W [768, 770] bf16 uniform[-1,1] seed 0 -> fp32 Y [960, 768]
+                  (B*T = 16*60 and I = 770 of "DietCode ... test_local_padding").
+Metric: useful TFLOP/s = (lower-triangle flops 2*HS*B*NH*T(T+1)/2 + dense flops 2*M*I*H)
+per step / step time. L2 is flushed (256 MiB write) between timed steps, outside the
+timed events. Rank 0 prints one JSON line.
+
+--impl reference times the fp64 CPU oracle (the only other implementation of the
+method; the pages ship no runnable GPU code) on the host cores, on a bounded
+sample of the same workload per step, and prints the same line.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "useful TFLOP/s (lower-triangle FLOPs) and % of GB300 bf16 dense peak"
+UNIT = "TFLOP/s"
+L2_FLUSH_BYTES = 256 * 1024 * 1024
+
+
+# --------------------------------------------------------------- work model --
+
+def trimul_flops(B, T, C, NH):
+    """Useful flops of the causal product: 2*HS per score, lower triangle incl. diagonal."""
+    HS = C // NH
+    return 2 * HS * B * NH * T * (T + 1) // 2
+
+
+def dense_flops(M, I, H):
+    """2*M*I*H, the count "DietCode ... test_local_padding" divides by time."""
+    return 2 * M * I * H
+
+
+def trimul_algorithmic_bytes(B, T, C, NH, lower_only=False):
+    """Minimum HBM traffic of one trimul_forward: every output element written once
+    (fp32), Q and K read once (bf16); V is never touched."""
+    out = B * NH * (T * (T + 1) // 2 if lower_only else T * T) * 4
+    qk = 2 * B * T * C * 2
+    return out + qk
+
+
+def dense_algorithmic_bytes(M, I, H):
+    return (M * I + H * I) * 2 + M * H * 4
+
+
+def tiled_traffic(M, N, K, bM, bN, bK):
+    """Global-memory element loads and writes of a tiled matmul that fetches an
+    A tile and a B tile per (M, N, K) tile step and writes each output tile once
+    ("kernl tutorial 1 - tiled matmul": loads (bM*bK + bK*bN) * K/bK * N/bN * M/bM,
+    writes M*N)."""
+    steps = math.ceil(M / bM) * math.ceil(N / bN) * math.ceil(K / bK)
+    return (bM * bK + bK * bN) * steps, M * N
+
+
+# ---------------------------------------------------------- distributed --
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = os.environ.get("CSA_BENCH_BACKEND", "nccl")
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest value of x over all ranks (the job's elapsed time)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks --
+
+_REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+            0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+            0x80: "hw_power_brake_slowdown", 0x100: "display_clocks"}
+
+
+class ClockSampler:
+    """Reads SM clock and clock-event reasons through NVML (read-only) in a thread."""
+
+    def __init__(self, index: int, period_s: float = 0.002):
+        self.period = period_s
+        self.samples = []
+        self.reasons = 0
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._ok = False
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            self.handle = ctypes.c_void_p()
+            if self.nvml.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index),
+                                                       ctypes.byref(self.handle)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = int(mx.value)
+            fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(self.nvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self._reasons_fn = fn
+            self._ok = True
+        except OSError:
+            self._ok = False
+
+    def _run(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(int(clk.value))
+            if self._reasons_fn(self.handle, ctypes.byref(rs)) == 0:
+                self.reasons |= int(rs.value)
+            time.sleep(self.period)
+
+    def start(self):
+        if self._ok:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+
+    def stop(self):
+        if self._thread:
+            self._stop.set()
+            self._thread.join()
+
+    def summary(self):
+        if not self._ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+        names = [n for bit, n in _REASONS.items() if self.reasons & bit]
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": names, "samples": len(self.samples)}
+
+
+def nvml_index(local_rank: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    parts = [p for p in vis.split(",") if p.strip()]
+    if parts and parts[min(local_rank, len(parts) - 1)].strip().isdigit():
+        return int(parts[min(local_rank, len(parts) - 1)])
+    return local_rank
+
+
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "trimul_gpt2_dram_traffic.txt")
+KERNEL_SOURCES = [os.path.join(ROOT, "causal_attention_score_gb300", "csrc", f)
+                  for f in ("trimul_sm103a.cu", "sm103a_ptx.cuh")]
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes (read + write) per trimul launch from the committed ncu summary,
+    or None when there is none or the kernel source changed since it was taken."""
+    try:
+        kv = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha256_16") != kernel_source_hash():
+            return None
+        return float(kv["dram_bytes_per_launch_full_size"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------ our arm --
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import causal_attention_score_gb300 as csa
+    from causal_attention_score_gb300 import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ts, ds = synth.TRIMUL_GPT2, synth.DENSE_RAGGED
+    qkv_h = synth.trimul_input(ts, seed=0, dist="normal")
+    X_h, W_h = synth.dense_input(ds, seed=0)
+    qkv = qkv_h.to(dev)
+    X, W = X_h.to(dev), W_h.to(dev)
+    out = torch.empty(ts.out_shape, dtype=torch.float32, device=dev)
+    Y = torch.empty((ds.M, ds.H), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        csa.trimul_forward(out, qkv, ts.B, ts.T, ts.C, ts.NH, stream=stream)
+        csa.dense_xwt(Y, X, W, ds.M, ds.I, ds.H, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if csa.get_status(stream) != 0:
+        raise RuntimeError("device status not ok after warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(nvml_index(local))
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()  # evict L2 between steps; not inside the timed events
+        ev[i][0].record(stream)
+        csa.trimul_forward(out, qkv, ts.B, ts.T, ts.C, ts.NH, stream=stream)
+        ev[i][1].record(stream)
+        csa.dense_xwt(Y, X, W, ds.M, ds.I, ds.H, stream=stream)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    sampler.stop()
+    barrier(world)
+    if csa.get_status(stream) != 0:
+        raise RuntimeError("device status not ok after the timed steps")
+
+    trimul_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    dense_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    step_ms = [a + b for a, b in zip(trimul_ms, dense_ms)]
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    flops_step = trimul_flops(ts.B, ts.T, ts.C, ts.NH) + dense_flops(ds.M, ds.I, ds.H)
+    value = world * K * flops_step / (total_ms * 1e-3) / 1e12
+
+    # End to end through the public API: host (pinned) inputs in, host results out.
+    qkv_p = qkv_h.pin_memory()
+    X_p, W_p = X_h.pin_memory(), W_h.pin_memory()
+    out_p = torch.empty(ts.out_shape, dtype=torch.float32, pin_memory=True)
+    Y_p = torch.empty((ds.M, ds.H), dtype=torch.float32, pin_memory=True)
+
+    def e2e_step():
+        qkv.copy_(qkv_p, non_blocking=True)
+        X.copy_(X_p, non_blocking=True)
+        W.copy_(W_p, non_blocking=True)
+        step()
+        out_p.copy_(out, non_blocking=True)
+        Y_p.copy_(Y, non_blocking=True)
+
+    for _ in range(max(1, min(args.warmup, 3))):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    ke = max(1, min(K, args.e2e_steps))
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(ke):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    barrier(world)
+    h2d = qkv_h.numel() * 2 + X_h.numel() * 2 + W_h.numel() * 2
+    d2h = out.numel() * 4 + Y.numel() * 4
+    e2e_value = world * ke * flops_step / (e2e_ms * 1e-3) / 1e12
+
+    hbm_peak, bf16_peak, peak_src = measured_peaks()
+    trimul_avg_s = statistics.mean(trimul_ms) * 1e-3
+    alg_bytes = trimul_algorithmic_bytes(ts.B, ts.T, ts.C, ts.NH)
+    achieved = alg_bytes / trimul_avg_s / 1e9
+    result = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / K, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) / uniform[-1,1], rounded to bf16)",
+        "config": {
+            "workload": "trimul GPT-2-small (B=8,T=1024,C=768,NH=12,HS=64) + dense ragged "
+                        "(M=960,I=770,H=768), one call each per step",
+            "trimul": {"B": ts.B, "T": ts.T, "C": ts.C, "NH": ts.NH, "mask": "NaN"},
+            "dense": {"M": ds.M, "I": ds.I, "H": ds.H},
+            "l2": "flushed between timed steps (256 MiB write, outside the timed events)",
+            "parallelism": f"replicas x{world}",
+        },
+        "pct_of_bf16_peak": round(100 * value / world / bf16_peak, 3),
+        "parts": {
+            "trimul_us": round(statistics.mean(trimul_ms) * 1e3, 2),
+            "dense_us": round(statistics.mean(dense_ms) * 1e3, 2),
+            "trimul_tflops": round(trimul_flops(ts.B, ts.T, ts.C, ts.NH) / trimul_avg_s / 1e12, 2),
+            "dense_tflops": round(dense_flops(ds.M, ds.I, ds.H)
+                                  / (statistics.mean(dense_ms) * 1e-3) / 1e12, 2),
+        },
+        "roofline": {
+            "kernel": "trimul_sm103a_kernel",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": hbm_peak,
+            "unit": "GB/s",
+            "frac": round(achieved / hbm_peak, 4),
+            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst copy)",
+            "algorithmic_bytes_per_launch": alg_bytes,
+            "traffic": args.traffic,
+        },
+        "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": ke,
+                "ms_per_step": round(e2e_ms / ke, 4)},
+        "gpu_launches": 2 * K,
+        "clocks": sampler.summary(),
+        "wall_s_timed_region": round(wall, 4),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    return result
+
+
+# --------------------------------------------------------- oracle timing --
+
+def _oracle_inputs():
+    import numpy as np  # noqa: F401
+    from causal_attention_score_gb300 import synth
+    ts, ds = synth.TRIMUL_GPT2, synth.DENSE_RAGGED
+    qkv = synth.bf16_bits(synth.trimul_input(ts, seed=0, dist="normal")).reshape(-1)
+    X, W = synth.dense_input(ds, seed=0)
+    return ts, ds, qkv, synth.bf16_bits(X).reshape(-1), synth.bf16_bits(W).reshape(-1)
+
+
+def oracle_sample_step(o, ts, ds, qkv, xb, wb, i):
+    """One bounded sample of the workload on the oracle: all T rows of one (b, h)
+    of the score product and 64 rows of the dense layer. Returns its useful flops."""
+    import numpy as np
+    bh = i % (ts.B * ts.NH)
+    b, h = divmod(bh, ts.NH)
+    bht = np.array([(b, h, t) for t in range(ts.T)], dtype=np.int64)
+    o.trimul_rows(qkv, ts.B, ts.T, ts.C, ts.NH, bht)
+    rows = (np.arange(64, dtype=np.int64) + 64 * i) % ds.M
+    o.dense_rows(xb, wb, ds.M, ds.I, ds.H, rows)
+    return (2 * ts.HS * ts.T * (ts.T + 1) // 2) + 2 * 64 * ds.I * ds.H
+
+
+def cpu_baseline(seconds: float):
+    """The oracle as it stands on the host cores: repeated bounded samples for about
+    `seconds` of CPU time; throughput in the metric's unit."""
+    import oracle
+    o = oracle.get()
+    ts, ds, qkv, xb, wb = _oracle_inputs()
+    flops, i = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        flops += oracle_sample_step(o, ts, ds, qkv, xb, wb, i)
+        i += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": o.num_threads(),
+            "kind": "oracle",
+            "sample": f"{i} samples of one (b,h) head of trimul GPT-2 (1024 rows) + 64 rows of "
+                      f"dense ragged, fp64, {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    o = oracle.get()
+    ts, ds, qkv, xb, wb = _oracle_inputs()
+    for i in range(args.warmup):
+        oracle_sample_step(o, ts, ds, qkv, xb, wb, i)
+    flops = 0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flops += oracle_sample_step(o, ts, ds, qkv, xb, wb, i)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded, rounded to bf16)",
+        "config": {
+            "workload": "trimul GPT-2-small (B=8,T=1024,C=768,NH=12,HS=64) + dense ragged "
+                        "(M=960,I=770,H=768); each step a bounded sample: one (b,h) head "
+                        "(1024 rows) + 64 dense rows",
+        },
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": o.num_threads(),
+                         "kind": "oracle", "sample": "per step: one (b,h) head + 64 dense rows"},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--traffic", type=float, default=None,
+                   help="dram bytes read+written per trimul launch from an ncu capture")
+    args = p.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        p.error("--warmup must be >= 3")
+
+    if args.impl == "reference":
+        # The oracle runs on the host of rank 0 only; other ranks have no work.
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        res = run_reference(args, rank, world)
+        if rank == 0 and res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    rank, world, local = dist_setup(args.gpus)
+    if args.traffic is None:
+        args.traffic = recorded_traffic()
+    res = run_ours(args, rank, world, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,44 @@
+"""The benchmark's work and traffic model against the numbers the pages print (CPU)."""
+import os
+
+import bench
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rows(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return [l.split() for l in f if l.strip() and not l.startswith("#")]
+
+
+def test_tiled_traffic_matches_kernl_worked_example():
+    for M, N, K, bM, bN, bK, loads, writes in _rows("kernl_tiled_matmul_traffic.txt"):
+        got = bench.tiled_traffic(int(M), int(N), int(K), int(bM), int(bN), int(bK))
+        assert got == (int(loads), int(writes))
+
+
+def test_smaller_tiles_load_more():
+    # the tutorial's closing remark: smaller block_M / block_N increase the loads
+    base = bench.tiled_traffic(15, 9, 12, 5, 3, 6)[0]
+    assert bench.tiled_traffic(15, 9, 12, 3, 3, 6)[0] > base
+    assert bench.tiled_traffic(15, 9, 12, 5, 1, 6)[0] > base
+
+
+def test_dense_flops_and_raggedness_of_dietcode_workload():
+    (name, B, T, I, H, _), = [r for r in _rows("dietcode_workloads.txt") if r[0] == "dense"]
+    B, T, I, H = int(B), int(T), int(I), int(H)
+    assert bench.dense_flops(B * T, I, H) == 2 * 16 * 60 * 770 * 2304
+    assert (B * T) % 128 != 0 and I % 4 != 0 and B * T == 960
+
+
+def test_trimul_flops_counts_lower_triangle_including_diagonal():
+    # T=1: one score per head; T=2: three; a full T x T product would give T^2
+    assert bench.trimul_flops(1, 1, 64, 1) == 2 * 64
+    assert bench.trimul_flops(1, 2, 64, 1) == 3 * 2 * 64
+    assert bench.trimul_flops(8, 1024, 768, 12) == 6_448_742_400
+
+
+def test_algorithmic_bytes():
+    assert bench.trimul_algorithmic_bytes(8, 1024, 768, 12) == 8 * 12 * 1024 * 1024 * 4 + 2 * 8 * 1024 * 768 * 2
+    assert bench.trimul_algorithmic_bytes(1, 4, 8, 1, lower_only=True) == 10 * 4 + 2 * 4 * 8 * 2
+    assert bench.dense_algorithmic_bytes(960, 770, 768) == (960 + 768) * 770 * 2 + 960 * 768 * 4
