@@ -42,7 +42,13 @@ constexpr int kThreads = 288;
 constexpr int kLoaderWarps = 4;
 constexpr int kMmaWarp = 4;
 constexpr int kFirstEpiWarp = 5;
-constexpr int kStoreBufs = 4;
+#ifndef CSA_DENSE_MAX_STAGES
+#define CSA_DENSE_MAX_STAGES 6
+#endif
+#ifndef CSA_DENSE_STORE_BUFS
+#define CSA_DENSE_STORE_BUFS 4
+#endif
+constexpr int kStoreBufs = CSA_DENSE_STORE_BUFS;  // staging boxes per epilogue warp
 constexpr int kBoxBytes = 32 * 32 * 4;
 constexpr int kStagingBytes = 4 * kStoreBufs * kBoxBytes;
 
@@ -51,6 +57,7 @@ struct DenseArgs {
   int m_tiles, n_tiles, kblocks, stages;
   long long num_tiles;
   uint32_t tma_load, tma_store, vec2;
+  int load_depth;  // cp.async stages in flight per loader warp (2..4, <= stages)
   uint32_t idesc;
   const uint16_t* X;
   const uint16_t* W;
@@ -72,9 +79,15 @@ __device__ __forceinline__ uint32_t load_pair(const uint16_t* row, int k, int I)
   }
 }
 
+__device__ __forceinline__ uint32_t swz_row_word(uint32_t tile, uint32_t rl, uint32_t lane) {
+  // bf16 pair (2*lane, 2*lane+1) of row rl in the 128-byte-swizzle K-major layout
+  return tile + rl * 128u + ((((lane >> 2) ^ (rl & 7u))) << 4) + ((lane & 3u) << 2);
+}
+
 // One loader warp's share of a rows x 64 operand block: rows w, w+4, w+8, ...
 // Each lane handles bf16 columns k, k+1 (k = kb*64 + 2*lane); the warp writes
 // whole 128-byte rows, so the swizzled stores are bank-conflict free.
+// Synchronous form (plain loads into registers, then st.shared), used for odd I.
 template <bool kPair>
 __device__ __forceinline__ void load_block(const uint16_t* src, int nrows, int row_base, int rows,
                                            int I, int k, uint32_t tile, uint32_t w,
@@ -90,9 +103,23 @@ __device__ __forceinline__ void load_block(const uint16_t* src, int nrows, int r
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const uint32_t rl = static_cast<uint32_t>((i0 + u) * kLoaderWarps) + w;
-      st_shared_b32(tile + rl * 128u + ((((lane >> 2) ^ (rl & 7u))) << 4) + ((lane & 3u) << 2),
-                    v[u]);
+      st_shared_b32(swz_row_word(tile, rl, lane), v[u]);
     }
+  }
+}
+
+// Asynchronous form (I even, 4-byte aligned rows): one 4-byte cp.async per lane
+// and row; out-of-range pairs are zero-filled by a source size of 0.
+__device__ __forceinline__ void issue_block_async(const uint16_t* src, int nrows, int row_base,
+                                                  int rows, int I, int k, uint32_t tile,
+                                                  uint32_t w, uint32_t lane) {
+  const bool k_in = k < I;
+  for (int i = 0; i < rows / kLoaderWarps; ++i) {
+    const uint32_t rl = static_cast<uint32_t>(i * kLoaderWarps) + w;
+    const int row = row_base + static_cast<int>(rl);
+    const bool in = k_in && row < nrows;
+    const uint16_t* p = in ? src + static_cast<size_t>(row) * I + k : src;
+    cp_async_4(swz_row_word(tile, rl, lane), p, in ? 4u : 0u);
   }
 }
 
@@ -185,6 +212,51 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+    } else if (a.vec2) {
+      // Asynchronous copies, kept up to `depth` stages ahead: a stage is handed to
+      // the MMA warp (proxy fence + arrive) once this warp's copies into it have
+      // completed, while later stages are still in flight.
+      const int depth = a.load_depth;
+      int stage = 0, oldest = 0, pending = 0;
+      uint32_t phase = 0;
+      bool aborted = false;
+      for (long long tile = blockIdx.x; tile < a.num_tiles && !aborted; tile += gridDim.x) {
+        const int mb = static_cast<int>(tile % a.m_tiles);
+        const int nb = static_cast<int>(tile / a.m_tiles);
+        for (int kb = 0; kb < a.kblocks; ++kb) {
+          if (!mbar_wait_warp(empty_bar(stage), phase ^ 1u, wd, kSiteLoaderEmpty)) {
+            aborted = true;
+            break;
+          }
+          const int k = kb * kBK + 2 * static_cast<int>(lane);
+          issue_block_async(a.X, a.M, mb * kBM, kBM, a.I, k, a_tile(stage), warp, lane);
+          issue_block_async(a.W, a.H, nb * a.BN, a.BN, a.I, k, b_tile(stage), warp, lane);
+          cp_async_commit();
+          if (++pending == depth) {
+            if (depth == 4) cp_async_wait<3>();
+            else if (depth == 3) cp_async_wait<2>();
+            else cp_async_wait<1>();
+            fence_proxy_async_smem();  // completed generic-proxy writes -> tcgen05.mma
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full_bar(oldest));
+            if (++oldest == a.stages) oldest = 0;
+            --pending;
+          }
+          if (++stage == a.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (!aborted) {
+        for (; pending > 0; --pending) {
+          if (lane == 0) mbar_arrive(full_bar(oldest));
+          if (++oldest == a.stages) oldest = 0;
+        }
+      }
     } else {
       int stage = 0;
       uint32_t phase = 0;
@@ -198,13 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const int k = kb * kBK + 2 * static_cast<int>(lane);
-          if (a.vec2) {
-            load_block<true>(a.X, a.M, mb * kBM, kBM, a.I, k, a_tile(stage), warp, lane);
-            load_block<true>(a.W, a.H, nb * a.BN, a.BN, a.I, k, b_tile(stage), warp, lane);
-          } else {
-            load_block<false>(a.X, a.M, mb * kBM, kBM, a.I, k, a_tile(stage), warp, lane);
-            load_block<false>(a.W, a.H, nb * a.BN, a.BN, a.I, k, b_tile(stage), warp, lane);
-          }
+          load_block<false>(a.X, a.M, mb * kBM, kBM, a.I, k, a_tile(stage), warp, lane);
+          load_block<false>(a.W, a.H, nb * a.BN, a.BN, a.I, k, b_tile(stage), warp, lane);
           fence_proxy_async_smem();  // generic smem writes -> visible to tcgen05.mma
           __syncwarp();
           if (lane == 0) mbar_arrive(full_bar(stage));
@@ -375,7 +442,9 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
 
   a.stage_bytes = static_cast<uint32_t>(kBM + a.BN) * 128u;
   const int fixed = kStagingBytes + 1024 + 1024;
-  a.stages = std::min(4, (dev.max_smem_optin - fixed) / static_cast<int>(a.stage_bytes));
+  a.stages = std::min(CSA_DENSE_MAX_STAGES,
+                      (dev.max_smem_optin - fixed) / static_cast<int>(a.stage_bytes));
+  a.load_depth = std::min(a.stages, 4);
   if (a.stages < 2) {
     err = "dense_xwt: not enough shared memory";
     return CSA_ERR_UNSUPPORTED;

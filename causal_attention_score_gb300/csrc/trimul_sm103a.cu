@@ -44,17 +44,27 @@ namespace {
 constexpr int kTile = 128;          // output tile edge
 constexpr int kChunkElems = 64;     // bf16 per 128-byte swizzle row
 constexpr int kChunkBytes = kTile * 128;  // one 128-row x 64-element operand chunk
-constexpr int kThreads = 192;
-constexpr int kStoreBufs = 4;       // staging boxes per epilogue warp
-constexpr int kBoxBytes = 32 * 32 * 4;
-constexpr int kStagingBytes = 4 * kStoreBufs * kBoxBytes;
+// Tuning constants (compile-time): operand ring depth and staging box pairs per
+// epilogue warp; the host picks the deepest staging that still leaves two stages.
+#ifndef CSA_TRIMUL_MAX_STAGES
+#define CSA_TRIMUL_MAX_STAGES 4
+#endif
+#ifndef CSA_TRIMUL_MAX_STORE_GROUPS
+#define CSA_TRIMUL_MAX_STORE_GROUPS 1
+#endif
+
+constexpr int kEpiWarps = 8;        // two per TMEM lane quarter
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kSlabCols = 64;       // accumulator columns per epilogue warp
+constexpr int kBoxBytes = 32 * 32 * 4;  // one 32 x 32 fp32 TMA store box
 constexpr int kTmemCols = 2 * kTile;
 constexpr uint32_t kIdesc = idesc_bf16_f32(kTile, kTile);
 
 struct TrimulArgs {
   int T, NH, BH, Tt;
   int kchunks, ksteps, stages;
-  long long num_tiles;
+  long long n_lower;  // tiles with t2-tile <= t-tile: MMA + epilogue
+  long long n_fill;   // tiles with t2-tile > t-tile: mask stores only (0 in lower-only mode)
   float scale;
   uint32_t mask_bits;
   uint32_t lower_only;
@@ -63,27 +73,37 @@ struct TrimulArgs {
   int* status;
   unsigned long long wait_limit_ns;
   int inject;
+  uint32_t store_groups;  // staging box pairs per epilogue warp (1 or 2)
   uint32_t stage_bytes, off_staging, off_mask, off_bars, off_misc;
 };
 
-__device__ __forceinline__ void decode_tile(long long id, const TrimulArgs& a, int& bh, int& ti,
-                                            int& tj) {
-  if (!a.lower_only) {
-    const long long per = static_cast<long long>(a.Tt) * a.Tt;
-    bh = static_cast<int>(id / per);
-    const int r = static_cast<int>(id - static_cast<long long>(bh) * per);
-    ti = r / a.Tt;
-    tj = r - ti * a.Tt;
-  } else {
-    const long long per = static_cast<long long>(a.Tt) * (a.Tt + 1) / 2;
-    bh = static_cast<int>(id / per);
-    const int r = static_cast<int>(id - static_cast<long long>(bh) * per);
-    int i = static_cast<int>((sqrtf(8.0f * static_cast<float>(r) + 1.0f) - 1.0f) * 0.5f);
-    while ((i + 1) * (i + 2) / 2 <= r) ++i;
-    while (i * (i + 1) / 2 > r) --i;
-    ti = i;
-    tj = r - i * (i + 1) / 2;
-  }
+// Largest i with i * (i + 1) / 2 <= r.
+__device__ __forceinline__ int tri_root(int r) {
+  int i = static_cast<int>((sqrtf(8.0f * static_cast<float>(r) + 1.0f) - 1.0f) * 0.5f);
+  while ((i + 1) * (i + 2) / 2 <= r) ++i;
+  while (i * (i + 1) / 2 > r) --i;
+  return i;
+}
+
+// Lower tile `id` (j <= i), enumerated per (b, h) row block by row block, so that
+// CTAs working at the same time share the row block's Q tile and K tiles in L2.
+__device__ __forceinline__ void decode_lower(long long id, int Tt, int& bh, int& ti, int& tj) {
+  const long long per = static_cast<long long>(Tt) * (Tt + 1) / 2;
+  bh = static_cast<int>(id / per);
+  const int r = static_cast<int>(id - static_cast<long long>(bh) * per);
+  ti = tri_root(r);
+  tj = r - ti * (ti + 1) / 2;
+}
+
+// Fill tile `id` (j > i): the transpose of the strictly-lower enumeration.
+__device__ __forceinline__ void decode_fill(long long id, int Tt, int& bh, int& ti, int& tj) {
+  const long long per = static_cast<long long>(Tt) * (Tt - 1) / 2;
+  bh = static_cast<int>(id / per);
+  const int r = static_cast<int>(id - static_cast<long long>(bh) * per);
+  const int i = tri_root(r) + 1;  // i * (i - 1) / 2 <= r < i * (i + 1) / 2
+  const int i2 = (i * (i - 1) / 2 > r) ? i - 1 : i;
+  ti = r - i2 * (i2 - 1) / 2;  // row tile (smaller index)
+  tj = i2;                     // column tile
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -120,7 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(tfull_bar(s), 1);
-      mbar_init(tempty_bar(s), 4);
+      mbar_init(tempty_bar(s), kEpiWarps);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -148,10 +168,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t issued = 0, issued_parity = 0;  // per-stage: loads that may be in flight
       bool injected = false;
       const uint32_t tx = static_cast<uint32_t>(a.kchunks) * 2u * kChunkBytes;
-      for (long long tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
+      for (long long id = blockIdx.x; id < a.n_lower; id += gridDim.x) {
         int bh, ti, tj;
-        decode_tile(tile, a, bh, ti, tj);
-        if (tj > ti) continue;
+        decode_lower(id, a.Tt, bh, ti, tj);
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, wd, kSiteProducerEmpty)) break;
         const int b = bh / a.NH, h = bh - b * a.NH;
         mbar_arrive_expect_tx(full_bar(stage), tx);
@@ -192,10 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (long long tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
-        int bh, ti, tj;
-        decode_tile(tile, a, bh, ti, tj);
-        if (tj > ti) continue;
+      for (long long id = blockIdx.x; id < a.n_lower; id += gridDim.x) {
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, wd, kSiteMmaTmemEmpty)) break;
         tc_fence_after_sync();
         if (!mbar_wait(full_bar(stage), phase, wd, kSiteMmaFull)) break;
@@ -226,35 +242,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------- epilogue --
-    const int q = static_cast<int>(warp & 3u);  // TMEM lane quarter this warp may read
-    const uint32_t staging = base + a.off_staging + (warp - 2u) * kStoreBufs * kBoxBytes;
+    // Warp e = warp - 2 owns the 32 rows of TMEM lane quarter warp % 4 (a warp may
+    // only read the lanes of its quarter) and the 64-column slab e / 4 of the tile:
+    // one 64-column TMEM load, one proxy fence and one commit group per tile.
+    const uint32_t ew = warp - 2u;
+    const int q = static_cast<int>(warp & 3u);
+    const int slab = static_cast<int>(ew >> 2);
+    const uint32_t staging = base + a.off_staging + ew * a.store_groups * 2u * kBoxBytes;
     const int T = a.T;
     int acc = 0;
     uint32_t acc_phase = 0;
-    uint32_t buf = 0;
-    for (long long tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
+    uint32_t grp = 0;
+    // This CTA's lower tiles (in the producer's order) merged with its fill tiles
+    // in proportion, starting with a fill tile so stores flow while the first
+    // operands are in flight.
+    const long long G = gridDim.x, c = blockIdx.x;
+    const long long n_low = c < a.n_lower ? (a.n_lower - c + G - 1) / G : 0;
+    const long long n_fil = c < a.n_fill ? (a.n_fill - c + G - 1) / G : 0;
+    long long nl = 0, nf = 0;
+    while (nl < n_low || nf < n_fil) {
+      const bool is_fill = nf < n_fil && (nl >= n_low || nf * n_low <= nl * n_fil);
       int bh, ti, tj;
-      decode_tile(tile, a, bh, ti, tj);
+      if (is_fill) decode_fill(c + (nf++) * G, a.Tt, bh, ti, tj);
+      else decode_lower(c + (nl++) * G, a.Tt, bh, ti, tj);
       const int row0 = ti * kTile + q * 32;
-      if (tj > ti) {
+      const int colw = tj * kTile + slab * kSlabCols;
+      if (is_fill) {
         // Fill tile: mask pattern only (full mode).
-        if (row0 >= T) continue;
+        if (row0 >= T || colw >= T) continue;
         if (a.tma_store) {
           if (lane == 0) {
-            for (int c = 0; c < 4; ++c) {
-              const int col0 = tj * kTile + c * 32;
-              if (col0 < T) {
-                tma_store_3d(&tmap_out, mask_box, col0, row0, bh);
-                bulk_commit();
-              }
-            }
+            tma_store_3d(&tmap_out, mask_box, colw, row0, bh);
+            if (colw + 32 < T) tma_store_3d(&tmap_out, mask_box, colw + 32, row0, bh);
+            bulk_commit();
           }
         } else {
           float* orow = a.out + (static_cast<size_t>(bh) * T + row0) * T;
           const float m = __uint_as_float(a.mask_bits);
           for (int rr = 0; rr < 32 && row0 + rr < T; ++rr) {
-            for (int c = 0; c < 4; ++c) {
-              const int col = tj * kTile + c * 32 + static_cast<int>(lane);
+            for (int c = 0; c < 2; ++c) {
+              const int col = colw + c * 32 + static_cast<int>(lane);
               if (col < T) orow[static_cast<size_t>(rr) * T + col] = m;
             }
           }
@@ -264,63 +291,73 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       if (!mbar_wait_warp(tfull_bar(acc), acc_phase, wd, kSiteEpilogueFull)) break;
       tc_fence_after_sync();
-      const uint32_t tcol =
-          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kTile);
-      const bool diag = (ti == tj);
-      const int r = row0 + static_cast<int>(lane);
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld_32cols(tcol + static_cast<uint32_t>(c * 32), v);
-        if (c == 3) {
-          // This warp's rows of the accumulator are in registers: release it.
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(tempty_bar(acc));
-        }
-        const int col0 = tj * kTile + c * 32;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          uint32_t bits = __float_as_uint(__uint_as_float(v[e]) * a.scale);
-          if (diag && col0 + e > r) bits = a.mask_bits;
-          v[e] = bits;
-        }
-        if (row0 >= T || col0 >= T) continue;  // box wholly past the end (tail tile)
-
-        // 0: skip, 1: TMA store, 2: plain stores (all), 3: plain stores, t2 <= t only
-        int mode = a.tma_store ? 1 : 2;
-        if (a.lower_only && diag) {
-          if (col0 > row0 + 31) mode = 0;
-          else if (col0 + 31 > row0) mode = 3;
-        }
-        if (mode == 0) continue;
-
-        if (lane == 0) bulk_wait_read<kStoreBufs - 1>();
-        __syncwarp();
-        const uint32_t box = staging + buf * kBoxBytes;
-        buf = (buf + 1u) & (kStoreBufs - 1u);
-        stage_row_sw128(box, lane, v);
-        if (mode == 1) {
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_3d(&tmap_out, box, col0, row0, bh);
-            bulk_commit();
-          }
-        } else {
-          __syncwarp();
-          const int col = col0 + static_cast<int>(lane);
-          float* ocol = a.out + (static_cast<size_t>(bh) * T + row0) * T + col;
-          for (int rr = 0; rr < 32; ++rr) {
-            const int row = row0 + rr;
-            const bool ok = row < T && col < T && (mode == 2 || col <= row);
-            const uint32_t val = staged_elem_sw128(box, static_cast<uint32_t>(rr), lane);
-            if (ok) ocol[static_cast<size_t>(rr) * T] = __uint_as_float(val);
-          }
-        }
-      }
+      uint32_t v[kSlabCols];
+      tmem_ld_64cols(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                         static_cast<uint32_t>(acc * kTile + slab * kSlabCols),
+                     v);
+      // This warp's part of the accumulator is in registers: release it.
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
+      }
+
+      const bool diag = (ti == tj);
+      const int r = row0 + static_cast<int>(lane);
+      if (!diag) {
+#pragma unroll
+        for (int e = 0; e < kSlabCols; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * a.scale);
+      } else {
+#pragma unroll
+        for (int e = 0; e < kSlabCols; ++e)
+          v[e] = (colw + e > r) ? a.mask_bits : __float_as_uint(__uint_as_float(v[e]) * a.scale);
+      }
+      if (row0 >= T || colw >= T) continue;  // slab wholly past the end (tail tile)
+
+      // Per 32-column box: 0 skip, 1 TMA store, 2 plain stores, 3 plain stores t2 <= t only.
+      int mode[2];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int col0 = colw + c * 32;
+        mode[c] = col0 >= T ? 0 : (a.tma_store ? 1 : 2);
+        if (mode[c] != 0 && a.lower_only && diag) {
+          if (col0 > row0 + 31) mode[c] = 0;
+          else if (col0 + 31 > row0) mode[c] = 3;
+        }
+      }
+      if (mode[0] == 0 && mode[1] == 0) continue;
+
+      if (lane == 0) {
+        if (a.store_groups == 2) bulk_wait_read<1>();
+        else bulk_wait_read<0>();
+      }
+      __syncwarp();
+      const uint32_t pair = staging + grp * 2u * kBoxBytes;
+      if (++grp == a.store_groups) grp = 0;
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+        if (mode[c] != 0) stage_row_sw128(pair + c * kBoxBytes, lane, v + 32 * c);
+      const bool any_tma = mode[0] == 1 || mode[1] == 1;
+      if (any_tma) fence_proxy_async_smem();
+      __syncwarp();
+      if (any_tma && lane == 0) {
+        for (int c = 0; c < 2; ++c)
+          if (mode[c] == 1) tma_store_3d(&tmap_out, pair + c * kBoxBytes, colw + c * 32, row0, bh);
+        bulk_commit();
+      }
+      for (int c = 0; c < 2; ++c) {
+        if (mode[c] < 2) continue;
+        const int col = colw + c * 32 + static_cast<int>(lane);
+        float* ocol = a.out + (static_cast<size_t>(bh) * T + row0) * T + col;
+        for (int rr = 0; rr < 32; ++rr) {
+          const int row = row0 + rr;
+          const bool ok = row < T && col < T && (mode[c] == 2 || col <= row);
+          const uint32_t val =
+              staged_elem_sw128(pair + c * kBoxBytes, static_cast<uint32_t>(rr), lane);
+          if (ok) ocol[static_cast<size_t>(rr) * T] = __uint_as_float(val);
+        }
       }
     }
     if (lane == 0) bulk_wait_all();
@@ -365,8 +402,8 @@ int trimul_launch(float* out, const void* qkv, int B, int T, int C, int NH, uint
   a.Tt = (T + kTile - 1) / kTile;
   a.kchunks = (HS + kChunkElems - 1) / kChunkElems;
   a.ksteps = (HS + 15) / 16;
-  a.num_tiles = BH * (lower_only ? static_cast<long long>(a.Tt) * (a.Tt + 1) / 2
-                                 : static_cast<long long>(a.Tt) * a.Tt);
+  a.n_lower = BH * (static_cast<long long>(a.Tt) * (a.Tt + 1) / 2);
+  a.n_fill = lower_only ? 0 : BH * (static_cast<long long>(a.Tt) * (a.Tt - 1) / 2);
   a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(HS)));
   a.mask_bits = mask_bits;
   a.lower_only = lower_only ? 1u : 0u;
@@ -377,16 +414,24 @@ int trimul_launch(float* out, const void* qkv, int B, int T, int C, int NH, uint
   a.inject = take_inject() ? 1 : 0;
 
   // Shared memory: operand ring | staging boxes | mask box | barriers | misc.
+  // Operand ring stages vs. staging depth: two box pairs per epilogue warp when
+  // that still leaves two ring stages, else one pair.
   a.stage_bytes = static_cast<uint32_t>(a.kchunks) * 2u * kChunkBytes;
-  const int fixed = kStagingBytes + kBoxBytes + 1024 /*bars+misc*/ + 1024 /*align slack*/;
-  const int budget = dev.max_smem_optin - fixed;
-  a.stages = std::min(4, budget / static_cast<int>(a.stage_bytes));
+  const int fixed = kBoxBytes + 1024 /*bars+misc*/ + 1024 /*align slack*/;
+  int staging_bytes = 0;
+  for (int groups = CSA_TRIMUL_MAX_STORE_GROUPS; groups >= 1; --groups) {
+    staging_bytes = kEpiWarps * groups * 2 * kBoxBytes;
+    a.store_groups = static_cast<uint32_t>(groups);
+    a.stages = std::min(CSA_TRIMUL_MAX_STAGES, (dev.max_smem_optin - fixed - staging_bytes) /
+                               static_cast<int>(a.stage_bytes));
+    if (a.stages >= 2) break;
+  }
   if (a.stages < 1) {
     err = "trimul_forward: not enough shared memory for one operand stage";
     return CSA_ERR_UNSUPPORTED;
   }
   a.off_staging = static_cast<uint32_t>(a.stages) * a.stage_bytes;
-  a.off_mask = a.off_staging + kStagingBytes;
+  a.off_mask = a.off_staging + static_cast<uint32_t>(staging_bytes);
   a.off_bars = a.off_mask + kBoxBytes;
   a.off_misc = a.off_bars + 8u * static_cast<uint32_t>(2 * a.stages + 5);
   const size_t smem = a.off_misc + 16 + 1024;
@@ -422,7 +467,7 @@ int trimul_launch(float* out, const void* qkv, int B, int T, int C, int NH, uint
     err = std::string("trimul_forward: cudaFuncSetAttribute: ") + cudaGetErrorString(e);
     return CSA_ERR_LAUNCH;
   }
-  const long long grid = std::min<long long>(a.num_tiles, dev.sm_count);
+  const long long grid = std::min<long long>(std::max(a.n_lower, a.n_fill), dev.sm_count);
   trimul_sm103a_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(map_qkv, map_out,
                                                                                 a);
   e = cudaGetLastError();
