@@ -17,7 +17,8 @@ rank, world, local = bench.dist_setup(2)
 t = 1.0 + rank  # rank 1 is slower
 m = bench.max_over_ranks(t, world)
 bench.barrier(world)
-print("RESULT", rank, world, m, flush=True)
+with open(os.path.join({out!r}, f"rank{{rank}}.txt"), "w") as f:
+    f.write(f"{{rank}} {{world}} {{m}}")
 dist.destroy_process_group()
 """
 
@@ -32,16 +33,15 @@ def _run_two(code, extra_env=None):
 
 def test_two_gloo_ranks_take_max_time(tmp_path):
     script = tmp_path / "w.py"
-    script.write_text(WORKER.format(root=ROOT))
+    script.write_text(WORKER.format(root=ROOT, out=str(tmp_path)))
     env = dict(os.environ, CSA_BENCH_BACKEND="gloo")
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
            "--master-addr", "127.0.0.1", "--master-port", "29517", str(script)]
     r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=240, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-2000:]
-    lines = [l.split() for l in r.stdout.splitlines() if l.startswith("RESULT")]
-    assert len(lines) == 2
-    for _, rank, world, m in lines:
-        assert int(world) == 2 and float(m) == 2.0
+    for rank in (0, 1):
+        got_rank, world, m = (tmp_path / f"rank{rank}.txt").read_text().split()
+        assert int(got_rank) == rank and int(world) == 2 and float(m) == 2.0
 
 
 def test_reference_arm_runs_on_rank0_only(tmp_path):
