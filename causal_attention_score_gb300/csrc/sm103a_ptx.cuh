@@ -36,6 +36,7 @@ enum WaitSite : int {
   kSiteEpilogueFull = 4,
   kSiteDrain = 5,
   kSiteLoaderEmpty = 6,
+  kSiteSched = 7,
 };
 
 // Shared by all bounded waits of one CTA.

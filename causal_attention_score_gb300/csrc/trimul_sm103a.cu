@@ -30,6 +30,8 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
+#include <mutex>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -65,6 +67,9 @@ struct TrimulArgs {
   int kchunks, ksteps, stages;
   long long n_lower;  // tiles with t2-tile <= t-tile: MMA + epilogue
   long long n_fill;   // tiles with t2-tile > t-tile: mask stores only (0 in lower-only mode)
+  int n_total;          // n_lower + n_fill: length of the work list
+  int per_lower, per_fill;  // lower / fill tiles per (b, h)
+  unsigned int* sched;  // this launch's counter pair: [0] next position, [1] CTAs done
   float scale;
   uint32_t mask_bits;
   uint32_t lower_only;
@@ -77,6 +82,37 @@ struct TrimulArgs {
   uint32_t stage_bytes, off_staging, off_mask, off_bars, off_misc;
 };
 
+// Work-list counters, one pair per launch in flight (slot chosen by the host);
+// the last CTA of a launch resets its pair to zero.
+constexpr int kSchedSlots = 256;
+__device__ unsigned int g_trimul_sched[kSchedSlots][2];
+
+#ifndef CSA_TRIMUL_SCHED_DEPTH
+#define CSA_TRIMUL_SCHED_DEPTH 4
+#endif
+#ifndef CSA_TRIMUL_FETCH_AHEAD
+#define CSA_TRIMUL_FETCH_AHEAD 2
+#endif
+constexpr int kSchedDepth = CSA_TRIMUL_SCHED_DEPTH;  // positions buffered between roles
+constexpr int kFetchAhead = CSA_TRIMUL_FETCH_AHEAD;  // work-list fetches in flight (1..4)
+constexpr unsigned int kEntryEnd = 0xFFFFFFFFu;      // ring entry: no more work
+
+// Position p of the work list: (b, h)-major, so CTAs working at the same time
+// share Q and K tiles in L2; within one (b, h) its per_fill fill tiles are
+// spread evenly among its per_lower lower tiles (exact small-integer test).
+// Returns true for a fill tile; r is its index among the (b, h)'s fill or
+// lower tiles.
+__device__ __forceinline__ bool position_is_fill(int p, int per_lower, int per_fill, int& bh,
+                                                 int& r) {
+  const int per = per_lower + per_fill;
+  bh = p / per;
+  const int q = p - bh * per;
+  const int f0 = (q * per_fill) / per;
+  const int f1 = ((q + 1) * per_fill) / per;
+  r = (f1 > f0) ? f0 : q - f0;
+  return f1 > f0;
+}
+
 // Largest i with i * (i + 1) / 2 <= r.
 __device__ __forceinline__ int tri_root(int r) {
   int i = static_cast<int>((sqrtf(8.0f * static_cast<float>(r) + 1.0f) - 1.0f) * 0.5f);
@@ -85,25 +121,18 @@ __device__ __forceinline__ int tri_root(int r) {
   return i;
 }
 
-// Lower tile `id` (j <= i), enumerated per (b, h) row block by row block, so that
-// CTAs working at the same time share the row block's Q tile and K tiles in L2.
-__device__ __forceinline__ void decode_lower(long long id, int Tt, int& bh, int& ti, int& tj) {
-  const long long per = static_cast<long long>(Tt) * (Tt + 1) / 2;
-  bh = static_cast<int>(id / per);
-  const int r = static_cast<int>(id - static_cast<long long>(bh) * per);
+// Lower tile number r (j <= i) of one (b, h), row block by row block.
+__device__ __forceinline__ void decode_lower(int r, int& ti, int& tj) {
   ti = tri_root(r);
   tj = r - ti * (ti + 1) / 2;
 }
 
-// Fill tile `id` (j > i): the transpose of the strictly-lower enumeration.
-__device__ __forceinline__ void decode_fill(long long id, int Tt, int& bh, int& ti, int& tj) {
-  const long long per = static_cast<long long>(Tt) * (Tt - 1) / 2;
-  bh = static_cast<int>(id / per);
-  const int r = static_cast<int>(id - static_cast<long long>(bh) * per);
+// Fill tile number r (j > i) of one (b, h): the transpose of the strictly-lower
+// enumeration.
+__device__ __forceinline__ void decode_fill(int r, int& ti, int& tj) {
   const int i = tri_root(r) + 1;  // i * (i - 1) / 2 <= r < i * (i + 1) / 2
-  const int i2 = (i * (i - 1) / 2 > r) ? i - 1 : i;
-  ti = r - i2 * (i2 - 1) / 2;  // row tile (smaller index)
-  tj = i2;                     // column tile
+  ti = r - i * (i - 1) / 2;       // row tile (smaller index)
+  tj = i;                         // column tile
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -123,6 +152,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tfull_bar = [&](int s) { return bars + 8u * (2 * a.stages + s); };
   auto tempty_bar = [&](int s) { return bars + 8u * (2 * a.stages + 2 + s); };
   const uint32_t drain_bar = bars + 8u * (2 * a.stages + 4);
+  auto sfull_bar = [&](int s) { return bars + 8u * (2 * a.stages + 5 + s); };
+  auto sempty_bar = [&](int s) { return bars + 8u * (2 * a.stages + 5 + kSchedDepth + s); };
+  auto sched_entry = [&](int s) { return base + a.off_misc + 16u + 4u * s; };
   const uint32_t tmem_slot = base + a.off_misc;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + a.off_misc + 4);
   const uint32_t mask_box = base + a.off_mask;
@@ -143,6 +175,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tempty_bar(s), kEpiWarps);
     }
     mbar_init(drain_bar, 1);
+    for (int s = 0; s < kSchedDepth; ++s) {
+      mbar_init(sfull_bar(s), 1);
+      mbar_init(sempty_bar(s), 1 + kEpiWarps);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -168,14 +204,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t issued = 0, issued_parity = 0;  // per-stage: loads that may be in flight
       bool injected = false;
       const uint32_t tx = static_cast<uint32_t>(a.kchunks) * 2u * kChunkBytes;
-      for (long long id = blockIdx.x; id < a.n_lower; id += gridDim.x) {
-        int bh, ti, tj;
-        decode_lower(id, a.Tt, bh, ti, tj);
+      // Work list: every tile of the launch, fill tiles spread evenly among the
+      // lower ones. With fill tiles present, positions are taken from a shared
+      // counter (kFetchAhead fetches in flight), so SMs that get more memory
+      // bandwidth take more tiles; in lower-only mode every tile needs operands
+      // fetched ahead, so positions are dealt statically (c, c+G, ...) instead.
+      // Each position goes to the MMA and epilogue warps through the shared ring.
+      const bool dynamic = a.n_fill > 0;
+      unsigned int static_next = blockIdx.x;
+      auto fetch = [&]() -> unsigned int {
+        if (dynamic) return atomicAdd(a.sched, 1u);
+        const unsigned int v = static_next;
+        static_next += gridDim.x;
+        return v;
+      };
+      unsigned int pf[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) pf[i] = i < kFetchAhead ? fetch() : 0u;
+      int slot = 0;
+      uint32_t sphase = 0;
+      while (true) {
+        const unsigned int cur = pf[0];
+        const bool done = cur >= static_cast<unsigned int>(a.n_total);
+#pragma unroll
+        for (int i = 0; i < 3; ++i) pf[i] = pf[i + 1];
+        if (!done) pf[kFetchAhead - 1] = fetch();
+        if (!mbar_wait(sempty_bar(slot), sphase ^ 1u, wd, kSiteSched)) break;
+        st_shared_b32(sched_entry(slot), done ? kEntryEnd : cur);
+        mbar_arrive(sfull_bar(slot));
+        if (++slot == kSchedDepth) {
+          slot = 0;
+          sphase ^= 1u;
+        }
+        if (done) break;
+        int bh, r, ti, tj;
+        if (position_is_fill(static_cast<int>(cur), a.per_lower, a.per_fill, bh, r)) continue;
+        decode_lower(r, ti, tj);
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, wd, kSiteProducerEmpty)) break;
         const int b = bh / a.NH, h = bh - b * a.NH;
         mbar_arrive_expect_tx(full_bar(stage), tx);
-        if (a.inject && blockIdx.x == 0 && !injected) {
-          injected = true;  // withhold this tile's loads: its consumer's wait must run out
+        if (a.inject && !injected) {
+          injected = true;  // withhold this CTA's first loads: its consumer's wait must run out
           issued &= ~(1u << stage);
         } else {
           for (int kc = 0; kc < a.kchunks; ++kc) {
@@ -211,7 +280,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (long long id = blockIdx.x; id < a.n_lower; id += gridDim.x) {
+      int slot = 0;
+      uint32_t sphase = 0;
+      while (true) {
+        if (!mbar_wait(sfull_bar(slot), sphase, wd, kSiteSched)) break;
+        const unsigned int cur = ld_shared_b32(sched_entry(slot));
+        mbar_arrive(sempty_bar(slot));
+        if (++slot == kSchedDepth) {
+          slot = 0;
+          sphase ^= 1u;
+        }
+        if (cur == kEntryEnd) break;
+        int bh, r;
+        if (position_is_fill(static_cast<int>(cur), a.per_lower, a.per_fill, bh, r)) continue;
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, wd, kSiteMmaTmemEmpty)) break;
         tc_fence_after_sync();
         if (!mbar_wait(full_bar(stage), phase, wd, kSiteMmaFull)) break;
@@ -253,18 +334,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t grp = 0;
-    // This CTA's lower tiles (in the producer's order) merged with its fill tiles
-    // in proportion, starting with a fill tile so stores flow while the first
-    // operands are in flight.
-    const long long G = gridDim.x, c = blockIdx.x;
-    const long long n_low = c < a.n_lower ? (a.n_lower - c + G - 1) / G : 0;
-    const long long n_fil = c < a.n_fill ? (a.n_fill - c + G - 1) / G : 0;
-    long long nl = 0, nf = 0;
-    while (nl < n_low || nf < n_fil) {
-      const bool is_fill = nf < n_fil && (nl >= n_low || nf * n_low <= nl * n_fil);
-      int bh, ti, tj;
-      if (is_fill) decode_fill(c + (nf++) * G, a.Tt, bh, ti, tj);
-      else decode_lower(c + (nl++) * G, a.Tt, bh, ti, tj);
+    int slot = 0;
+    uint32_t sphase = 0;
+    while (true) {
+      int ok = 1;
+      unsigned int cur = 0;
+      if (lane == 0) {
+        ok = mbar_wait(sfull_bar(slot), sphase, wd, kSiteSched) ? 1 : 0;
+        if (ok) {
+          cur = ld_shared_b32(sched_entry(slot));
+          mbar_arrive(sempty_bar(slot));
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      cur = __shfl_sync(0xffffffffu, cur, 0);
+      if (!ok || cur == kEntryEnd) break;
+      if (++slot == kSchedDepth) {
+        slot = 0;
+        sphase ^= 1u;
+      }
+      int bh, rank, ti, tj;
+      const bool is_fill =
+          position_is_fill(static_cast<int>(cur), a.per_lower, a.per_fill, bh, rank);
+      if (is_fill) decode_fill(rank, ti, tj);
+      else decode_lower(rank, ti, tj);
       const int row0 = ti * kTile + q * 32;
       const int colw = tj * kTile + slab * kSlabCols;
       if (is_fill) {
@@ -369,6 +462,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, kTmemCols);
   }
+  if (threadIdx.x == 0) {
+    // Every fetch of this CTA is done; the last CTA to get here resets the pair.
+    __threadfence();
+    if (atomicAdd(a.sched + 1, 1u) == gridDim.x - 1) {
+      atomicExch(a.sched, 0u);
+      atomicExch(a.sched + 1, 0u);
+    }
+  }
 }
 
 }  // namespace
@@ -404,6 +505,13 @@ int trimul_launch(float* out, const void* qkv, int B, int T, int C, int NH, uint
   a.ksteps = (HS + 15) / 16;
   a.n_lower = BH * (static_cast<long long>(a.Tt) * (a.Tt + 1) / 2);
   a.n_fill = lower_only ? 0 : BH * (static_cast<long long>(a.Tt) * (a.Tt - 1) / 2);
+  if (a.n_lower + a.n_fill >= (1LL << 31) - (1LL << 20)) {
+    err = "trimul_forward: too many tiles";
+    return CSA_ERR_SHAPE;
+  }
+  a.n_total = static_cast<int>(a.n_lower + a.n_fill);
+  a.per_lower = a.Tt * (a.Tt + 1) / 2;
+  a.per_fill = lower_only ? 0 : a.Tt * (a.Tt - 1) / 2;
   a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(HS)));
   a.mask_bits = mask_bits;
   a.lower_only = lower_only ? 1u : 0u;
@@ -417,7 +525,7 @@ int trimul_launch(float* out, const void* qkv, int B, int T, int C, int NH, uint
   // Operand ring stages vs. staging depth: two box pairs per epilogue warp when
   // that still leaves two ring stages, else one pair.
   a.stage_bytes = static_cast<uint32_t>(a.kchunks) * 2u * kChunkBytes;
-  const int fixed = kBoxBytes + 1024 /*bars+misc*/ + 1024 /*align slack*/;
+  const int fixed = kBoxBytes + 1024 /*bars+misc+ring*/ + 1024 /*align slack*/;
   int staging_bytes = 0;
   for (int groups = CSA_TRIMUL_MAX_STORE_GROUPS; groups >= 1; --groups) {
     staging_bytes = kEpiWarps * groups * 2 * kBoxBytes;
@@ -433,8 +541,8 @@ int trimul_launch(float* out, const void* qkv, int B, int T, int C, int NH, uint
   a.off_staging = static_cast<uint32_t>(a.stages) * a.stage_bytes;
   a.off_mask = a.off_staging + static_cast<uint32_t>(staging_bytes);
   a.off_bars = a.off_mask + kBoxBytes;
-  a.off_misc = a.off_bars + 8u * static_cast<uint32_t>(2 * a.stages + 5);
-  const size_t smem = a.off_misc + 16 + 1024;
+  a.off_misc = a.off_bars + 8u * static_cast<uint32_t>(2 * a.stages + 5 + 2 * kSchedDepth);
+  const size_t smem = a.off_misc + 16 + 4 * kSchedDepth + 1024;
 
   CUtensorMap map_qkv, map_out;
   {
@@ -460,6 +568,26 @@ int trimul_launch(float* out, const void* qkv, int B, int T, int C, int NH, uint
     std::memset(&map_out, 0, sizeof map_out);
   }
 
+  {
+    static std::mutex mu;
+    static unsigned int* sched_base[64] = {};
+    static std::atomic<unsigned int> launch_seq{0};
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev.device < 0 || dev.device >= 64) {
+      err = "trimul_forward: device ordinal out of range";
+      return CSA_ERR_CUDA;
+    }
+    if (!sched_base[dev.device]) {
+      void* p = nullptr;
+      cudaError_t se = cudaGetSymbolAddress(&p, g_trimul_sched);
+      if (se != cudaSuccess) {
+        err = std::string("trimul_forward: cudaGetSymbolAddress: ") + cudaGetErrorString(se);
+        return CSA_ERR_CUDA;
+      }
+      sched_base[dev.device] = static_cast<unsigned int*>(p);
+    }
+    a.sched = sched_base[dev.device] + 2 * (launch_seq.fetch_add(1) % kSchedSlots);
+  }
   cudaError_t e = cudaFuncSetAttribute(trimul_sm103a_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
@@ -467,7 +595,7 @@ int trimul_launch(float* out, const void* qkv, int B, int T, int C, int NH, uint
     err = std::string("trimul_forward: cudaFuncSetAttribute: ") + cudaGetErrorString(e);
     return CSA_ERR_LAUNCH;
   }
-  const long long grid = std::min<long long>(std::max(a.n_lower, a.n_fill), dev.sm_count);
+  const long long grid = std::min<long long>(a.n_total, dev.sm_count);
   trimul_sm103a_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(map_qkv, map_out,
                                                                                 a);
   e = cudaGetLastError();

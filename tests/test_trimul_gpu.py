@@ -134,3 +134,24 @@ def test_trimul_gpt2_full_size(oracle_lib):
 
 def test_trimul_long_context_full_size(oracle_lib):
     _full_size(oracle_lib, synth.TRIMUL_LONG, seed=0, rows_per_bh=2)
+
+
+def test_trimul_many_launches_reuse_schedule_slots(oracle_lib):
+    """More launches than the kernel's per-launch counter slots, alternating modes
+    and streams; the last launch must still be exact (counters are reset by the
+    last CTA of each launch)."""
+    shape, qkv = trimul_case(2, 384, 2, 64, seed=11)
+    q = qkv.cuda()
+    out = torch.empty(shape.out_shape, dtype=torch.float32, device="cuda")
+    side = torch.cuda.Stream()
+    for i in range(300):
+        s = side if i % 3 == 0 else torch.cuda.current_stream()
+        with torch.cuda.stream(s):
+            csa.trimul_forward(out, q, 2, 384, shape.C, 2, lower_only=(i % 2 == 1), stream=s)
+        s.synchronize()
+    out.view(torch.int32).fill_(-1)
+    csa.trimul_forward(out, q, 2, 384, shape.C, 2)
+    torch.cuda.synchronize()
+    assert csa.get_status() == 0
+    ref = oracle_lib.trimul(synth.bf16_bits(qkv).reshape(-1), 2, 384, shape.C, 2, 0)
+    check_trimul_full(f32_bits(out), out.cpu().numpy(), ref, NAN_BITS, "after 300 launches")
