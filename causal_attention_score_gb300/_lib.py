@@ -33,6 +33,7 @@ _u32 = ctypes.c_uint32
 SIGNATURES = {
     "trimul_forward": (_i, [_vp, _vp, _i, _i, _i, _i]),
     "trimul_forward_ex": (_i, [_vp, _vp, _i, _i, _i, _i, _u32, _u32, _vp]),
+    "trimul_forward_noalloc": (_i, [_vp, _vp, _i, _i, _i, _i, _u32, _u32, _vp]),
     "dense_xwt": (_i, [_vp, _vp, _vp, _i, _i, _i]),
     "dense_xwt_ex": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp]),
     "csa_get_status": (_i, [_vp]),

@@ -32,8 +32,16 @@ uint64_t wait_limit_ns();
 bool take_inject();
 
 // Kernel launchers; each validates what is specific to its kernel.
+// `counters`: work-list counter pair to use instead of the library's per-launch
+// slot ring (nullptr = slot ring); it must be zero when the kernel starts.
 int trimul_launch(float* out, const void* qkv, int B, int T, int C, int NH, uint32_t mask_bits,
-                  uint32_t flags, cudaStream_t stream, const DeviceInfo& dev, std::string& err);
+                  uint32_t flags, cudaStream_t stream, const DeviceInfo& dev, std::string& err,
+                  unsigned int* counters = nullptr);
+
+// trimul_launch with its scratch in a fixed device array (no allocation).
+int trimul_launch_noalloc(float* out, const void* qkv, int B, int T, int C, int NH,
+                          uint32_t mask_bits, uint32_t flags, cudaStream_t stream,
+                          const DeviceInfo& dev, std::string& err);
 
 int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
                  cudaStream_t stream, const DeviceInfo& dev, std::string& err);

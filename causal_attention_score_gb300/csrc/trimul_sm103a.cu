@@ -475,7 +475,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 int trimul_launch(float* out, const void* qkv, int B, int T, int C, int NH, uint32_t mask_bits,
-                  uint32_t flags, cudaStream_t stream, const DeviceInfo& dev, std::string& err) {
+                  uint32_t flags, cudaStream_t stream, const DeviceInfo& dev, std::string& err,
+                  unsigned int* counters) {
   const int HS = C / NH;
   if (HS % 8 != 0) {
     err = "trimul_forward: HS = C/NH must be a multiple of 8 (TMA row pitch of a head)";
@@ -568,7 +569,9 @@ int trimul_launch(float* out, const void* qkv, int B, int T, int C, int NH, uint
     std::memset(&map_out, 0, sizeof map_out);
   }
 
-  {
+  if (counters) {
+    a.sched = counters;  // caller-provided counter pair (zeroed before this launch)
+  } else {
     static std::mutex mu;
     static unsigned int* sched_base[64] = {};
     static std::atomic<unsigned int> launch_seq{0};
@@ -604,6 +607,61 @@ int trimul_launch(float* out, const void* qkv, int B, int T, int C, int NH, uint
     return CSA_ERR_LAUNCH;
   }
   return CSA_OK;
+}
+
+// ---------------------------------------------------- allocation-free variant --
+//
+// Scratch of trimul_launch_noalloc: the work-list counter pair the kernel needs,
+// in a fixed array that every device loading this library holds until exit
+// (no cudaMalloc anywhere on that path). One array per device, shared by every
+// call on that device, so calls whose kernels overlap on the GPU race on it.
+constexpr size_t kNoallocScratchBytes = 256;
+static __device__ __align__(256) unsigned int g_trimul_noalloc_scratch[kNoallocScratchBytes / 4];
+
+int trimul_launch_noalloc(float* out, const void* qkv, int B, int T, int C, int NH,
+                          uint32_t mask_bits, uint32_t flags, cudaStream_t stream,
+                          const DeviceInfo& dev, std::string& err) {
+  // What this call keeps in the scratch: the two 32-bit work-list counters.
+  constexpr size_t kNeeded = 2 * sizeof(unsigned int);
+  static_assert(kNeeded <= kNoallocScratchBytes, "scratch array too small");
+  // The counters index the work list; a list beyond their range is rejected.
+  const long long Tt = (static_cast<long long>(T) + kTile - 1) / kTile;
+  const long long tiles = static_cast<long long>(B) * NH * Tt * Tt;
+  if (tiles >= (1LL << 31) - (1LL << 20)) {
+    err = "trimul_forward_noalloc: " + std::to_string(tiles) +
+          " output tiles exceed what its fixed scratch counters can index (2^31 - 2^20)";
+    return CSA_ERR_SHAPE;
+  }
+  // Set-up, once per device, with that device current: the device address of the
+  // scratch array (its name is only a host-side stand-in in host code).
+  static std::mutex mu;
+  static unsigned int* scratch[64] = {};
+  unsigned int* counters = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev.device < 0 || dev.device >= 64) {
+      err = "trimul_forward_noalloc: device ordinal out of range";
+      return CSA_ERR_CUDA;
+    }
+    if (!scratch[dev.device]) {
+      void* p = nullptr;
+      const cudaError_t e = cudaGetSymbolAddress(&p, g_trimul_noalloc_scratch);
+      if (e != cudaSuccess || !p) {
+        err = std::string("trimul_forward_noalloc: cudaGetSymbolAddress: ") +
+              cudaGetErrorString(e);
+        return CSA_ERR_CUDA;
+      }
+      scratch[dev.device] = static_cast<unsigned int*>(p);
+    }
+    counters = scratch[dev.device];
+  }
+  // The counters must start at zero; the array keeps whatever the last call left.
+  const cudaError_t e = cudaMemsetAsync(counters, 0, kNeeded, stream);
+  if (e != cudaSuccess) {
+    err = std::string("trimul_forward_noalloc: clearing scratch: ") + cudaGetErrorString(e);
+    return CSA_ERR_CUDA;
+  }
+  return trimul_launch(out, qkv, B, T, C, NH, mask_bits, flags, stream, dev, err, counters);
 }
 
 }  // namespace csa

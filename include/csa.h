@@ -96,6 +96,34 @@ csa_status trimul_forward_ex(float* out, const void* qkv, int B, int T, int C, i
                              uint32_t mask_bits, uint32_t flags, void* stream);
 
 /*
+ * trimul_forward_noalloc -- trimul_forward_ex for callers that must not
+ * allocate device memory. No passage of the pages has a counterpart: this
+ * entry point exists for deployment, not for the method.
+ *
+ * Who needs it: code that runs where a new device allocation is not allowed or
+ * not affordable -- under a memory manager that forbids allocations after
+ * start-up, inside a region that must not trigger the device-wide
+ * synchronisation cudaFree brings, or in plug-in hosts that only hand out
+ * buffers. trimul_forward_ex itself never calls cudaMalloc either, but keeps
+ * per-launch scheduling counters in a ring of slots; this variant instead
+ * keeps its scratch -- the kernel's two work-list counters -- in one fixed
+ * 256-byte device array that every GPU loading the library holds until exit,
+ * and calls no cudaMalloc, cudaFree or allocating library routine.
+ *
+ * Arguments, layouts, results and errors are those of trimul_forward_ex, plus:
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - Every call clears the counters (cudaMemsetAsync on `stream`) before its
+ *    kernel starts. All calls on a device share the array, so two calls whose
+ *    kernels overlap on the GPU (different streams, no ordering) race and may
+ *    leave output tiles unwritten; serialise them.
+ *  - A problem whose tile list exceeds what the 32-bit counters can index
+ *    (2^31 - 2^20 output tiles of 128 x 128) is rejected with CSA_ERR_SHAPE.
+ */
+csa_status trimul_forward_noalloc(float* out, const void* qkv, int B, int T, int C, int NH,
+                                  uint32_t mask_bits, uint32_t flags, void* stream);
+
+/*
  * dense_xwt -- Y = X W^T, default stream.
  *
  *   Y  device, fp32, [M, H] row-major, fully overwritten.

@@ -86,3 +86,13 @@ def test_binding_refuses_cpu_tensors(lib):
     out = torch.zeros((1, 1, 4, 4))
     with pytest.raises(ValueError):
         csa.trimul_forward(out, qkv, 1, 4, 8, 1)
+
+
+@pytest.mark.parametrize("args,code", [
+    ((None, 16, 1, 1, 8, 1, 0, 0, None), _lib.CSA_ERR_NULL),
+    ((16, 16, 1, 1, 10, 3, 0, 0, None), _lib.CSA_ERR_SHAPE),
+    ((16, 16, 1, 1, 12, 1, 0, 0, None), _lib.CSA_ERR_ALIGN),
+    ((16, 16, 1, 1, 64, 1, 0, 4, None), _lib.CSA_ERR_UNSUPPORTED),
+])
+def test_noalloc_argument_errors(lib, args, code):
+    assert lib.trimul_forward_noalloc(*args) == code
