@@ -24,6 +24,14 @@ SHAPES = [
     (64, 768, 3072),
     (300, 1000, 770),
     (257, 129, 255),
+    # bulk + realign fetch (I even, rows not 16-byte multiples), incl. rows shorter
+    # than the 144-byte copy window and arrays whose size is not a multiple of 16
+    (33, 10, 17),
+    (5, 2, 3),
+    (7, 10, 9),
+    (200, 130, 300),
+    (131, 258, 129),
+    (1024, 770, 1024),
 ]
 
 
@@ -93,3 +101,23 @@ def test_dense_sweep(oracle_lib):
         ref = oracle_lib.dense_rows(synth.bf16_bits(X).reshape(-1), wbits, M, I, H, rows)
         assert_close(Y[torch.from_numpy(rows).cuda()].cpu().numpy(), ref, f"sweep call {i} M={M}")
         assert bool(torch.all(torch.isfinite(Y)))
+
+
+@pytest.mark.parametrize("offset", [1, 2])
+def test_dense_misaligned_views(oracle_lib, offset):
+    """X and W views starting 2 or 4 bytes into their storage: not 16-byte aligned,
+    so the plain-load fetch runs (2-byte pairs or 4-byte pairs)."""
+    M, I, H = 130, 770, 70
+    Xb, Wb = synth.dense_input(synth.DenseShape(M=M, I=I + offset, H=H), seed=9)
+    Xf = Xb.reshape(-1)[offset:offset + M * I].reshape(M, I)
+    Wf = Wb.reshape(-1)[offset:offset + H * I].reshape(H, I)
+    Xd = Xb.reshape(-1).cuda()[offset:offset + M * I]
+    Wd = Wb.reshape(-1).cuda()[offset:offset + H * I]
+    assert Xd.data_ptr() % 16 != 0
+    ref = oracle_lib.dense(synth.bf16_bits(Xf.contiguous()).reshape(-1),
+                           synth.bf16_bits(Wf.contiguous()).reshape(-1), M, I, H)
+    Y = poisoned((M, H))
+    csa.dense_xwt(Y, Xd, Wd, M, I, H)
+    torch.cuda.synchronize()
+    assert csa.get_status() == 0
+    assert_close(Y.cpu().numpy(), ref, f"misaligned by {2 * offset} bytes")
