@@ -113,3 +113,25 @@ def dense_sweep_inputs(seed: int = 0):
     xs = [uniform_bf16((DENSE_SWEEP_BATCH * t, DENSE_SWEEP_I), 1000 + i)
           for i, t in enumerate(dense_sweep_lengths(seed))]
     return xs, W
+
+
+@dataclass(frozen=True)
+class BmmShape:
+    batch: int
+    T1: int
+    T2: int
+    D: int
+
+
+# "DietCode ... test_local_padding_ii": B, T, H, NH = 16, 120, 768, 12 -> batch
+# B*NH = 192, T = 120, D = H/NH = 64.
+BMM_NT_RAGGED = BmmShape(batch=16 * 12, T1=120, T2=120, D=64)
+
+
+def bmm_input(shape: BmmShape, seed: int = 0):
+    """(X [batch, T1, D], W [batch, T2, D]) bf16 iid uniform[-1, 1]; X first, one
+    generator seeded with ``seed``."""
+    g = torch.Generator().manual_seed(seed)
+    X = uniform_bf16((shape.batch, shape.T1, shape.D), seed, generator=g)
+    W = uniform_bf16((shape.batch, shape.T2, shape.D), seed, generator=g)
+    return X, W

@@ -13,6 +13,8 @@ pages it follows:
 * ``dense`` / ``dense_rows``: the dense workload ``Y = X W^T`` of
   "DietCode tests/codegen/test_1_local_padding.py" (test_local_padding
   docstring).
+* ``bmm_nt``: the batched NT workload of the same file (test_local_padding_ii
+  docstring), ``Y[i, j, k] = sum_l X[i, j, l] W[i, k, l]``.
 
 Inputs are bf16 tensors passed as their raw 16-bit patterns (numpy uint16);
 outputs are float64.
@@ -67,8 +69,9 @@ class Oracle:
         self.lib.oracle_trimul_rows.argtypes = [dp, up, i64, i64, i64, i64, lp, i64, ctypes.c_int]
         self.lib.oracle_dense.argtypes = [dp, up, up, i64, i64, i64]
         self.lib.oracle_dense_rows.argtypes = [dp, up, up, i64, i64, i64, lp, i64]
+        self.lib.oracle_bmm_nt.argtypes = [dp, up, up, i64, i64, i64, i64]
         for f in ("oracle_trimul", "oracle_trimul_rows", "oracle_dense", "oracle_dense_rows",
-                  "oracle_num_threads"):
+                  "oracle_bmm_nt", "oracle_num_threads"):
             getattr(self.lib, f).restype = ctypes.c_int
         self.lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         self.lib.oracle_set_num_threads.restype = None
@@ -132,6 +135,22 @@ class Oracle:
                                         _ptr(r, ctypes.c_int64), r.shape[0])
         if rc != 0:
             raise ValueError(f"oracle_dense_rows rejected the arguments (rc={rc})")
+        return Y
+
+
+    # -- batched NT product -----------------------------------------------
+    def bmm_nt(self, X_u16: np.ndarray, W_u16: np.ndarray, batch: int, T1: int, T2: int,
+               D: int) -> np.ndarray:
+        """Y[i, j, k] = sum_l X[i, j, l] W[i, k, l] as (batch, T1, T2) float64."""
+        x = np.ascontiguousarray(X_u16, dtype=np.uint16)
+        w = np.ascontiguousarray(W_u16, dtype=np.uint16)
+        if x.size != batch * T1 * D or w.size != batch * T2 * D:
+            raise ValueError("X / W sizes do not match (batch, T1, D) / (batch, T2, D)")
+        Y = np.empty((batch, T1, T2), dtype=np.float64)
+        rc = self.lib.oracle_bmm_nt(_ptr(Y, ctypes.c_double), _ptr(x, ctypes.c_uint16),
+                                    _ptr(w, ctypes.c_uint16), batch, T1, T2, D)
+        if rc != 0:
+            raise ValueError(f"oracle_bmm_nt rejected the shape (rc={rc})")
         return Y
 
 

@@ -19,6 +19,10 @@
  *  - "DietCode tests/codegen/test_1_local_padding.py", test_local_padding
  *    docstring, the dense workload: Y[i, j] += X[i, k] * W[j, k], i.e.
  *    Y = X W^T with X [B*T, I], W [H, I], Y [B*T, H].
+ *  - the same file, test_local_padding_ii docstring, the batched NT workload:
+ *    Y[i, j, k] += X[i, j, l] * W[i, k, l] with X [B*NH, T, H/NH],
+ *    W [B*NH, T, H/NH], Y [B*NH, T, T] (the unmasked, unscaled score product;
+ *    the docstring prints X's last dimension as H/A, read here as H/NH).
  *
  * Readings taken where the pages leave a step open:
  *  - The score is divided by sqrt(HS) in fp64 (the definition), where the
@@ -186,5 +190,32 @@ int oracle_dense_rows(double *Y, const uint16_t *X, const uint16_t *W,
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t r = 0; r < n; r++)
         dense_row(Y + r * H, X, W, I, H, rows[r]);
+    return 0;
+}
+
+/*
+ * Batched NT product Y[i][j][k] = sum_l X[i][j][l] * W[i][k][l]
+ * (test_local_padding_ii): X [batch, T1, D], W [batch, T2, D] bf16,
+ * Y [batch, T1, T2] doubles. T1 and T2 may differ (the page uses T1 = T2).
+ */
+int oracle_bmm_nt(double *Y, const uint16_t *X, const uint16_t *W, int64_t batch,
+                  int64_t T1, int64_t T2, int64_t D)
+{
+    if (batch <= 0 || T1 <= 0 || T2 <= 0 || D <= 0)
+        return -2;
+    const int64_t rows = batch * T1;
+#pragma omp parallel for schedule(dynamic, 8)
+    for (int64_t r = 0; r < rows; r++) {
+        const int64_t i = r / T1, j = r % T1;
+        const uint16_t *x = X + (i * T1 + j) * D;
+        double *y = Y + (i * T1 + j) * T2;
+        for (int64_t k = 0; k < T2; k++) {
+            const uint16_t *w = W + (i * T2 + k) * D;
+            double acc = 0.0;
+            for (int64_t l = 0; l < D; l++)
+                acc += bf16_to_double(x[l]) * bf16_to_double(w[l]);
+            y[k] = acc;
+        }
+    }
     return 0;
 }

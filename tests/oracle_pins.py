@@ -273,9 +273,76 @@ def pin_dense_local_padding(o):
     assert np.array_equal(Yt, Y.T)
 
 
+# ------------------------------------------------------ batched NT pins --
+
+def _bmm_random(batch, T1, T2, D, seed):
+    X, W = synth.bmm_input(synth.BmmShape(batch=batch, T1=T1, T2=T2, D=D), seed=seed)
+    return synth.bf16_bits(X).reshape(-1), synth.bf16_bits(W).reshape(-1)
+
+
+def pin_bmm_exact_rational(o):
+    batch, T1, T2, D = 2, 3, 4, 5
+    x, w = _bmm_random(batch, T1, T2, D, 51)
+    xf = _u16_to_f32(x).reshape(batch, T1, D)
+    wf = _u16_to_f32(w).reshape(batch, T2, D)
+    Y = o.bmm_nt(x, w, batch, T1, T2, D)
+    for i in range(batch):
+        for j in range(T1):
+            for k in range(T2):
+                exact = sum((Fraction(float(xf[i, j, l])) * Fraction(float(wf[i, k, l]))
+                             for l in range(D)), Fraction(0))
+                assert abs(Y[i, j, k] - float(exact)) <= 1e-15 * (1 + abs(float(exact)))
+
+
+def pin_bmm_matmul_identity(o):
+    for (batch, T1, T2, D, seed) in [(3, 17, 29, 24, 52), (2, 120, 120, 64, 53)]:
+        x, w = _bmm_random(batch, T1, T2, D, seed)
+        xf = torch.from_numpy(_u16_to_f32(x).astype(np.float64).reshape(batch, T1, D))
+        wf = torch.from_numpy(_u16_to_f32(w).astype(np.float64).reshape(batch, T2, D))
+        want = torch.bmm(xf, wf.transpose(1, 2)).numpy()
+        Y = o.bmm_nt(x, w, batch, T1, T2, D)
+        assert np.max(np.abs(Y - want) / (1 + np.abs(want))) <= 1e-12
+
+
+def pin_bmm_integer_exact_and_structure(o):
+    """Small integers: exact against int64; swapping X and W transposes each
+    batch; each batch depends only on its own inputs."""
+    rng = np.random.default_rng(13)
+    batch, T1, T2, D = 3, 9, 7, 16
+    Xi = rng.integers(-4, 5, size=(batch, T1, D)).astype(np.int64)
+    Wi = rng.integers(-4, 5, size=(batch, T2, D)).astype(np.int64)
+    xb, wb = _bits_of(Xi.astype(np.float32)), _bits_of(Wi.astype(np.float32))
+    Y = o.bmm_nt(xb, wb, batch, T1, T2, D)
+    assert np.array_equal(Y, np.einsum("bjl,bkl->bjk", Xi, Wi).astype(np.float64))
+    Yt = o.bmm_nt(wb, xb, batch, T2, T1, D)
+    assert np.array_equal(Yt, Y.transpose(0, 2, 1))
+    Wi2 = Wi.copy()
+    Wi2[1] = -Wi2[1]
+    Y2 = o.bmm_nt(xb, _bits_of(Wi2.astype(np.float32)), batch, T1, T2, D)
+    assert np.array_equal(Y2[[0, 2]], Y[[0, 2]]) and np.array_equal(Y2[1], -Y[1])
+
+
+def pin_bmm_vs_causal_score(o):
+    """The causal score of "trimat_forward.cu" is the lower triangle of the batched
+    NT product of its Q and K heads, divided by sqrt(HS); checked between two
+    independently written oracle functions."""
+    B, T, NH, HS = 2, 21, 2, 16
+    qkv = _random_qkv(B, T, NH, HS, 61)
+    q5 = qkv.reshape(B, T, 3, NH, HS)
+    Q = np.ascontiguousarray(q5[:, :, 0].transpose(0, 2, 1, 3)).reshape(-1)
+    K = np.ascontiguousarray(q5[:, :, 1].transpose(0, 2, 1, 3)).reshape(-1)
+    Y = o.bmm_nt(Q, K, B * NH, T, T, HS).reshape(B, NH, T, T)
+    S = o.trimul(qkv, B, T, NH * HS, NH, MASK_NAN)
+    lower = np.tril(np.ones((T, T), dtype=bool))
+    assert np.array_equal(S[..., lower], Y[..., lower] / math.sqrt(HS))
+
+
+BMM_PINS = [pin_bmm_exact_rational, pin_bmm_matmul_identity, pin_bmm_integer_exact_and_structure,
+            pin_bmm_vs_causal_score]
+
 TRIMUL_PINS = [pin_trimul_exact_rational, pin_trimul_matmul_identity, pin_trimul_closed_forms,
                pin_trimul_integer_exact, pin_trimul_index_roles, pin_trimul_mask_and_causality,
                pin_trimul_rows]
 DENSE_PINS = [pin_dense_exact_rational, pin_dense_matmul_identity, pin_dense_integer_exact,
               pin_dense_local_padding]
-ALL_PINS = TRIMUL_PINS + DENSE_PINS
+ALL_PINS = TRIMUL_PINS + DENSE_PINS + BMM_PINS

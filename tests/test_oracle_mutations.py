@@ -35,6 +35,11 @@ MUTATIONS = [
     ("dense_transposed_w", "W[j * I + k]", "W[k * H + j]", oracle_pins.DENSE_PINS),
     ("dense_drops_last_k", "k < I; k++", "k < I - 1; k++", oracle_pins.DENSE_PINS),
     ("dense_sign", "dst[j] = acc;", "dst[j] = -acc;", oracle_pins.DENSE_PINS),
+    ("bmm_drops_last_term", "l < D; l++)", "l < D - 1; l++)", oracle_pins.BMM_PINS),
+    ("bmm_sign", "y[k] = acc;", "y[k] = -acc;", oracle_pins.BMM_PINS),
+    ("bmm_rows_reversed", "x = X + (i * T1 + j) * D", "x = X + (i * T1 + (T1 - 1 - j)) * D",
+     oracle_pins.BMM_PINS),
+    ("bmm_batch_ignored_in_w", "w = W + (i * T2 + k) * D", "w = W + k * D", oracle_pins.BMM_PINS),
     ("dense_bf16_truncated", "(uint32_t)h << 16", "((uint32_t)h << 16) & 0xFFFE0000u",
      oracle_pins.ALL_PINS),
 ]
