@@ -187,6 +187,27 @@ csa_status trimul_forward(float* out, const void* qkv, int B, int T, int C, int 
   return trimul_forward_ex(out, qkv, B, T, C, NH, CSA_MASK_NAN, CSA_TRIMUL_FULL, nullptr);
 }
 
+csa_status batch_matmul_nt(float* Y, const void* X, const void* W, int batch, int T1, int T2,
+                           int D, void* stream) {
+  t_last_error.clear();
+  if (!Y || !X || !W) return set_error(CSA_ERR_NULL, "batch_matmul_nt: null pointer");
+  if (batch <= 0 || T1 <= 0 || T2 <= 0 || D <= 0)
+    return set_error(CSA_ERR_SHAPE, "batch_matmul_nt: batch, T1, T2, D must be >= 1");
+  if (D % 8 != 0)
+    return set_error(CSA_ERR_ALIGN, "batch_matmul_nt: D must be a multiple of 8");
+  if (D > 256) return set_error(CSA_ERR_UNSUPPORTED, "batch_matmul_nt: D > 256");
+  if (reinterpret_cast<uintptr_t>(X) % 16 || reinterpret_cast<uintptr_t>(W) % 16 ||
+      reinterpret_cast<uintptr_t>(Y) % 4)
+    return set_error(CSA_ERR_ALIGN, "batch_matmul_nt: X, W need 16-byte and Y 4-byte alignment");
+  DeviceInfo dev;
+  std::string err;
+  int rc = current_device(dev, err);
+  if (rc != CSA_OK) return set_error(rc, err);
+  rc = bmm_nt_launch(Y, X, W, batch, T1, T2, D, static_cast<cudaStream_t>(stream), dev, err);
+  if (rc != CSA_OK) return set_error(rc, err);
+  return CSA_OK;
+}
+
 csa_status dense_xwt_ex(float* Y, const void* X, const void* W, int M, int I, int H,
                         void* stream) {
   t_last_error.clear();

@@ -63,7 +63,10 @@ constexpr int kTmemCols = 2 * kTile;
 constexpr uint32_t kIdesc = idesc_bf16_f32(kTile, kTile);
 
 struct TrimulArgs {
-  int T, NH, BH, Tt;
+  int T, T2, BH, Tt, Tt2;  // rows / columns of each (b, h) output and their tile counts
+  int nh_div, b_off;       // operand coordinates: A (bh % nh_div), B (b_off + bh % nh_div),
+                           // both at outer index bh / nh_div
+  uint32_t causal;         // 1: triangular tiles, mask above the diagonal; 0: all tiles
   int kchunks, ksteps, stages;
   long long n_lower;  // tiles with t2-tile <= t-tile: MMA + epilogue
   long long n_fill;   // tiles with t2-tile > t-tile: mask stores only (0 in lower-only mode)
@@ -127,6 +130,18 @@ __device__ __forceinline__ void decode_lower(int r, int& ti, int& tj) {
   tj = r - ti * (ti + 1) / 2;
 }
 
+// Computed tile number r of one (b, h): the lower triangle in causal mode, row
+// by row over all Tt2 column tiles otherwise.
+__device__ __forceinline__ void decode_computed(int r, uint32_t causal, int Tt2, int& ti,
+                                                int& tj) {
+  if (causal) {
+    decode_lower(r, ti, tj);
+  } else {
+    ti = r / Tt2;
+    tj = r - ti * Tt2;
+  }
+}
+
 // Fill tile number r (j > i) of one (b, h): the transpose of the strictly-lower
 // enumeration.
 __device__ __forceinline__ void decode_fill(int r, int& ti, int& tj) {
@@ -136,7 +151,8 @@ __device__ __forceinline__ void decode_fill(int r, int& ti, int& tj) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    trimul_sm103a_kernel(const __grid_constant__ CUtensorMap tmap_qkv,
+    trimul_sm103a_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                         const __grid_constant__ CUtensorMap tmap_b,
                          const __grid_constant__ CUtensorMap tmap_out, const TrimulArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -198,7 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0) {
-      tma_prefetch_map(&tmap_qkv);
+      tma_prefetch_map(&tmap_a);
+      tma_prefetch_map(&tmap_b);
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;  // per-stage: loads that may be in flight
@@ -239,19 +256,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (done) break;
         int bh, r, ti, tj;
         if (position_is_fill(static_cast<int>(cur), a.per_lower, a.per_fill, bh, r)) continue;
-        decode_lower(r, ti, tj);
+        decode_computed(r, a.causal, a.Tt2, ti, tj);
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, wd, kSiteProducerEmpty)) break;
-        const int b = bh / a.NH, h = bh - b * a.NH;
+        const int outer = bh / a.nh_div, inner = bh - outer * a.nh_div;
         mbar_arrive_expect_tx(full_bar(stage), tx);
         if (a.inject && !injected) {
           injected = true;  // withhold this CTA's first loads: its consumer's wait must run out
           issued &= ~(1u << stage);
         } else {
           for (int kc = 0; kc < a.kchunks; ++kc) {
-            tma_load_4d(q_chunk(stage, kc), &tmap_qkv, full_bar(stage), kc * kChunkElems, h,
-                        ti * kTile, b);
-            tma_load_4d(k_chunk(stage, kc), &tmap_qkv, full_bar(stage), kc * kChunkElems,
-                        a.NH + h, tj * kTile, b);
+            tma_load_4d(q_chunk(stage, kc), &tmap_a, full_bar(stage), kc * kChunkElems, inner,
+                        ti * kTile, outer);
+            tma_load_4d(k_chunk(stage, kc), &tmap_b, full_bar(stage), kc * kChunkElems,
+                        a.b_off + inner, tj * kTile, outer);
           }
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -330,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = static_cast<int>(warp & 3u);
     const int slab = static_cast<int>(ew >> 2);
     const uint32_t staging = base + a.off_staging + ew * a.store_groups * 2u * kBoxBytes;
-    const int T = a.T;
+    const int T = a.T, T2 = a.T2;  // output rows and columns of one (b, h)
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t grp = 0;
@@ -357,25 +374,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool is_fill =
           position_is_fill(static_cast<int>(cur), a.per_lower, a.per_fill, bh, rank);
       if (is_fill) decode_fill(rank, ti, tj);
-      else decode_lower(rank, ti, tj);
+      else decode_computed(rank, a.causal, a.Tt2, ti, tj);
       const int row0 = ti * kTile + q * 32;
       const int colw = tj * kTile + slab * kSlabCols;
       if (is_fill) {
         // Fill tile: mask pattern only (full mode).
-        if (row0 >= T || colw >= T) continue;
+        if (row0 >= T || colw >= T2) continue;
         if (a.tma_store) {
           if (lane == 0) {
             tma_store_3d(&tmap_out, mask_box, colw, row0, bh);
-            if (colw + 32 < T) tma_store_3d(&tmap_out, mask_box, colw + 32, row0, bh);
+            if (colw + 32 < T2) tma_store_3d(&tmap_out, mask_box, colw + 32, row0, bh);
             bulk_commit();
           }
         } else {
-          float* orow = a.out + (static_cast<size_t>(bh) * T + row0) * T;
+          float* orow = a.out + (static_cast<size_t>(bh) * T + row0) * T2;
           const float m = __uint_as_float(a.mask_bits);
           for (int rr = 0; rr < 32 && row0 + rr < T; ++rr) {
             for (int c = 0; c < 2; ++c) {
               const int col = colw + c * 32 + static_cast<int>(lane);
-              if (col < T) orow[static_cast<size_t>(rr) * T + col] = m;
+              if (col < T2) orow[static_cast<size_t>(rr) * T2 + col] = m;
             }
           }
         }
@@ -397,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_phase ^= 1u;
       }
 
-      const bool diag = (ti == tj);
+      const bool diag = a.causal && ti == tj;
       const int r = row0 + static_cast<int>(lane);
       if (!diag) {
 #pragma unroll
@@ -407,14 +424,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < kSlabCols; ++e)
           v[e] = (colw + e > r) ? a.mask_bits : __float_as_uint(__uint_as_float(v[e]) * a.scale);
       }
-      if (row0 >= T || colw >= T) continue;  // slab wholly past the end (tail tile)
+      if (row0 >= T || colw >= T2) continue;  // slab wholly past the end (tail tile)
 
       // Per 32-column box: 0 skip, 1 TMA store, 2 plain stores, 3 plain stores t2 <= t only.
       int mode[2];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int col0 = colw + c * 32;
-        mode[c] = col0 >= T ? 0 : (a.tma_store ? 1 : 2);
+        mode[c] = col0 >= T2 ? 0 : (a.tma_store ? 1 : 2);
         if (mode[c] != 0 && a.lower_only && diag) {
           if (col0 > row0 + 31) mode[c] = 0;
           else if (col0 + 31 > row0) mode[c] = 3;
@@ -443,13 +460,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 2; ++c) {
         if (mode[c] < 2) continue;
         const int col = colw + c * 32 + static_cast<int>(lane);
-        float* ocol = a.out + (static_cast<size_t>(bh) * T + row0) * T + col;
+        float* ocol = a.out + (static_cast<size_t>(bh) * T + row0) * T2 + col;
         for (int rr = 0; rr < 32; ++rr) {
           const int row = row0 + rr;
-          const bool ok = row < T && col < T && (mode[c] == 2 || col <= row);
+          const bool ok = row < T && col < T2 && (mode[c] == 2 || col <= row);
           const uint32_t val =
               staged_elem_sw128(pair + c * kBoxBytes, static_cast<uint32_t>(rr), lane);
-          if (ok) ocol[static_cast<size_t>(rr) * T] = __uint_as_float(val);
+          if (ok) ocol[static_cast<size_t>(rr) * T2] = __uint_as_float(val);
         }
       }
     }
@@ -474,57 +491,57 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-int trimul_launch(float* out, const void* qkv, int B, int T, int C, int NH, uint32_t mask_bits,
-                  uint32_t flags, cudaStream_t stream, const DeviceInfo& dev, std::string& err,
+namespace {
+
+// One launch of the score kernel over BH (b, h) problems with T x T2 outputs
+// each, given the operand tensor maps (A rows index t, B rows index t2).
+int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& map_b, float* out,
+                  long long BH, int T, int T2, int D, int nh_div, int b_off, bool causal,
+                  bool lower_only, float scale, uint32_t mask_bits, bool inject,
+                  cudaStream_t stream, const DeviceInfo& dev, std::string& err,
                   unsigned int* counters) {
-  const int HS = C / NH;
-  if (HS % 8 != 0) {
-    err = "trimul_forward: HS = C/NH must be a multiple of 8 (TMA row pitch of a head)";
-    return CSA_ERR_ALIGN;
-  }
-  if (HS > 256) {
-    err = "trimul_forward: HS > 256 is not supported";
-    return CSA_ERR_UNSUPPORTED;
-  }
-  if (reinterpret_cast<uintptr_t>(qkv) % 16 != 0 || reinterpret_cast<uintptr_t>(out) % 4 != 0) {
-    err = "trimul_forward: qkv must be 16-byte aligned and out 4-byte aligned";
-    return CSA_ERR_ALIGN;
-  }
-  const long long BH = static_cast<long long>(B) * NH;
-  if (BH > (1LL << 30) || static_cast<long long>(T) > (1LL << 30)) {
-    err = "trimul_forward: B*NH or T too large";
+  const std::string name(who);
+  if (BH > (1LL << 30) || static_cast<long long>(T) > (1LL << 30) ||
+      static_cast<long long>(T2) > (1LL << 30)) {
+    err = name + ": too many (b, h) problems or too long a sequence";
     return CSA_ERR_SHAPE;
   }
-  const bool lower_only = (flags & CSA_TRIMUL_LOWER_ONLY) != 0;
-
   TrimulArgs a{};
   a.T = T;
-  a.NH = NH;
+  a.T2 = T2;
   a.BH = static_cast<int>(BH);
   a.Tt = (T + kTile - 1) / kTile;
-  a.kchunks = (HS + kChunkElems - 1) / kChunkElems;
-  a.ksteps = (HS + 15) / 16;
-  a.n_lower = BH * (static_cast<long long>(a.Tt) * (a.Tt + 1) / 2);
-  a.n_fill = lower_only ? 0 : BH * (static_cast<long long>(a.Tt) * (a.Tt - 1) / 2);
-  if (a.n_lower + a.n_fill >= (1LL << 31) - (1LL << 20)) {
-    err = "trimul_forward: too many tiles";
+  a.Tt2 = (T2 + kTile - 1) / kTile;
+  a.nh_div = nh_div;
+  a.b_off = b_off;
+  a.causal = causal ? 1u : 0u;
+  a.kchunks = (D + kChunkElems - 1) / kChunkElems;
+  a.ksteps = (D + 15) / 16;
+  const long long per_lower = causal ? static_cast<long long>(a.Tt) * (a.Tt + 1) / 2
+                                     : static_cast<long long>(a.Tt) * a.Tt2;
+  const long long per_fill =
+      (causal && !lower_only) ? static_cast<long long>(a.Tt) * (a.Tt - 1) / 2 : 0;
+  a.n_lower = BH * per_lower;
+  a.n_fill = BH * per_fill;
+  if (a.n_lower + a.n_fill >= (1LL << 31) - (1LL << 20) || per_lower + per_fill >= (1LL << 20)) {
+    err = name + ": too many tiles";
     return CSA_ERR_SHAPE;
   }
   a.n_total = static_cast<int>(a.n_lower + a.n_fill);
-  a.per_lower = a.Tt * (a.Tt + 1) / 2;
-  a.per_fill = lower_only ? 0 : a.Tt * (a.Tt - 1) / 2;
-  a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(HS)));
+  a.per_lower = static_cast<int>(per_lower);
+  a.per_fill = static_cast<int>(per_fill);
+  a.scale = scale;
   a.mask_bits = mask_bits;
   a.lower_only = lower_only ? 1u : 0u;
-  a.tma_store = (T % 4 == 0 && reinterpret_cast<uintptr_t>(out) % 16 == 0) ? 1u : 0u;
+  a.tma_store = (T2 % 4 == 0 && reinterpret_cast<uintptr_t>(out) % 16 == 0) ? 1u : 0u;
   a.out = out;
   a.status = dev.status_word;
   a.wait_limit_ns = wait_limit_ns();
-  a.inject = take_inject() ? 1 : 0;
+  a.inject = inject ? 1 : 0;
 
   // Shared memory: operand ring | staging boxes | mask box | barriers | misc.
-  // Operand ring stages vs. staging depth: two box pairs per epilogue warp when
-  // that still leaves two ring stages, else one pair.
+  // Operand ring stages vs. staging depth: the most box pairs per epilogue warp
+  // that still leave two ring stages, else one pair.
   a.stage_bytes = static_cast<uint32_t>(a.kchunks) * 2u * kChunkBytes;
   const int fixed = kBoxBytes + 1024 /*bars+misc+ring*/ + 1024 /*align slack*/;
   int staging_bytes = 0;
@@ -532,11 +549,11 @@ int trimul_launch(float* out, const void* qkv, int B, int T, int C, int NH, uint
     staging_bytes = kEpiWarps * groups * 2 * kBoxBytes;
     a.store_groups = static_cast<uint32_t>(groups);
     a.stages = std::min(CSA_TRIMUL_MAX_STAGES, (dev.max_smem_optin - fixed - staging_bytes) /
-                               static_cast<int>(a.stage_bytes));
+                                                   static_cast<int>(a.stage_bytes));
     if (a.stages >= 2) break;
   }
   if (a.stages < 1) {
-    err = "trimul_forward: not enough shared memory for one operand stage";
+    err = name + ": not enough shared memory for one operand stage";
     return CSA_ERR_UNSUPPORTED;
   }
   a.off_staging = static_cast<uint32_t>(a.stages) * a.stage_bytes;
@@ -545,22 +562,12 @@ int trimul_launch(float* out, const void* qkv, int B, int T, int C, int NH, uint
   a.off_misc = a.off_bars + 8u * static_cast<uint32_t>(2 * a.stages + 5 + 2 * kSchedDepth);
   const size_t smem = a.off_misc + 16 + 4 * kSchedDepth + 1024;
 
-  CUtensorMap map_qkv, map_out;
-  {
-    const uint64_t dims[4] = {static_cast<uint64_t>(HS), static_cast<uint64_t>(3 * NH),
-                              static_cast<uint64_t>(T), static_cast<uint64_t>(B)};
-    const uint64_t strides[3] = {static_cast<uint64_t>(HS) * 2, static_cast<uint64_t>(C) * 6,
-                                 static_cast<uint64_t>(T) * C * 6};
-    const uint32_t box[4] = {kChunkElems, 1, kTile, 1};
-    int rc = encode_tiled(&map_qkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, qkv, dims, strides, box,
-                          CU_TENSOR_MAP_SWIZZLE_128B, err);
-    if (rc != CSA_OK) return rc;
-  }
+  CUtensorMap map_out;
   if (a.tma_store) {
-    const uint64_t dims[3] = {static_cast<uint64_t>(T), static_cast<uint64_t>(T),
+    const uint64_t dims[3] = {static_cast<uint64_t>(T2), static_cast<uint64_t>(T),
                               static_cast<uint64_t>(BH)};
-    const uint64_t strides[2] = {static_cast<uint64_t>(T) * 4,
-                                 static_cast<uint64_t>(T) * static_cast<uint64_t>(T) * 4};
+    const uint64_t strides[2] = {static_cast<uint64_t>(T2) * 4,
+                                 static_cast<uint64_t>(T) * static_cast<uint64_t>(T2) * 4};
     const uint32_t box[3] = {32, 32, 1};
     int rc = encode_tiled(&map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, out, dims, strides, box,
                           CU_TENSOR_MAP_SWIZZLE_128B, err);
@@ -577,14 +584,14 @@ int trimul_launch(float* out, const void* qkv, int B, int T, int C, int NH, uint
     static std::atomic<unsigned int> launch_seq{0};
     std::lock_guard<std::mutex> lock(mu);
     if (dev.device < 0 || dev.device >= 64) {
-      err = "trimul_forward: device ordinal out of range";
+      err = name + ": device ordinal out of range";
       return CSA_ERR_CUDA;
     }
     if (!sched_base[dev.device]) {
       void* p = nullptr;
       cudaError_t se = cudaGetSymbolAddress(&p, g_trimul_sched);
       if (se != cudaSuccess) {
-        err = std::string("trimul_forward: cudaGetSymbolAddress: ") + cudaGetErrorString(se);
+        err = name + ": cudaGetSymbolAddress: " + cudaGetErrorString(se);
         return CSA_ERR_CUDA;
       }
       sched_base[dev.device] = static_cast<unsigned int*>(p);
@@ -595,18 +602,88 @@ int trimul_launch(float* out, const void* qkv, int B, int T, int C, int NH, uint
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) {
-    err = std::string("trimul_forward: cudaFuncSetAttribute: ") + cudaGetErrorString(e);
+    err = name + ": cudaFuncSetAttribute: " + cudaGetErrorString(e);
     return CSA_ERR_LAUNCH;
   }
   const long long grid = std::min<long long>(a.n_total, dev.sm_count);
-  trimul_sm103a_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(map_qkv, map_out,
-                                                                                a);
+  trimul_sm103a_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(map_a, map_b,
+                                                                                map_out, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
-    err = std::string("trimul_forward: launch: ") + cudaGetErrorString(e);
+    err = name + ": launch: " + cudaGetErrorString(e);
     return CSA_ERR_LAUNCH;
   }
   return CSA_OK;
+}
+
+}  // namespace
+
+int trimul_launch(float* out, const void* qkv, int B, int T, int C, int NH, uint32_t mask_bits,
+                  uint32_t flags, cudaStream_t stream, const DeviceInfo& dev, std::string& err,
+                  unsigned int* counters) {
+  const int HS = C / NH;
+  if (HS % 8 != 0) {
+    err = "trimul_forward: HS = C/NH must be a multiple of 8 (TMA row pitch of a head)";
+    return CSA_ERR_ALIGN;
+  }
+  if (HS > 256) {
+    err = "trimul_forward: HS > 256 is not supported";
+    return CSA_ERR_UNSUPPORTED;
+  }
+  if (reinterpret_cast<uintptr_t>(qkv) % 16 != 0 || reinterpret_cast<uintptr_t>(out) % 4 != 0) {
+    err = "trimul_forward: qkv must be 16-byte aligned and out 4-byte aligned";
+    return CSA_ERR_ALIGN;
+  }
+  // Q of head h is index h and its key index NH + h along the (3, NH) axis of
+  // the packed tensor, read in place.
+  CUtensorMap map_qkv;
+  {
+    const uint64_t dims[4] = {static_cast<uint64_t>(HS), static_cast<uint64_t>(3 * NH),
+                              static_cast<uint64_t>(T), static_cast<uint64_t>(B)};
+    const uint64_t strides[3] = {static_cast<uint64_t>(HS) * 2, static_cast<uint64_t>(C) * 6,
+                                 static_cast<uint64_t>(T) * C * 6};
+    const uint32_t box[4] = {kChunkElems, 1, kTile, 1};
+    int rc = encode_tiled(&map_qkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, qkv, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B, err);
+    if (rc != CSA_OK) return rc;
+  }
+  const float scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(HS)));
+  return launch_scores("trimul_forward", map_qkv, map_qkv, out, static_cast<long long>(B) * NH, T,
+                       T, HS, NH, NH, true, (flags & CSA_TRIMUL_LOWER_ONLY) != 0, scale,
+                       mask_bits, take_inject(), stream, dev, err, counters);
+}
+
+int bmm_nt_launch(float* Y, const void* X, const void* W, int batch, int T1, int T2, int D,
+                  cudaStream_t stream, const DeviceInfo& dev, std::string& err) {
+  if (D % 8 != 0) {
+    err = "batch_matmul_nt: D must be a multiple of 8 (TMA row pitch)";
+    return CSA_ERR_ALIGN;
+  }
+  if (D > 256) {
+    err = "batch_matmul_nt: D > 256 is not supported";
+    return CSA_ERR_UNSUPPORTED;
+  }
+  if (reinterpret_cast<uintptr_t>(X) % 16 != 0 || reinterpret_cast<uintptr_t>(W) % 16 != 0 ||
+      reinterpret_cast<uintptr_t>(Y) % 4 != 0) {
+    err = "batch_matmul_nt: X and W must be 16-byte aligned and Y 4-byte aligned";
+    return CSA_ERR_ALIGN;
+  }
+  // X [batch, T1, D] and W [batch, T2, D] as 4-D maps (D, 1, rows, batch) so the
+  // kernel addresses them like the packed tensor with a single head.
+  CUtensorMap map_x, map_w;
+  for (int which = 0; which < 2; ++which) {
+    const int rows = which == 0 ? T1 : T2;
+    const uint64_t dims[4] = {static_cast<uint64_t>(D), 1, static_cast<uint64_t>(rows),
+                              static_cast<uint64_t>(batch)};
+    const uint64_t strides[3] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(D) * 2,
+                                 static_cast<uint64_t>(rows) * D * 2};
+    const uint32_t box[4] = {kChunkElems, 1, kTile, 1};
+    int rc = encode_tiled(which == 0 ? &map_x : &map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                          which == 0 ? X : W, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, err);
+    if (rc != CSA_OK) return rc;
+  }
+  return launch_scores("batch_matmul_nt", map_x, map_w, Y, batch, T1, T2, D, 1, 0, false, false,
+                       1.0f, 0u, false, stream, dev, err, nullptr);
 }
 
 // ---------------------------------------------------- allocation-free variant --

@@ -62,6 +62,18 @@ def dense_xwt(Y: torch.Tensor, X: torch.Tensor, W: torch.Tensor, M: int, I: int,
     _lib.check(rc, "dense_xwt")
 
 
+def batch_matmul_nt(Y: torch.Tensor, X: torch.Tensor, W: torch.Tensor, batch: int, T1: int,
+                    T2: int, D: int, stream=None) -> None:
+    """Y[i, j, k] = sum_l X[i, j, l] W[i, k, l]: bf16 X [batch, T1, D], W [batch, T2, D]
+    into fp32 Y [batch, T1, T2]."""
+    _need(X, "X", torch.bfloat16, batch * T1 * D)
+    _need(W, "W", torch.bfloat16, batch * T2 * D)
+    _need(Y, "Y", torch.float32, batch * T1 * T2)
+    rc = _lib.load().batch_matmul_nt(Y.data_ptr(), X.data_ptr(), W.data_ptr(), batch, T1, T2, D,
+                                     _stream_ptr(stream))
+    _lib.check(rc, "batch_matmul_nt")
+
+
 def trimul(qkv: torch.Tensor, mask="nan", lower_only: bool = False, stream=None) -> torch.Tensor:
     """Allocating form: qkv (B, T, 3, NH, HS) bf16 -> scores (B, NH, T, T) fp32."""
     B, T, three, NH, HS = qkv.shape

@@ -143,6 +143,22 @@ csa_status dense_xwt_ex(float* Y, const void* X, const void* W, int M, int I, in
                         void* stream);
 
 /*
+ * batch_matmul_nt -- the unmasked, unscaled batched NT product of
+ * "DietCode tests/codegen/test_1_local_padding.py" (test_local_padding_ii
+ * docstring, BatchMatmulNT):
+ *   Y[i][j][k] = sum_l X[i][j][l] * W[i][k][l]
+ *   Y  device, fp32, [batch, T1, T2] row-major, fully overwritten.
+ *   X  device, bf16, [batch, T1, D]; W device, bf16, [batch, T2, D].
+ *   batch, T1, T2 >= 1 (any values: rows and columns past T1 / T2 are
+ *   zero-filled on fetch and clipped on store), D % 8 == 0, D <= 256.
+ * X and W 16-byte aligned, Y 4-byte aligned (TMA stores when T2 % 4 == 0 and Y
+ * is 16-byte aligned). Same kernel as trimul_forward with every tile computed
+ * and no mask or scale. Asynchronous on `stream` (cudaStream_t as void*).
+ */
+csa_status batch_matmul_nt(float* Y, const void* X, const void* W, int batch, int T1, int T2,
+                           int D, void* stream);
+
+/*
  * csa_get_status -- synchronises `stream`, then returns and clears the current
  * device's status word: CSA_OK, or CSA_ERR_TIMEOUT if a kernel's bounded wait
  * ran out since the last call. Returns CSA_ERR_CUDA if synchronisation fails.
