@@ -219,37 +219,168 @@ def measured_peaks():
 
 # ------------------------------------------------------------ our arm --
 
-def run_ours(args, rank, world, local):
+class Workload:
+    """What one step runs: launch functions timed back to back with CUDA events,
+    the useful flops of a step, the dominant kernel's roofline terms, and the
+    host<->device copies of the end-to-end variant."""
+
+    def __init__(self, name, config, parts, flops, roof, h2d, d2h):
+        self.name = name          # human-readable workload string (config.workload)
+        self.config = config      # extra config keys
+        self.parts = parts        # [(label, fn(stream))]
+        self.flops = flops        # useful flops per step
+        self.roof = roof          # dict: part, kernel, bound, per_launch (bytes or flops)
+        self.h2d = h2d            # [(device tensor, host tensor)]
+        self.d2h = d2h            # [(host tensor, device tensor)]
+
+
+def make_workload(name, dev):
     import torch
 
     import causal_attention_score_gb300 as csa
     from causal_attention_score_gb300 import synth
 
+    def trimul_part(shape, lower_only=False, seed=0):
+        qkv_h = synth.trimul_input(shape, seed=seed, dist="normal")
+        qkv = qkv_h.to(dev)
+        out = torch.empty(shape.out_shape, dtype=torch.float32, device=dev)
+        fn = lambda st: csa.trimul_forward(out, qkv, shape.B, shape.T, shape.C, shape.NH,
+                                           lower_only=lower_only, stream=st)
+        return fn, [(qkv, qkv_h)], [out]
+
+    def dense_part(shape, seed=0):
+        X_h, W_h = synth.dense_input(shape, seed=seed)
+        X, W = X_h.to(dev), W_h.to(dev)
+        Y = torch.empty((shape.M, shape.H), dtype=torch.float32, device=dev)
+        fn = lambda st: csa.dense_xwt(Y, X, W, shape.M, shape.I, shape.H, stream=st)
+        return fn, [(X, X_h), (W, W_h)], [Y]
+
+    def pinned_like(t):
+        return torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+
+    def finish(wl_name, config, parts, flops, roof, h2d, outs):
+        h2d = [(d, h.pin_memory()) for d, h in h2d]
+        d2h = [(pinned_like(o), o) for o in outs]
+        return Workload(wl_name, config, parts, flops, roof, h2d, d2h)
+
+    ts, ds = synth.TRIMUL_GPT2, synth.DENSE_RAGGED
+    if name == "step":
+        tf, th, to = trimul_part(ts)
+        df, dh, do = dense_part(ds)
+        return finish(
+            "trimul GPT-2-small (B=8,T=1024,C=768,NH=12,HS=64) + dense ragged "
+            "(M=960,I=770,H=768), one call each per step",
+            {"trimul": {"B": ts.B, "T": ts.T, "C": ts.C, "NH": ts.NH, "mask": "NaN"},
+             "dense": {"M": ds.M, "I": ds.I, "H": ds.H}},
+            [("trimul", tf), ("dense", df)],
+            trimul_flops(ts.B, ts.T, ts.C, ts.NH) + dense_flops(ds.M, ds.I, ds.H),
+            {"part": 0, "kernel": "trimul_sm103a_kernel", "bound": "hbm",
+             "per_launch": trimul_algorithmic_bytes(ts.B, ts.T, ts.C, ts.NH)},
+            th + dh, to + do)
+    if name in ("trimul_gpt2", "trimul_long", "trimul_gpt2_lower", "trimul_long_lower"):
+        shape = synth.TRIMUL_GPT2 if "gpt2" in name else synth.TRIMUL_LONG
+        lower = name.endswith("_lower")
+        tf, th, to = trimul_part(shape, lower_only=lower)
+        return finish(
+            f"trimul {'GPT-2-small' if 'gpt2' in name else 'long context'} (B={shape.B},"
+            f"T={shape.T},C={shape.C},NH={shape.NH},HS={shape.HS})"
+            + (", lower triangle only" if lower else ""),
+            {"trimul": {"B": shape.B, "T": shape.T, "C": shape.C, "NH": shape.NH,
+                        "mask": "untouched" if lower else "NaN"}},
+            [("trimul", tf)], trimul_flops(shape.B, shape.T, shape.C, shape.NH),
+            {"part": 0, "kernel": "trimul_sm103a_kernel", "bound": "hbm",
+             "per_launch": trimul_algorithmic_bytes(shape.B, shape.T, shape.C, shape.NH, lower)},
+            th, to)
+    if name == "dense_ragged":
+        df, dh, do = dense_part(ds)
+        return finish("dense ragged (M=960,I=770,H=768)", {"dense": {"M": ds.M, "I": ds.I,
+                                                                     "H": ds.H}},
+                      [("dense", df)], dense_flops(ds.M, ds.I, ds.H),
+                      {"part": 0, "kernel": "dense_sm103a_kernel", "bound": "tensor",
+                       "per_launch": dense_flops(ds.M, ds.I, ds.H)}, dh, do)
+    if name == "dense_sweep":
+        xs_h, W_h = synth.dense_sweep_inputs(seed=0)
+        W = W_h.to(dev)
+        H, I = W_h.shape
+        parts, h2d, outs, flops = [], [(W, W_h)], [], 0
+        for i, X_h in enumerate(xs_h):
+            X = X_h.to(dev)
+            M = X_h.shape[0]
+            Y = torch.empty((M, H), dtype=torch.float32, device=dev)
+            parts.append((f"call{i}", (lambda X, Y, M: lambda st: csa.dense_xwt(
+                Y, X, W, M, I, H, stream=st))(X, Y, M)))
+            h2d.append((X, X_h))
+            outs.append(Y)
+            flops += dense_flops(M, I, H)
+        return finish("dense dynamic-shape sweep: 32 calls, M = 16*T, T ~ U{1..128} (seed 0), "
+                      "I=768, H=3072", {"dense_sweep": {"calls": len(xs_h), "I": I, "H": H}},
+                      parts, flops, {"part": None, "kernel": "dense_sm103a_kernel",
+                                     "bound": "tensor", "per_launch": flops}, h2d, outs)
+    if name == "bmm_nt":
+        bs = synth.BMM_NT_RAGGED
+        X_h, W_h = synth.bmm_input(bs, seed=0)
+        X, W = X_h.to(dev), W_h.to(dev)
+        Y = torch.empty((bs.batch, bs.T1, bs.T2), dtype=torch.float32, device=dev)
+        fn = lambda st: csa.batch_matmul_nt(Y, X, W, bs.batch, bs.T1, bs.T2, bs.D, stream=st)
+        flops = 2 * bs.batch * bs.T1 * bs.T2 * bs.D
+        nbytes = bs.batch * bs.T1 * bs.T2 * 4 + bs.batch * (bs.T1 + bs.T2) * bs.D * 2
+        return finish("batched NT product (B*NH=192, T=120, D=64; DietCode BatchMatmulNT)",
+                      {"bmm_nt": {"batch": bs.batch, "T1": bs.T1, "T2": bs.T2, "D": bs.D}},
+                      [("bmm_nt", fn)], flops,
+                      {"part": 0, "kernel": "trimul_sm103a_kernel", "bound": "hbm",
+                       "per_launch": nbytes}, [(X, X_h), (W, W_h)], [Y])
+    raise ValueError(f"unknown workload {name}")
+
+
+WORKLOADS = ["step", "trimul_gpt2", "trimul_long", "trimul_gpt2_lower", "trimul_long_lower",
+             "dense_ragged", "dense_sweep", "bmm_nt"]
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import causal_attention_score_gb300 as csa
+
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    ts, ds = synth.TRIMUL_GPT2, synth.DENSE_RAGGED
-    qkv_h = synth.trimul_input(ts, seed=0, dist="normal")
-    X_h, W_h = synth.dense_input(ds, seed=0)
-    qkv = qkv_h.to(dev)
-    X, W = X_h.to(dev), W_h.to(dev)
-    out = torch.empty(ts.out_shape, dtype=torch.float32, device=dev)
-    Y = torch.empty((ds.M, ds.H), dtype=torch.float32, device=dev)
+    wl = make_workload(args.workload, dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    P = len(wl.parts)
 
     def step():
-        csa.trimul_forward(out, qkv, ts.B, ts.T, ts.C, ts.NH, stream=stream)
-        csa.dense_xwt(Y, X, W, ds.M, ds.I, ds.H, stream=stream)
+        for _, fn in wl.parts:
+            fn(stream)
+
+    graph = None
+    if args.graph:
+        # The step's launches captured once and replayed as one CUDA graph.
+        step()
+        torch.cuda.synchronize(dev)
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            for _, fn in wl.parts:
+                fn(side)
+        torch.cuda.synchronize(dev)
+
+    def run_step():
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
 
     for _ in range(args.warmup):
         flush.zero_()
-        step()
+        run_step()
     torch.cuda.synchronize(dev)
     if csa.get_status(stream) != 0:
         raise RuntimeError("device status not ok after warm-up")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    nev = 2 if graph is not None else P + 1
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(K)]
     sampler = ClockSampler(nvml_index(local))
     barrier(world)
     torch.cuda.synchronize(dev)
@@ -258,10 +389,13 @@ def run_ours(args, rank, world, local):
     for i in range(K):
         flush.zero_()  # evict L2 between steps; not inside the timed events
         ev[i][0].record(stream)
-        csa.trimul_forward(out, qkv, ts.B, ts.T, ts.C, ts.NH, stream=stream)
-        ev[i][1].record(stream)
-        csa.dense_xwt(Y, X, W, ds.M, ds.I, ds.H, stream=stream)
-        ev[i][2].record(stream)
+        if graph is not None:
+            graph.replay()
+            ev[i][1].record(stream)
+        else:
+            for p, (_, fn) in enumerate(wl.parts):
+                fn(stream)
+                ev[i][p + 1].record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
     sampler.stop()
@@ -269,26 +403,20 @@ def run_ours(args, rank, world, local):
     if csa.get_status(stream) != 0:
         raise RuntimeError("device status not ok after the timed steps")
 
-    trimul_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    dense_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    step_ms = [a + b for a, b in zip(trimul_ms, dense_ms)]
+    step_ms = [e[0].elapsed_time(e[-1]) for e in ev]
     total_ms = max_over_ranks(sum(step_ms), world, dev)
-    flops_step = trimul_flops(ts.B, ts.T, ts.C, ts.NH) + dense_flops(ds.M, ds.I, ds.H)
-    value = world * K * flops_step / (total_ms * 1e-3) / 1e12
+    value = world * K * wl.flops / (total_ms * 1e-3) / 1e12
+    part_ms = None
+    if graph is None:
+        part_ms = [statistics.mean(e[p].elapsed_time(e[p + 1]) for e in ev) for p in range(P)]
 
     # End to end through the public API: host (pinned) inputs in, host results out.
-    qkv_p = qkv_h.pin_memory()
-    X_p, W_p = X_h.pin_memory(), W_h.pin_memory()
-    out_p = torch.empty(ts.out_shape, dtype=torch.float32, pin_memory=True)
-    Y_p = torch.empty((ds.M, ds.H), dtype=torch.float32, pin_memory=True)
-
     def e2e_step():
-        qkv.copy_(qkv_p, non_blocking=True)
-        X.copy_(X_p, non_blocking=True)
-        W.copy_(W_p, non_blocking=True)
-        step()
-        out_p.copy_(out, non_blocking=True)
-        Y_p.copy_(Y, non_blocking=True)
+        for d, h in wl.h2d:
+            d.copy_(h, non_blocking=True)
+        run_step()
+        for h, d in wl.d2h:
+            h.copy_(d, non_blocking=True)
 
     for _ in range(max(1, min(args.warmup, 3))):
         e2e_step()
@@ -303,14 +431,31 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     barrier(world)
-    h2d = qkv_h.numel() * 2 + X_h.numel() * 2 + W_h.numel() * 2
-    d2h = out.numel() * 4 + Y.numel() * 4
-    e2e_value = world * ke * flops_step / (e2e_ms * 1e-3) / 1e12
+    h2d = sum(d.numel() * d.element_size() for d, _ in wl.h2d)
+    d2h = sum(d.numel() * d.element_size() for _, d in wl.d2h)
+    e2e_value = world * ke * wl.flops / (e2e_ms * 1e-3) / 1e12
 
     hbm_peak, bf16_peak, peak_src = measured_peaks()
-    trimul_avg_s = statistics.mean(trimul_ms) * 1e-3
-    alg_bytes = trimul_algorithmic_bytes(ts.B, ts.T, ts.C, ts.NH)
-    achieved = alg_bytes / trimul_avg_s / 1e9
+    roof = wl.roof
+    dom_s = (part_ms[roof["part"]] if (part_ms is not None and roof["part"] is not None)
+             else total_ms / K) * 1e-3
+    if roof["bound"] == "hbm":
+        achieved = roof["per_launch"] / dom_s / 1e9
+        roofline = {"kernel": roof["kernel"], "bound": "hbm", "achieved": round(achieved, 1),
+                    "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                    "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst copy)",
+                    "algorithmic_bytes_per_launch": roof["per_launch"],
+                    "traffic": args.traffic if args.workload == "step" else None}
+    else:
+        achieved = roof["per_launch"] / dom_s / 1e12
+        roofline = {"kernel": roof["kernel"], "bound": "tensor", "achieved": round(achieved, 2),
+                    "peak": bf16_peak, "unit": "TFLOP/s", "frac": round(achieved / bf16_peak, 4),
+                    "peak_source": f"{peak_src} (MEASURED_PEAKS.json bf16_tflops, burst cuBLAS)",
+                    "algorithmic_flops_per_launch": roof["per_launch"], "traffic": None}
+    config = {"workload": wl.name, **wl.config,
+              "l2": "flushed between timed steps (256 MiB write, outside the timed events)",
+              "launch": "one CUDA graph per step" if graph is not None else "direct launches",
+              "parallelism": f"replicas x{world}"}
     result = {
         "metric": METRIC,
         "value": round(value, 3),
@@ -324,41 +469,20 @@ def run_ours(args, rank, world, local):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) / uniform[-1,1], rounded to bf16)",
-        "config": {
-            "workload": "trimul GPT-2-small (B=8,T=1024,C=768,NH=12,HS=64) + dense ragged "
-                        "(M=960,I=770,H=768), one call each per step",
-            "trimul": {"B": ts.B, "T": ts.T, "C": ts.C, "NH": ts.NH, "mask": "NaN"},
-            "dense": {"M": ds.M, "I": ds.I, "H": ds.H},
-            "l2": "flushed between timed steps (256 MiB write, outside the timed events)",
-            "parallelism": f"replicas x{world}",
-        },
+        "config": config,
         "pct_of_bf16_peak": round(100 * value / world / bf16_peak, 3),
-        "parts": {
-            "trimul_us": round(statistics.mean(trimul_ms) * 1e3, 2),
-            "dense_us": round(statistics.mean(dense_ms) * 1e3, 2),
-            "trimul_tflops": round(trimul_flops(ts.B, ts.T, ts.C, ts.NH) / trimul_avg_s / 1e12, 2),
-            "dense_tflops": round(dense_flops(ds.M, ds.I, ds.H)
-                                  / (statistics.mean(dense_ms) * 1e-3) / 1e12, 2),
-        },
-        "roofline": {
-            "kernel": "trimul_sm103a_kernel",
-            "bound": "hbm",
-            "achieved": round(achieved, 1),
-            "peak": hbm_peak,
-            "unit": "GB/s",
-            "frac": round(achieved / hbm_peak, 4),
-            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst copy)",
-            "algorithmic_bytes_per_launch": alg_bytes,
-            "traffic": args.traffic,
-        },
+        "roofline": roofline,
         "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": ke,
                 "ms_per_step": round(e2e_ms / ke, 4)},
-        "gpu_launches": 2 * K,
+        "gpu_launches": P * K,
         "clocks": sampler.summary(),
         "wall_s_timed_region": round(wall, 4),
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if part_ms is not None and P <= 4:
+        result["parts"] = {f"{label}_us": round(ms * 1e3, 2)
+                           for (label, _), ms in zip(wl.parts, part_ms)}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "step":
         result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     return result
 
@@ -456,6 +580,10 @@ def main(argv=None):
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--workload", choices=WORKLOADS, default="step",
+                   help="what a step runs (default: the headline step)")
+    p.add_argument("--graph", action="store_true",
+                   help="capture each step's launches as one CUDA graph and replay it")
     p.add_argument("--traffic", type=float, default=None,
                    help="dram bytes read+written per trimul launch from an ncu capture")
     args = p.parse_args(argv)
