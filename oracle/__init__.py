@@ -13,6 +13,8 @@ pages it follows:
 * ``dense`` / ``dense_rows``: the dense workload ``Y = X W^T`` of
   "DietCode tests/codegen/test_1_local_padding.py" (test_local_padding
   docstring).
+* ``causal_softmax`` / ``causal_softmax_rows``: the two-pass row softmax of the
+  "Smallem" article 5 (kernels-gpu) over each causal score row (t2 <= t), 0 above.
 * ``bmm_nt``: the batched NT workload of the same file (test_local_padding_ii
   docstring), ``Y[i, j, k] = sum_l X[i, j, l] W[i, k, l]``.
 
@@ -70,8 +72,11 @@ class Oracle:
         self.lib.oracle_dense.argtypes = [dp, up, up, i64, i64, i64]
         self.lib.oracle_dense_rows.argtypes = [dp, up, up, i64, i64, i64, lp, i64]
         self.lib.oracle_bmm_nt.argtypes = [dp, up, up, i64, i64, i64, i64]
+        self.lib.oracle_causal_softmax.argtypes = [dp, up, i64, i64, i64, i64]
+        self.lib.oracle_causal_softmax_rows.argtypes = [dp, up, i64, i64, i64, i64, lp, i64]
         for f in ("oracle_trimul", "oracle_trimul_rows", "oracle_dense", "oracle_dense_rows",
-                  "oracle_bmm_nt", "oracle_num_threads"):
+                  "oracle_bmm_nt", "oracle_causal_softmax", "oracle_causal_softmax_rows",
+                  "oracle_num_threads"):
             getattr(self.lib, f).restype = ctypes.c_int
         self.lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         self.lib.oracle_set_num_threads.restype = None
@@ -152,6 +157,32 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"oracle_bmm_nt rejected the shape (rc={rc})")
         return Y
+
+
+    # -- causal softmax ---------------------------------------------------
+    def causal_softmax(self, qkv_u16: np.ndarray, B: int, T: int, C: int, NH: int) -> np.ndarray:
+        """Softmax over t2 <= t of each causal score row, 0 above; (B, NH, T, T) float64."""
+        q = np.ascontiguousarray(qkv_u16, dtype=np.uint16)
+        if q.size != B * T * 3 * C:
+            raise ValueError("qkv size does not match (B, T, 3, C)")
+        out = np.empty((B, NH, T, T), dtype=np.float64)
+        rc = self.lib.oracle_causal_softmax(_ptr(out, ctypes.c_double), _ptr(q, ctypes.c_uint16),
+                                            B, T, C, NH)
+        if rc != 0:
+            raise ValueError(f"oracle_causal_softmax rejected the shape (rc={rc})")
+        return out
+
+    def causal_softmax_rows(self, qkv_u16: np.ndarray, B: int, T: int, C: int, NH: int,
+                            bht: np.ndarray) -> np.ndarray:
+        q = np.ascontiguousarray(qkv_u16, dtype=np.uint16)
+        idx = np.ascontiguousarray(bht, dtype=np.int64).reshape(-1, 3)
+        out = np.empty((idx.shape[0], T), dtype=np.float64)
+        rc = self.lib.oracle_causal_softmax_rows(_ptr(out, ctypes.c_double),
+                                                 _ptr(q, ctypes.c_uint16), B, T, C, NH,
+                                                 _ptr(idx, ctypes.c_int64), idx.shape[0])
+        if rc != 0:
+            raise ValueError(f"oracle_causal_softmax_rows rejected the arguments (rc={rc})")
+        return out
 
 
 _default: Oracle | None = None

@@ -19,6 +19,11 @@
  *  - "DietCode tests/codegen/test_1_local_padding.py", test_local_padding
  *    docstring, the dense workload: Y[i, j] += X[i, k] * W[j, k], i.e.
  *    Y = X W^T with X [B*T, I], W [H, I], Y [B*T, H].
+ *  - "Smallem" article 5 (kernels-gpu), its two-pass softmax: per row the
+ *    maximum m and the sum of exp(x - m), then exp(x - m) / sum; applied to
+ *    the causal scores of trimul_cpu (whose comment says it is taken from the
+ *    attention forward pass, where a softmax over t2 <= t follows), masked
+ *    positions t2 > t get probability 0.
  *  - the same file, test_local_padding_ii docstring, the batched NT workload:
  *    Y[i, j, k] += X[i, j, l] * W[i, k, l] with X [B*NH, T, H/NH],
  *    W [B*NH, T, H/NH], Y [B*NH, T, T] (the unmasked, unscaled score product;
@@ -217,5 +222,62 @@ int oracle_bmm_nt(double *Y, const uint16_t *X, const uint16_t *W, int64_t batch
             y[k] = acc;
         }
     }
+    return 0;
+}
+
+/*
+ * Causal softmax of the score rows: for each (b, h, t), over t2 <= t,
+ * P[t2] = exp(s[t2] - m) / sum_{u <= t} exp(s[u] - m) with s = the trimul_cpu
+ * score and m = max_{u <= t} s[u]; P[t2] = 0 for t2 > t. (B, NH, T, T) doubles.
+ */
+static void softmax_row(double *dst, const uint16_t *qkv, int64_t T, int64_t C,
+                        int64_t NH, int64_t b, int64_t h, int64_t t)
+{
+    score_row(dst, qkv, T, C, NH, b, h, t, 0.0);
+    double m = dst[0];
+    for (int64_t t2 = 1; t2 <= t; t2++)
+        if (dst[t2] > m)
+            m = dst[t2];
+    double sum = 0.0;
+    for (int64_t t2 = 0; t2 <= t; t2++) {
+        dst[t2] = exp(dst[t2] - m);
+        sum += dst[t2];
+    }
+    for (int64_t t2 = 0; t2 <= t; t2++)
+        dst[t2] /= sum;
+    for (int64_t t2 = t + 1; t2 < T; t2++)
+        dst[t2] = 0.0;
+}
+
+int oracle_causal_softmax(double *out, const uint16_t *qkv, int64_t B, int64_t T,
+                          int64_t C, int64_t NH)
+{
+    if (check_trimul_shape(B, T, C, NH))
+        return -2;
+    const int64_t rows = B * NH * T;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t r = 0; r < rows; r++) {
+        const int64_t t = r % T;
+        const int64_t h = (r / T) % NH;
+        const int64_t b = r / (T * NH);
+        softmax_row(out + r * T, qkv, T, C, NH, b, h, t);
+    }
+    return 0;
+}
+
+/* Selected rows (b, h, t) of the causal softmax, n x T doubles. */
+int oracle_causal_softmax_rows(double *out, const uint16_t *qkv, int64_t B, int64_t T,
+                               int64_t C, int64_t NH, const int64_t *bht, int64_t n)
+{
+    if (check_trimul_shape(B, T, C, NH))
+        return -2;
+    for (int64_t i = 0; i < n; i++) {
+        const int64_t b = bht[3 * i], h = bht[3 * i + 1], t = bht[3 * i + 2];
+        if (b < 0 || b >= B || h < 0 || h >= NH || t < 0 || t >= T)
+            return -2;
+    }
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t i = 0; i < n; i++)
+        softmax_row(out + i * T, qkv, T, C, NH, bht[3 * i], bht[3 * i + 1], bht[3 * i + 2]);
     return 0;
 }

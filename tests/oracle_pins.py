@@ -337,6 +337,70 @@ def pin_bmm_vs_causal_score(o):
     assert np.array_equal(S[..., lower], Y[..., lower] / math.sqrt(HS))
 
 
+# -------------------------------------------------------- softmax pins --
+
+def pin_softmax_matches_library_softmax(o):
+    """Each row equals scipy.special.softmax of the causal score row (t2 <= t); 0 above."""
+    import scipy.special
+    for (B, T, NH, HS, seed, dist) in [(2, 37, 3, 24, 71, "normal"), (1, 130, 2, 64, 72, "uniform")]:
+        qkv = _random_qkv(B, T, NH, HS, seed, dist)
+        P = o.causal_softmax(qkv, B, T, NH * HS, NH)
+        S = o.trimul(qkv, B, T, NH * HS, NH, MASK_NAN)
+        for b in range(B):
+            for h in range(NH):
+                for t in range(T):
+                    want = scipy.special.softmax(S[b, h, t, :t + 1])
+                    assert np.max(np.abs(P[b, h, t, :t + 1] - want)) <= 1e-14
+                    assert np.all(P[b, h, t, t + 1:] == 0.0)
+        assert np.max(np.abs(P.sum(axis=-1) - 1.0)) <= 1e-12
+
+
+def pin_softmax_large_scores_and_closed_form(o):
+    """Scores beyond 709 (where exp overflows in fp64) stay finite and exact against
+    scipy (the row maximum is subtracted); equal scores give 1/(t+1)."""
+    import scipy.special
+    B, T, NH, HS = 1, 12, 1, 16
+    Q = np.zeros((B, T, NH, HS), np.float32)
+    K = np.zeros((B, T, NH, HS), np.float32)
+    for t in range(T):
+        Q[0, t, 0, 0] = 64.0 * (1 if t % 2 else -1)
+        K[0, t, 0, 0] = float(t % 5 - 2) * 16.0  # q.k/4 in [-512, 512]
+        Q[0, t, 0, 1] = 32.0
+        K[0, t, 0, 1] = float(t) * 8.0             # + up to 704: exp() of it overflows fp64
+    qkv = _qkv_from_parts(Q, K, np.zeros_like(Q))
+    P = o.causal_softmax(qkv, B, T, NH * HS, NH)
+    S = o.trimul(qkv, B, T, NH * HS, NH, MASK_NAN)
+    assert np.nanmax(S) > 720
+    assert np.all(np.isfinite(P))
+    for t in range(T):
+        assert np.max(np.abs(P[0, 0, t, :t + 1] - scipy.special.softmax(S[0, 0, t, :t + 1]))) <= 1e-14
+    ones = np.ones((1, 9, 1, 8), np.float32)
+    P1 = o.causal_softmax(_qkv_from_parts(ones, ones, ones), 1, 9, 8, 1)
+    for t in range(9):
+        assert np.all(P1[0, 0, t, :t + 1] == 1.0 / (t + 1))
+        assert np.all(P1[0, 0, t, t + 1:] == 0.0)
+
+
+def pin_softmax_causality_and_rows(o):
+    """Changing key row s changes exactly the rows t >= s; sampled rows match."""
+    B, T, NH, HS = 1, 17, 2, 8
+    qkv = _random_qkv(B, T, NH, HS, 73)
+    P = o.causal_softmax(qkv, B, T, NH * HS, NH)
+    s = 6
+    pert = qkv.reshape(B, T, 3, NH, HS).copy()
+    pert[:, s, 1] = _bits_of(np.full((B, NH, HS), 0.5, np.float32))
+    P2 = o.causal_softmax(pert.reshape(-1), B, T, NH * HS, NH)
+    changed_rows = np.any(P2 != P, axis=-1)  # (B, NH, T)
+    assert not np.any(changed_rows[..., :s]) and np.all(changed_rows[..., s:])
+    bht = np.array([[0, 0, 0], [0, 1, 16], [0, 1, 5]])
+    rows = o.causal_softmax_rows(qkv, B, T, NH * HS, NH, bht)
+    for i, (b, h, t) in enumerate(bht):
+        assert np.array_equal(rows[i], P[b, h, t])
+
+
+SOFTMAX_PINS = [pin_softmax_matches_library_softmax, pin_softmax_large_scores_and_closed_form,
+                pin_softmax_causality_and_rows]
+
 BMM_PINS = [pin_bmm_exact_rational, pin_bmm_matmul_identity, pin_bmm_integer_exact_and_structure,
             pin_bmm_vs_causal_score]
 
@@ -345,4 +409,4 @@ TRIMUL_PINS = [pin_trimul_exact_rational, pin_trimul_matmul_identity, pin_trimul
                pin_trimul_rows]
 DENSE_PINS = [pin_dense_exact_rational, pin_dense_matmul_identity, pin_dense_integer_exact,
               pin_dense_local_padding]
-ALL_PINS = TRIMUL_PINS + DENSE_PINS + BMM_PINS
+ALL_PINS = TRIMUL_PINS + DENSE_PINS + BMM_PINS + SOFTMAX_PINS

@@ -40,6 +40,14 @@ MUTATIONS = [
     ("bmm_rows_reversed", "x = X + (i * T1 + j) * D", "x = X + (i * T1 + (T1 - 1 - j)) * D",
      oracle_pins.BMM_PINS),
     ("bmm_batch_ignored_in_w", "w = W + (i * T2 + k) * D", "w = W + k * D", oracle_pins.BMM_PINS),
+    ("softmax_no_max_subtracted", "if (dst[t2] > m)\n            m = dst[t2];",
+     "if (dst[t2] > m)\n            m = 0.0;", oracle_pins.SOFTMAX_PINS),
+    ("softmax_min_subtracted", "if (dst[t2] > m)", "if (dst[t2] < m)", oracle_pins.SOFTMAX_PINS),
+    ("softmax_sum_drops_diagonal", "t2 <= t; t2++) {\n        dst[t2] = exp",
+     "t2 < t; t2++) {\n        dst[t2] = exp", oracle_pins.SOFTMAX_PINS),
+    ("softmax_multiplies", "dst[t2] /= sum", "dst[t2] *= sum", oracle_pins.SOFTMAX_PINS),
+    ("softmax_upper_not_zero", "dst[t2] = 0.0;\n}", "dst[t2] = 1e-30;\n}", oracle_pins.SOFTMAX_PINS),
+    ("softmax_counts_terms", "sum += dst[t2];", "sum += 1.0;", oracle_pins.SOFTMAX_PINS),
     ("dense_bf16_truncated", "(uint32_t)h << 16", "((uint32_t)h << 16) & 0xFFFE0000u",
      oracle_pins.ALL_PINS),
 ]
