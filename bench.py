@@ -291,6 +291,21 @@ def make_workload(name, dev):
             {"part": 0, "kernel": "trimul_sm103a_kernel", "bound": "hbm",
              "per_launch": trimul_algorithmic_bytes(shape.B, shape.T, shape.C, shape.NH, lower)},
             th, to)
+    if name in ("softmax_gpt2", "softmax_long"):
+        shape = synth.TRIMUL_GPT2 if name == "softmax_gpt2" else synth.TRIMUL_LONG
+        qkv_h = synth.trimul_input(shape, seed=0, dist="normal")
+        qkv = qkv_h.to(dev)
+        att = torch.empty(shape.out_shape, dtype=torch.float32, device=dev)
+        fn = lambda st: csa.causal_softmax_forward(att, qkv, shape.B, shape.T, shape.C, shape.NH,
+                                                   stream=st)
+        return finish(
+            f"causal softmax of the scores, {'GPT-2-small' if name == 'softmax_gpt2' else 'long context'}"
+            f" (B={shape.B},T={shape.T},C={shape.C},NH={shape.NH},HS={shape.HS})",
+            {"softmax": {"B": shape.B, "T": shape.T, "C": shape.C, "NH": shape.NH}},
+            [("softmax", fn)], trimul_flops(shape.B, shape.T, shape.C, shape.NH),
+            {"part": 0, "kernel": "softmax_sm103a_kernel", "bound": "hbm",
+             "per_launch": trimul_algorithmic_bytes(shape.B, shape.T, shape.C, shape.NH)},
+            [(qkv, qkv_h)], [att])
     if name == "dense_ragged":
         df, dh, do = dense_part(ds)
         return finish("dense ragged (M=960,I=770,H=768)", {"dense": {"M": ds.M, "I": ds.I,
@@ -333,7 +348,7 @@ def make_workload(name, dev):
 
 
 WORKLOADS = ["step", "trimul_gpt2", "trimul_long", "trimul_gpt2_lower", "trimul_long_lower",
-             "dense_ragged", "dense_sweep", "bmm_nt"]
+             "dense_ragged", "dense_sweep", "bmm_nt", "softmax_gpt2", "softmax_long"]
 
 
 def run_ours(args, rank, world, local):

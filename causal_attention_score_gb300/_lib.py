@@ -36,6 +36,7 @@ SIGNATURES = {
     "trimul_forward_noalloc": (_i, [_vp, _vp, _i, _i, _i, _i, _u32, _u32, _vp]),
     "dense_xwt": (_i, [_vp, _vp, _vp, _i, _i, _i]),
     "batch_matmul_nt": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp]),
+    "causal_softmax_forward": (_i, [_vp, _vp, _i, _i, _i, _i, _vp]),
     "dense_xwt_ex": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp]),
     "csa_get_status": (_i, [_vp]),
     "csa_status_string": (ctypes.c_char_p, [_i]),

@@ -187,6 +187,29 @@ csa_status trimul_forward(float* out, const void* qkv, int B, int T, int C, int 
   return trimul_forward_ex(out, qkv, B, T, C, NH, CSA_MASK_NAN, CSA_TRIMUL_FULL, nullptr);
 }
 
+csa_status causal_softmax_forward(float* att, const void* qkv, int B, int T, int C, int NH,
+                                  void* stream) {
+  t_last_error.clear();
+  if (!att || !qkv) return set_error(CSA_ERR_NULL, "causal_softmax_forward: null pointer");
+  if (B <= 0 || T <= 0 || C <= 0 || NH <= 0)
+    return set_error(CSA_ERR_SHAPE, "causal_softmax_forward: B, T, C, NH must be >= 1");
+  if (C % NH != 0) return set_error(CSA_ERR_SHAPE, "causal_softmax_forward: C % NH != 0");
+  const int HS = C / NH;
+  if (HS % 8 != 0)
+    return set_error(CSA_ERR_ALIGN, "causal_softmax_forward: HS = C/NH must be a multiple of 8");
+  if (HS > 128) return set_error(CSA_ERR_UNSUPPORTED, "causal_softmax_forward: HS > 128");
+  if (reinterpret_cast<uintptr_t>(qkv) % 16 != 0 || reinterpret_cast<uintptr_t>(att) % 4 != 0)
+    return set_error(CSA_ERR_ALIGN,
+                     "causal_softmax_forward: qkv must be 16-byte aligned, att 4-byte");
+  DeviceInfo dev;
+  std::string err;
+  int rc = current_device(dev, err);
+  if (rc != CSA_OK) return set_error(rc, err);
+  rc = softmax_launch(att, qkv, B, T, C, NH, static_cast<cudaStream_t>(stream), dev, err);
+  if (rc != CSA_OK) return set_error(rc, err);
+  return CSA_OK;
+}
+
 csa_status batch_matmul_nt(float* Y, const void* X, const void* W, int batch, int T1, int T2,
                            int D, void* stream) {
   t_last_error.clear();

@@ -46,6 +46,9 @@ int trimul_launch_noalloc(float* out, const void* qkv, int B, int T, int C, int 
 int bmm_nt_launch(float* Y, const void* X, const void* W, int batch, int T1, int T2, int D,
                   cudaStream_t stream, const DeviceInfo& dev, std::string& err);
 
+int softmax_launch(float* out, const void* qkv, int B, int T, int C, int NH, cudaStream_t stream,
+                   const DeviceInfo& dev, std::string& err);
+
 int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
                  cudaStream_t stream, const DeviceInfo& dev, std::string& err);
 

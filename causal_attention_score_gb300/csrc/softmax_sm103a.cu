@@ -1,0 +1,645 @@
+// Fused causal softmax of the score rows on sm_103a:
+//
+//   att[b][h][t][t2] = exp(s - m) / sum_{u <= t} exp(s_u - m)   for t2 <= t,
+//   att[b][h][t][t2] = 0                                          for t2 > t,
+//   s = (Q[b][h][t][:] . K[b][h][t2][:]) / sqrt(HS),  m = max_{u <= t} s_u,
+//
+// the scores of "llm.c dev/cuda/trimat_forward.cu" (trimul_cpu, whose comment
+// says it is taken from the attention forward pass) followed by the two-pass
+// row softmax of the "Smallem" article 5 (row maximum and sum of exponentials,
+// then normalisation). The scores never reach global memory.
+//
+// Design (one persistent launch, one CTA per SM, 10 warps):
+//  - work unit = one (b, h) row block of 128 query rows; units are taken from
+//    a per-launch counter, longest row blocks first.
+//  - warp 0: TMA producer. Per unit it loads the Q tile once (two buffers, so
+//    the next unit's Q arrives while this one computes) and streams the unit's
+//    K tiles j = 0..i twice through a multi-stage ring.
+//  - warp 1: tcgen05.mma issuer, 128 x 128 x HS per tile into one of two TMEM
+//    accumulators, both passes.
+//  - warps 2..9: epilogue, each owning 32 rows x 64 columns of every tile.
+//    Pass 1 keeps, per row, the running maximum m and sum l of exp2 of the
+//    scores (log2 domain); the two warps holding the two halves of a row then
+//    combine (m, l) through shared memory behind a bounded mbarrier. Pass 2
+//    recomputes each tile and writes exp2(x - m) / l, staged through swizzled
+//    shared memory into 32 x 32 TMA stores (plain stores when T % 4 != 0).
+//    The unit's tiles above the diagonal are stored as zeros.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "csa_internal.h"
+#include "sm103a_ptx.cuh"
+
+namespace csa {
+namespace {
+
+constexpr int kTile = 128;
+constexpr int kChunkElems = 64;
+constexpr int kChunkBytes = kTile * 128;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kSlabCols = 64;
+constexpr int kBoxBytes = 32 * 32 * 4;
+constexpr int kPairBytes = 2 * kBoxBytes;  // one 32 x 64 fp32 slab as two TMA boxes
+constexpr int kStatsBytes = 2 * kEpiWarps * 32 * 8;  // (m, l) per row half, two units
+constexpr int kTmemCols = 2 * kTile;
+constexpr int kRingDepth = 4;
+constexpr int kSlots = 256;
+constexpr unsigned int kEnd = 0xFFFFFFFFu;
+constexpr uint32_t kIdesc = idesc_bf16_f32(kTile, kTile);
+
+// Work-list counters, one pair per launch in flight; the last CTA resets its pair.
+__device__ unsigned int g_softmax_sched[kSlots][2];
+
+struct SoftmaxArgs {
+  int T, NH, BH, Tt;
+  int kchunks, ksteps, stages;
+  int n_units;
+  float scale_log2e;  // log2(e) / sqrt(HS)
+  uint32_t tma_store;
+  uint32_t pairs;  // staging pairs per epilogue warp (1 or 2)
+  float* out;
+  int* status;
+  unsigned long long wait_limit_ns;
+  unsigned int* sched;
+  uint32_t q_bytes, k_bytes;
+  uint32_t off_k, off_staging, off_zero, off_stats, off_bars, off_misc;
+};
+
+// Unit p: row block i = Tt - 1 - p / BH (longest first) of (b, h) = p % BH.
+__device__ __forceinline__ void decode_unit(unsigned int p, const SoftmaxArgs& a, int& bh,
+                                            int& ti) {
+  const int row = static_cast<int>(p) / a.BH;
+  bh = static_cast<int>(p) - row * a.BH;
+  ti = a.Tt - 1 - row;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    softmax_sm103a_kernel(const __grid_constant__ CUtensorMap tmap_qkv,
+                          const __grid_constant__ CUtensorMap tmap_out, const SoftmaxArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = lane_id();
+  const int S = a.stages;
+
+  const uint32_t bars = base + a.off_bars;
+  auto qfull_bar = [&](int s) { return bars + 8u * s; };
+  auto qempty_bar = [&](int s) { return bars + 8u * (2 + s); };
+  auto kfull_bar = [&](int s) { return bars + 8u * (4 + s); };
+  auto kempty_bar = [&](int s) { return bars + 8u * (4 + S + s); };
+  auto tfull_bar = [&](int s) { return bars + 8u * (4 + 2 * S + s); };
+  auto tempty_bar = [&](int s) { return bars + 8u * (6 + 2 * S + s); };
+  const uint32_t drain_bar = bars + 8u * (8 + 2 * S);
+  const uint32_t stats_bar = bars + 8u * (9 + 2 * S);
+  auto rfull_bar = [&](int s) { return bars + 8u * (10 + 2 * S + s); };
+  auto rempty_bar = [&](int s) { return bars + 8u * (10 + 2 * S + kRingDepth + s); };
+  const uint32_t tmem_slot = base + a.off_misc;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + a.off_misc + 4);
+  auto ring_entry = [&](int s) { return base + a.off_misc + 16u + 4u * s; };
+  auto q_chunk = [&](int qb, int kc) { return base + qb * a.q_bytes + kc * kChunkBytes; };
+  auto k_chunk = [&](int s, int kc) { return base + a.off_k + s * a.k_bytes + kc * kChunkBytes; };
+  const uint32_t zero_box = base + a.off_zero;
+  const uint32_t stats = base + a.off_stats;
+
+  const Watchdog wd{a.wait_limit_ns, a.status, abort_flag};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(qfull_bar(s), 1);
+      mbar_init(qempty_bar(s), 1);
+      mbar_init(tfull_bar(s), 1);
+      mbar_init(tempty_bar(s), kEpiWarps);
+    }
+    for (int s = 0; s < S; ++s) {
+      mbar_init(kfull_bar(s), 1);
+      mbar_init(kempty_bar(s), 1);
+    }
+    mbar_init(drain_bar, 1);
+    mbar_init(stats_bar, kEpiWarps);
+    for (int s = 0; s < kRingDepth; ++s) {
+      mbar_init(rfull_bar(s), 1);
+      mbar_init(rempty_bar(s), 1 + kEpiWarps);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  for (uint32_t w = threadIdx.x; w < kBoxBytes / 4; w += kThreads) st_shared_b32(zero_box + 4u * w, 0u);
+  fence_proxy_async_smem();
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+    tc_fence_before_sync();
+  }
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = ld_shared_b32(tmem_slot);
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      tma_prefetch_map(&tmap_qkv);
+      int stage = 0, qb = 0, slot = 0;
+      uint32_t phase = 0, qphase = 0, sphase = 0;
+      uint32_t kissued = 0, kparity = 0, qissued = 0, qparity = 0;
+      const uint32_t qtx = a.q_bytes, ktx = a.k_bytes;
+      unsigned int p0 = atomicAdd(a.sched, 1u), p1 = atomicAdd(a.sched, 1u);
+      bool ok = true;
+      while (ok) {
+        const unsigned int cur = p0;
+        const bool done = cur >= static_cast<unsigned int>(a.n_units);
+        p0 = p1;
+        if (!done) p1 = atomicAdd(a.sched, 1u);
+        if (!mbar_wait(rempty_bar(slot), sphase ^ 1u, wd, kSiteSched)) break;
+        st_shared_b32(ring_entry(slot), done ? kEnd : cur);
+        mbar_arrive(rfull_bar(slot));
+        if (++slot == kRingDepth) {
+          slot = 0;
+          sphase ^= 1u;
+        }
+        if (done) break;
+        int bh, ti;
+        decode_unit(cur, a, bh, ti);
+        const int b = bh / a.NH, h = bh - b * a.NH;
+        if (!mbar_wait(qempty_bar(qb), qphase ^ 1u, wd, kSiteProducerEmpty)) break;
+        mbar_arrive_expect_tx(qfull_bar(qb), qtx);
+        for (int kc = 0; kc < a.kchunks; ++kc)
+          tma_load_4d(q_chunk(qb, kc), &tmap_qkv, qfull_bar(qb), kc * kChunkElems, h, ti * kTile,
+                      b);
+        qissued |= 1u << qb;
+        qparity = (qparity & ~(1u << qb)) | (qphase << qb);
+        if (++qb == 2) {
+          qb = 0;
+          qphase ^= 1u;
+        }
+        for (int pass = 0; ok && pass < 2; ++pass) {
+          for (int tj = 0; tj <= ti; ++tj) {
+            if (!mbar_wait(kempty_bar(stage), phase ^ 1u, wd, kSiteProducerEmpty)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(kfull_bar(stage), ktx);
+            for (int kc = 0; kc < a.kchunks; ++kc)
+              tma_load_4d(k_chunk(stage, kc), &tmap_qkv, kfull_bar(stage), kc * kChunkElems,
+                          a.NH + h, tj * kTile, b);
+            kissued |= 1u << stage;
+            kparity = (kparity & ~(1u << stage)) | (phase << stage);
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      if (*abort_flag) {
+        // Let every load still in flight land before shared memory goes away.
+        for (int s = 0; s < S + 2; ++s) {
+          const bool is_q = s >= S;
+          const int i = is_q ? s - S : s;
+          if (!((is_q ? qissued : kissued) & (1u << i))) continue;
+          const uint32_t bar = is_q ? qfull_bar(i) : kfull_bar(i);
+          const uint32_t par = ((is_q ? qparity : kparity) >> i) & 1u;
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_test(bar, par) && globaltimer_ns() - t0 < a.wait_limit_ns) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      int stage = 0, qb = 0, acc = 0, slot = 0;
+      uint32_t phase = 0, qphase = 0, acc_phase = 0, sphase = 0;
+      bool ok = true;
+      while (ok) {
+        if (!mbar_wait(rfull_bar(slot), sphase, wd, kSiteSched)) break;
+        const unsigned int cur = ld_shared_b32(ring_entry(slot));
+        mbar_arrive(rempty_bar(slot));
+        if (++slot == kRingDepth) {
+          slot = 0;
+          sphase ^= 1u;
+        }
+        if (cur == kEnd) break;
+        int bh, ti;
+        decode_unit(cur, a, bh, ti);
+        if (!mbar_wait(qfull_bar(qb), qphase, wd, kSiteMmaFull)) break;
+        tc_fence_after_sync();
+        for (int pass = 0; ok && pass < 2; ++pass) {
+          for (int tj = 0; tj <= ti; ++tj) {
+            if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, wd, kSiteMmaTmemEmpty) ||
+                !mbar_wait(kfull_bar(stage), phase, wd, kSiteMmaFull)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kTile);
+            for (int k = 0; k < a.ksteps; ++k) {
+              const uint32_t off = static_cast<uint32_t>(k & 3) * 32u;
+              umma_bf16(d, umma_desc_k_sw128(q_chunk(qb, k >> 2) + off),
+                        umma_desc_k_sw128(k_chunk(stage, k >> 2) + off), kIdesc,
+                        k > 0 ? 1u : 0u);
+            }
+            umma_commit(kempty_bar(stage));
+            umma_commit(tfull_bar(acc));
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            if (++acc == 2) {
+              acc = 0;
+              acc_phase ^= 1u;
+            }
+          }
+        }
+        if (!ok) break;
+        umma_commit(qempty_bar(qb));  // the unit's MMAs are done with its Q tile
+        if (++qb == 2) {
+          qb = 0;
+          qphase ^= 1u;
+        }
+      }
+      umma_commit(drain_bar);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_test(drain_bar, 0) && globaltimer_ns() - t0 < a.wait_limit_ns) {
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue --
+    // Warp ew = warp - 2 owns the 32 rows of TMEM lane quarter warp % 4 and the
+    // 64-column slab ew / 4 of every tile; warp ew ^ 4 holds the other half of
+    // the same rows.
+    const uint32_t ew = warp - 2u;
+    const int q = static_cast<int>(warp & 3u);
+    const int slab = static_cast<int>(ew >> 2);
+    const uint32_t staging = base + a.off_staging + ew * a.pairs * kPairBytes;
+    uint32_t pair = 0;
+    const int T = a.T;
+    int acc = 0, slot = 0;
+    uint32_t acc_phase = 0, sphase = 0, stats_phase = 0;
+    bool ok = true;
+    while (ok) {
+      int got = 1;
+      unsigned int cur = 0;
+      if (lane == 0) {
+        got = mbar_wait(rfull_bar(slot), sphase, wd, kSiteSched) ? 1 : 0;
+        if (got) {
+          cur = ld_shared_b32(ring_entry(slot));
+          mbar_arrive(rempty_bar(slot));
+        }
+      }
+      got = __shfl_sync(0xffffffffu, got, 0);
+      cur = __shfl_sync(0xffffffffu, cur, 0);
+      if (!got || cur == kEnd) break;
+      if (++slot == kRingDepth) {
+        slot = 0;
+        sphase ^= 1u;
+      }
+      int bh, ti;
+      decode_unit(cur, a, bh, ti);
+      const int row0 = ti * kTile + q * 32;
+      const int r = row0 + static_cast<int>(lane);
+      // Tiles above the diagonal hold probability 0 whatever the statistics are:
+      // store them first, so the unit's writes overlap its first pass.
+      if (row0 < T) {
+        for (int tj = ti + 1; tj < a.Tt; ++tj) {
+          const int colw = tj * kTile + slab * kSlabCols;
+          if (colw >= T) continue;
+          if (a.tma_store) {
+            if (lane == 0) {
+              tma_store_3d(&tmap_out, zero_box, colw, row0, bh);
+              if (colw + 32 < T) tma_store_3d(&tmap_out, zero_box, colw + 32, row0, bh);
+              bulk_commit();
+            }
+          } else {
+            float* orow = a.out + (static_cast<size_t>(bh) * T + row0) * T;
+            for (int rr = 0; rr < 32 && row0 + rr < T; ++rr)
+              for (int c = 0; c < 2; ++c) {
+                const int col = colw + c * 32 + static_cast<int>(lane);
+                if (col < T) orow[static_cast<size_t>(rr) * T + col] = 0.0f;
+              }
+          }
+        }
+      }
+      // The unit's 2n tiles (pass 1: tj = 0..ti, then pass 2 over the same tiles)
+      // come out of the accumulators in order. The TMEM load of tile k + 1 is
+      // issued before tile k is processed, so its latency hides behind the
+      // arithmetic; exactly one load is outstanding whenever a buffer is in use.
+      const int n = ti + 1;
+      const float sc = a.scale_log2e;
+      float m = -INFINITY, l = 0.0f, shift = 0.0f;
+      uint32_t va[kSlabCols], vb[kSlabCols];
+      int held = 0;
+      auto issue = [&](uint32_t(&v)[kSlabCols]) -> bool {
+        if (!mbar_wait_warp_inline(tfull_bar(acc), acc_phase, wd, kSiteEpilogueFull)) return false;
+        tc_fence_after_sync();
+        tmem_ld_64cols_async(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                 static_cast<uint32_t>(acc * kTile + slab * kSlabCols),
+                             v);
+        held = acc;
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+        return true;
+      };
+      auto retire = [&](uint32_t(&v)[kSlabCols]) {
+        tmem_wait_ld_64(v);
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(held));
+      };
+      auto process = [&](uint32_t(&v)[kSlabCols], int k) -> bool {
+        const bool second = k >= n;
+        const int tj = second ? k - n : k;
+        const int colw = tj * kTile + slab * kSlabCols;
+        // Columns of this slab in row r's causal window are the offsets e <= lim.
+        const int lim = min(r, T - 1) - colw;
+        // Lane 0 has the warp's smallest window, so this test is warp-uniform.
+        const bool full = min(row0, T - 1) - colw >= kSlabCols - 1;
+        if (!second) {
+          // The maximum is taken on the raw products; scaling by sc > 0 is
+          // monotone in fp32, so it commutes with the maximum.
+          float mx = -INFINITY;
+          if (full) {
+            float t[kSlabCols / 2];
+#pragma unroll
+            for (int e = 0; e < kSlabCols / 2; ++e)
+              t[e] = fmaxf(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+#pragma unroll
+            for (int w = kSlabCols / 4; w >= 1; w >>= 1)
+#pragma unroll
+              for (int e = 0; e < w; ++e) t[e] = fmaxf(t[e], t[e + w]);
+            mx = t[0];
+          } else {
+#pragma unroll
+            for (int e = 0; e < kSlabCols; ++e)
+              if (e <= lim) mx = fmaxf(mx, __uint_as_float(v[e]));
+          }
+          mx *= sc;
+          if (mx > m) {
+            l *= ex2_approx(m - mx);
+            m = mx;
+          }
+          float part[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) part[e] = 0.0f;
+          if (full) {
+#pragma unroll
+            for (int e = 0; e < kSlabCols; ++e)
+              part[e & 7] += ex2_approx(fmaf(__uint_as_float(v[e]), sc, -m));
+          } else {
+#pragma unroll
+            for (int e = 0; e < kSlabCols; ++e)
+              if (e <= lim) part[e & 7] += ex2_approx(fmaf(__uint_as_float(v[e]), sc, -m));
+          }
+          l += ((part[0] + part[1]) + (part[2] + part[3])) +
+               ((part[4] + part[5]) + (part[6] + part[7]));
+          if (k != n - 1) return true;
+          // Combine the two halves of each row: (m, l) of this warp and of warp
+          // ew ^ 4. Slots alternate between units: a warp can be one unit ahead
+          // of its partner's read, never two (that needs the partner's next arrival).
+          const uint32_t sbase = stats + stats_phase * (kEpiWarps * 32u * 8u);
+          st_shared_b32(sbase + (ew * 32u + lane) * 8u, __float_as_uint(m));
+          st_shared_b32(sbase + (ew * 32u + lane) * 8u + 4u, __float_as_uint(l));
+          __syncwarp();
+          if (lane == 0) mbar_arrive(stats_bar);
+          if (!mbar_wait_warp_inline(stats_bar, stats_phase, wd, kSiteEpilogueFull)) return false;
+          stats_phase ^= 1u;
+          const uint32_t other = sbase + ((ew ^ 4u) * 32u + lane) * 8u;
+          const float m2 = __uint_as_float(ld_shared_b32(other));
+          const float l2 = __uint_as_float(ld_shared_b32(other + 4u));
+          const float mm = fmaxf(m, m2);
+          const float ll = (m == -INFINITY ? 0.0f : l * ex2_approx(m - mm)) +
+                           (m2 == -INFINITY ? 0.0f : l2 * ex2_approx(m2 - mm));
+          // exp2(x - m) / l = exp2(x - (m + log2 l)): pass 2 needs one shift.
+          shift = mm + log2f(ll);
+          return true;
+        }
+        if (full) {
+#pragma unroll
+          for (int e = 0; e < kSlabCols; ++e)
+            v[e] = __float_as_uint(ex2_approx(fmaf(__uint_as_float(v[e]), sc, -shift)));
+        } else {
+#pragma unroll
+          for (int e = 0; e < kSlabCols; ++e)
+            v[e] = e <= lim ? __float_as_uint(ex2_approx(fmaf(__uint_as_float(v[e]), sc, -shift)))
+                            : 0u;
+        }
+        if (row0 >= T || colw >= T) return true;
+        if (lane == 0) {
+          if (a.pairs == 2) bulk_wait_read<1>();
+          else bulk_wait_read<0>();
+        }
+        __syncwarp();
+        const uint32_t box0 = staging + pair * kPairBytes;
+        if (++pair == a.pairs) pair = 0;
+        const int nbox = (colw + 32 < T) ? 2 : 1;
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          if (c < nbox) stage_row_sw128(box0 + c * kBoxBytes, lane, v + 32 * c);
+        if (a.tma_store) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            for (int c = 0; c < nbox; ++c)
+              tma_store_3d(&tmap_out, box0 + c * kBoxBytes, colw + c * 32, row0, bh);
+            bulk_commit();
+          }
+        } else {
+          __syncwarp();
+          for (int c = 0; c < nbox; ++c) {
+            const int col = colw + c * 32 + static_cast<int>(lane);
+            float* ocol = a.out + (static_cast<size_t>(bh) * T + row0) * T + col;
+            for (int rr = 0; rr < 32; ++rr) {
+              const uint32_t val =
+                  staged_elem_sw128(box0 + c * kBoxBytes, static_cast<uint32_t>(rr), lane);
+              if (row0 + rr < T && col < T) ocol[static_cast<size_t>(rr) * T] = __uint_as_float(val);
+            }
+          }
+        }
+        return true;
+      };
+      if (!issue(va)) {
+        ok = false;
+        break;
+      }
+      // 2n is even: tiles k (buffer va) and k + 1 (buffer vb) per step.
+      for (int k = 0; k < 2 * n; k += 2) {
+        retire(va);
+        if (!issue(vb)) {
+          ok = false;
+          break;
+        }
+        if (!process(va, k)) {
+          retire(vb);
+          ok = false;
+          break;
+        }
+        retire(vb);
+        const bool more = k + 2 < 2 * n;
+        if (more && !issue(va)) {
+          ok = false;
+          break;
+        }
+        if (!process(vb, k + 1)) {
+          if (more) retire(va);
+          ok = false;
+          break;
+        }
+      }
+      if (!ok) break;
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(a.sched + 1, 1u) == gridDim.x - 1) {
+      atomicExch(a.sched, 0u);
+      atomicExch(a.sched + 1, 0u);
+    }
+  }
+}
+
+}  // namespace
+
+int softmax_launch(float* out, const void* qkv, int B, int T, int C, int NH, cudaStream_t stream,
+                   const DeviceInfo& dev, std::string& err) {
+  const int HS = C / NH;
+  if (HS % 8 != 0) {
+    err = "causal_softmax_forward: HS = C/NH must be a multiple of 8";
+    return CSA_ERR_ALIGN;
+  }
+  if (HS > 128) {
+    err = "causal_softmax_forward: HS > 128 is not supported";
+    return CSA_ERR_UNSUPPORTED;
+  }
+  if (reinterpret_cast<uintptr_t>(qkv) % 16 != 0 || reinterpret_cast<uintptr_t>(out) % 4 != 0) {
+    err = "causal_softmax_forward: qkv must be 16-byte aligned and out 4-byte aligned";
+    return CSA_ERR_ALIGN;
+  }
+  const long long BH = static_cast<long long>(B) * NH;
+  const long long Tt = (static_cast<long long>(T) + kTile - 1) / kTile;
+  if (BH * Tt >= (1LL << 31) - (1LL << 20) || BH > (1LL << 30)) {
+    err = "causal_softmax_forward: too many row blocks";
+    return CSA_ERR_SHAPE;
+  }
+  SoftmaxArgs a{};
+  a.T = T;
+  a.NH = NH;
+  a.BH = static_cast<int>(BH);
+  a.Tt = static_cast<int>(Tt);
+  a.kchunks = (HS + kChunkElems - 1) / kChunkElems;
+  a.ksteps = (HS + 15) / 16;
+  a.n_units = static_cast<int>(BH * Tt);
+  a.scale_log2e = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(HS)));
+  a.tma_store = (T % 4 == 0 && reinterpret_cast<uintptr_t>(out) % 16 == 0) ? 1u : 0u;
+  a.out = out;
+  a.status = dev.status_word;
+  a.wait_limit_ns = wait_limit_ns();
+
+  // Shared memory: Q (2 buffers) | K ring | staging | zero box | stats | barriers | misc.
+  a.q_bytes = static_cast<uint32_t>(a.kchunks) * kChunkBytes;
+  a.k_bytes = a.q_bytes;
+  // Two staging pairs per epilogue warp when that still leaves two K stages.
+  int staging_bytes = 0;
+  for (int pairs = 2; pairs >= 1; --pairs) {
+    staging_bytes = kEpiWarps * pairs * kPairBytes;
+    const int fixed = 2 * static_cast<int>(a.q_bytes) + staging_bytes + kBoxBytes + kStatsBytes +
+                      1024 + 1024;
+    a.pairs = static_cast<uint32_t>(pairs);
+    a.stages = std::min(4, (dev.max_smem_optin - fixed) / static_cast<int>(a.k_bytes));
+    if (a.stages >= 2) break;
+  }
+  if (a.stages < 2) {
+    err = "causal_softmax_forward: not enough shared memory";
+    return CSA_ERR_UNSUPPORTED;
+  }
+  a.off_k = 2u * a.q_bytes;
+  a.off_staging = a.off_k + static_cast<uint32_t>(a.stages) * a.k_bytes;
+  a.off_zero = a.off_staging + static_cast<uint32_t>(staging_bytes);
+  a.off_stats = a.off_zero + kBoxBytes;
+  a.off_bars = a.off_stats + kStatsBytes;
+  a.off_misc = a.off_bars + 8u * static_cast<uint32_t>(10 + 2 * a.stages + 2 * kRingDepth);
+  const size_t smem = a.off_misc + 16 + 4 * kRingDepth + 1024;
+
+  CUtensorMap map_qkv, map_out;
+  {
+    const uint64_t dims[4] = {static_cast<uint64_t>(HS), static_cast<uint64_t>(3 * NH),
+                              static_cast<uint64_t>(T), static_cast<uint64_t>(B)};
+    const uint64_t strides[3] = {static_cast<uint64_t>(HS) * 2, static_cast<uint64_t>(C) * 6,
+                                 static_cast<uint64_t>(T) * C * 6};
+    const uint32_t box[4] = {kChunkElems, 1, kTile, 1};
+    int rc = encode_tiled(&map_qkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, qkv, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B, err);
+    if (rc != CSA_OK) return rc;
+  }
+  if (a.tma_store) {
+    const uint64_t dims[3] = {static_cast<uint64_t>(T), static_cast<uint64_t>(T),
+                              static_cast<uint64_t>(BH)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(T) * 4,
+                                 static_cast<uint64_t>(T) * static_cast<uint64_t>(T) * 4};
+    const uint32_t box[3] = {32, 32, 1};
+    int rc = encode_tiled(&map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, out, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B, err);
+    if (rc != CSA_OK) return rc;
+  } else {
+    std::memset(&map_out, 0, sizeof map_out);
+  }
+  {
+    static std::mutex mu;
+    static unsigned int* sched_base[64] = {};
+    static std::atomic<unsigned int> launch_seq{0};
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev.device < 0 || dev.device >= 64) {
+      err = "causal_softmax_forward: device ordinal out of range";
+      return CSA_ERR_CUDA;
+    }
+    if (!sched_base[dev.device]) {
+      void* p = nullptr;
+      cudaError_t se = cudaGetSymbolAddress(&p, g_softmax_sched);
+      if (se != cudaSuccess) {
+        err = std::string("causal_softmax_forward: cudaGetSymbolAddress: ") +
+              cudaGetErrorString(se);
+        return CSA_ERR_CUDA;
+      }
+      sched_base[dev.device] = static_cast<unsigned int*>(p);
+    }
+    a.sched = sched_base[dev.device] + 2 * (launch_seq.fetch_add(1) % kSlots);
+  }
+  cudaError_t e = cudaFuncSetAttribute(softmax_sm103a_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) {
+    err = std::string("causal_softmax_forward: cudaFuncSetAttribute: ") + cudaGetErrorString(e);
+    return CSA_ERR_LAUNCH;
+  }
+  const long long grid = std::min<long long>(a.n_units, dev.sm_count);
+  softmax_sm103a_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(map_qkv, map_out,
+                                                                                 a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    err = std::string("causal_softmax_forward: launch: ") + cudaGetErrorString(e);
+    return CSA_ERR_LAUNCH;
+  }
+  return CSA_OK;
+}
+
+}  // namespace csa

@@ -74,6 +74,27 @@ def batch_matmul_nt(Y: torch.Tensor, X: torch.Tensor, W: torch.Tensor, batch: in
     _lib.check(rc, "batch_matmul_nt")
 
 
+def causal_softmax_forward(att: torch.Tensor, qkv: torch.Tensor, B: int, T: int, C: int, NH: int,
+                           stream=None) -> None:
+    """Softmax over t2 <= t of the causal scores into ``att`` (fp32, (B, NH, T, T)),
+    0 above the diagonal; ``qkv`` bf16 (B, T, 3, NH, HS)."""
+    _need(qkv, "qkv", torch.bfloat16, B * T * 3 * C)
+    _need(att, "att", torch.float32, B * NH * T * T)
+    rc = _lib.load().causal_softmax_forward(att.data_ptr(), qkv.data_ptr(), B, T, C, NH,
+                                            _stream_ptr(stream))
+    _lib.check(rc, "causal_softmax_forward")
+
+
+def causal_softmax(qkv: torch.Tensor, stream=None) -> torch.Tensor:
+    """Allocating form of causal_softmax_forward."""
+    B, T, three, NH, HS = qkv.shape
+    if three != 3:
+        raise ValueError("qkv must have shape (B, T, 3, NH, HS)")
+    att = torch.empty((B, NH, T, T), dtype=torch.float32, device=qkv.device)
+    causal_softmax_forward(att, qkv, B, T, NH * HS, NH, stream=stream)
+    return att
+
+
 def trimul(qkv: torch.Tensor, mask="nan", lower_only: bool = False, stream=None) -> torch.Tensor:
     """Allocating form: qkv (B, T, 3, NH, HS) bf16 -> scores (B, NH, T, T) fp32."""
     B, T, three, NH, HS = qkv.shape

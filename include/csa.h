@@ -143,6 +143,23 @@ csa_status dense_xwt_ex(float* Y, const void* X, const void* W, int M, int I, in
                         void* stream);
 
 /*
+ * causal_softmax_forward -- the causal score rows of trimul_forward followed by
+ * a softmax over t2 <= t, in one kernel (the scores never reach memory):
+ *   att[b][h][t][t2] = exp(s[t2] - m) / sum_{u <= t} exp(s[u] - m)  for t2 <= t,
+ *   att[b][h][t][t2] = 0                                               for t2 > t,
+ * s = Q[b][h][t] . K[b][h][t2] / sqrt(HS), m = max_{u <= t} s[u]. The score is
+ * the referee of "llm.c dev/cuda/trimat_forward.cu" (taken, as its comment
+ * says, from the attention forward pass, where this softmax follows); the
+ * softmax is the two-pass form of the "Smallem" article 5 (row maximum and sum
+ * of exponentials, then normalisation).
+ *   att  device, fp32, (B, NH, T, T) contiguous, fully overwritten.
+ *   qkv  device, bf16, (B, T, 3, NH, HS), HS = C / NH, HS % 8 == 0, HS <= 128.
+ * qkv 16-byte aligned, att 4-byte aligned. Asynchronous on `stream`.
+ */
+csa_status causal_softmax_forward(float* att, const void* qkv, int B, int T, int C, int NH,
+                                  void* stream);
+
+/*
  * batch_matmul_nt -- the unmasked, unscaled batched NT product of
  * "DietCode tests/codegen/test_1_local_padding.py" (test_local_padding_ii
  * docstring, BatchMatmulNT):
