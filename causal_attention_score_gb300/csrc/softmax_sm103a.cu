@@ -23,7 +23,15 @@
 //    combine (m, l) through shared memory behind a bounded mbarrier. Pass 2
 //    recomputes each tile and writes exp2(x - m) / l, staged through swizzled
 //    shared memory into 32 x 32 TMA stores (plain stores when T % 4 != 0).
-//    The unit's tiles above the diagonal are stored as zeros.
+//  - warp 10: writes the tiles above the diagonal (probability 0) from a global
+//    pool of 128 x 128 zero tiles, as 128 x 16 TMA stores of a zeroed shared
+//    buffer (plain stores when T % 4 != 0). It takes a tile only while its own
+//    epilogue is not storing (start-up, pass 1, after the last unit), two tiles
+//    in flight at most, so the SM's write stream has no gaps and the pool
+//    evens out the end of the launch across SMs.
+//  - Writes saturate HBM and queue ahead of reads, so the producer prefetches
+//    the next unit's Q and first K tiles into L2 a whole unit early; K is kept
+//    in L2 (every row block of its (b, h) reads it, twice), the output is not.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -45,10 +53,13 @@ constexpr int kTile = 128;
 constexpr int kChunkElems = 64;
 constexpr int kChunkBytes = kTile * 128;
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kZeroWarp = 2 + kEpiWarps;
+constexpr int kThreads = 64 + 32 * kEpiWarps + 32;
 constexpr int kSlabCols = 64;
 constexpr int kBoxBytes = 32 * 32 * 4;
 constexpr int kPairBytes = 2 * kBoxBytes;  // one 32 x 64 fp32 slab as two TMA boxes
+constexpr int kZeroCols = 128, kZeroRows = 16;  // zero-writer TMA box
+constexpr int kZeroBytes = kZeroCols * kZeroRows * 4;
 constexpr int kStatsBytes = 2 * kEpiWarps * 32 * 8;  // (m, l) per row half, two units
 constexpr int kTmemCols = 2 * kTile;
 constexpr int kRingDepth = 4;
@@ -56,13 +67,17 @@ constexpr int kSlots = 256;
 constexpr unsigned int kEnd = 0xFFFFFFFFu;
 constexpr uint32_t kIdesc = idesc_bf16_f32(kTile, kTile);
 
-// Work-list counters, one pair per launch in flight; the last CTA resets its pair.
-__device__ unsigned int g_softmax_sched[kSlots][2];
+// Work-list counters, one set per launch in flight: [0] row-block units,
+// [1] finished CTAs, [2] zero tiles. The last CTA to finish resets its set.
+constexpr int kSchedWords = 4;
+__device__ unsigned int g_softmax_sched[kSlots][kSchedWords];
+constexpr int kPrefetchK = 4;  // K tiles of the next unit prefetched into L2
 
 struct SoftmaxArgs {
   int T, NH, BH, Tt;
   int kchunks, ksteps, stages;
   int n_units;
+  int n_zero;  // zero tiles: BH * Tt * (Tt - 1) / 2
   float scale_log2e;  // log2(e) / sqrt(HS)
   uint32_t tma_store;
   uint32_t pairs;  // staging pairs per epilogue warp (1 or 2)
@@ -84,7 +99,8 @@ __device__ __forceinline__ void decode_unit(unsigned int p, const SoftmaxArgs& a
 
 __global__ void __launch_bounds__(kThreads, 1)
     softmax_sm103a_kernel(const __grid_constant__ CUtensorMap tmap_qkv,
-                          const __grid_constant__ CUtensorMap tmap_out, const SoftmaxArgs a) {
+                          const __grid_constant__ CUtensorMap tmap_out,
+                          const __grid_constant__ CUtensorMap tmap_zero, const SoftmaxArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -107,11 +123,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto rempty_bar = [&](int s) { return bars + 8u * (10 + 2 * S + kRingDepth + s); };
   const uint32_t tmem_slot = base + a.off_misc;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + a.off_misc + 4);
+  // Set while the epilogue is in pass 2 (storing), read by the zero writer.
+  volatile int* epi_storing = reinterpret_cast<volatile int*>(gbase + a.off_misc + 8);
   auto ring_entry = [&](int s) { return base + a.off_misc + 16u + 4u * s; };
   auto q_chunk = [&](int qb, int kc) { return base + qb * a.q_bytes + kc * kChunkBytes; };
   auto k_chunk = [&](int s, int kc) { return base + a.off_k + s * a.k_bytes + kc * kChunkBytes; };
-  const uint32_t zero_box = base + a.off_zero;
   const uint32_t stats = base + a.off_stats;
+  const uint32_t zero_buf = base + a.off_zero;
 
   const Watchdog wd{a.wait_limit_ns, a.status, abort_flag};
 
@@ -133,10 +151,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(rempty_bar(s), 1 + kEpiWarps);
     }
     *abort_flag = 0;
+    *epi_storing = 0;
     fence_barrier_init();
   }
-  for (uint32_t w = threadIdx.x; w < kBoxBytes / 4; w += kThreads) st_shared_b32(zero_box + 4u * w, 0u);
-  fence_proxy_async_smem();
+  if (a.tma_store) {
+    for (uint32_t w = threadIdx.x; w < kZeroBytes / 16; w += kThreads)
+      st_shared_v4(zero_buf + 16u * w, 0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+  }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
@@ -154,13 +176,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, qphase = 0, sphase = 0;
       uint32_t kissued = 0, kparity = 0, qissued = 0, qparity = 0;
       const uint32_t qtx = a.q_bytes, ktx = a.k_bytes;
+      const uint64_t keep = l2_policy_evict_last(), once = l2_policy_evict_first();
+      // Prefetches unit p's Q and K tiles into L2 (nothing past the work list).
+      auto prefetch_unit = [&](unsigned int p) {
+        if (p >= static_cast<unsigned int>(a.n_units)) return;
+        int pbh, pti;
+        decode_unit(p, a, pbh, pti);
+        const int pb = pbh / a.NH, ph = pbh - pb * a.NH;
+        for (int kc = 0; kc < a.kchunks; ++kc) {
+          tma_prefetch_l2_4d(&tmap_qkv, kc * kChunkElems, ph, pti * kTile, pb, keep);
+          for (int tj = 0; tj <= pti && tj < kPrefetchK; ++tj)
+            tma_prefetch_l2_4d(&tmap_qkv, kc * kChunkElems, a.NH + ph, tj * kTile, pb, keep);
+        }
+      };
       unsigned int p0 = atomicAdd(a.sched, 1u), p1 = atomicAdd(a.sched, 1u);
+      prefetch_unit(p1);
       bool ok = true;
       while (ok) {
         const unsigned int cur = p0;
         const bool done = cur >= static_cast<unsigned int>(a.n_units);
         p0 = p1;
-        if (!done) p1 = atomicAdd(a.sched, 1u);
+        if (!done) {
+          p1 = atomicAdd(a.sched, 1u);
+          prefetch_unit(p1);
+        }
         if (!mbar_wait(rempty_bar(slot), sphase ^ 1u, wd, kSiteSched)) break;
         st_shared_b32(ring_entry(slot), done ? kEnd : cur);
         mbar_arrive(rfull_bar(slot));
@@ -175,8 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(qempty_bar(qb), qphase ^ 1u, wd, kSiteProducerEmpty)) break;
         mbar_arrive_expect_tx(qfull_bar(qb), qtx);
         for (int kc = 0; kc < a.kchunks; ++kc)
-          tma_load_4d(q_chunk(qb, kc), &tmap_qkv, qfull_bar(qb), kc * kChunkElems, h, ti * kTile,
-                      b);
+          tma_load_4d_hint(q_chunk(qb, kc), &tmap_qkv, qfull_bar(qb), kc * kChunkElems, h,
+                           ti * kTile, b, once);
         qissued |= 1u << qb;
         qparity = (qparity & ~(1u << qb)) | (qphase << qb);
         if (++qb == 2) {
@@ -191,8 +230,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mbar_arrive_expect_tx(kfull_bar(stage), ktx);
             for (int kc = 0; kc < a.kchunks; ++kc)
-              tma_load_4d(k_chunk(stage, kc), &tmap_qkv, kfull_bar(stage), kc * kChunkElems,
-                          a.NH + h, tj * kTile, b);
+              tma_load_4d_hint(k_chunk(stage, kc), &tmap_qkv, kfull_bar(stage), kc * kChunkElems,
+                               a.NH + h, tj * kTile, b, keep);
             kissued |= 1u << stage;
             kparity = (kparity & ~(1u << stage)) | (phase << stage);
             if (++stage == S) {
@@ -274,6 +313,72 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (!mbar_test(drain_bar, 0) && globaltimer_ns() - t0 < a.wait_limit_ns) {
       }
     }
+  } else if (warp == kZeroWarp) {
+    // ------------------------------------------------------- zero writer --
+    // Columns c >= (i + 1) * 128 of row block i hold probability 0 whatever the
+    // row statistics are; this warp writes them with streaming stores while the
+    // epilogue computes, so they never queue in front of its TMA stores.
+    const int T = a.T;
+    const bool vec = a.tma_store != 0;  // T % 4 == 0 and a 16-byte aligned output
+    const uint64_t once = l2_policy_evict_first();
+    const int Tt = a.Tt;
+    bool ok = true;
+    while (ok) {
+      // Yield to the epilogue while it stores (bounded: the epilogue leaves pass 2
+      // within the wait limit, or the CTA aborts).
+      int z = 0;
+      if (lane == 0) {
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t it = 0; *epi_storing != 0; ++it) {
+          if (*abort_flag) {
+            ok = false;
+            break;
+          }
+          if ((it & 63u) == 63u && globaltimer_ns() - t0 > a.wait_limit_ns) {
+            *abort_flag = 1;
+            if (atomicCAS(a.status, 0, CSA_ERR_TIMEOUT) == 0) atomicExch(a.status + 1, kSiteSched);
+            ok = false;
+            break;
+          }
+          __nanosleep(128);
+        }
+        z = ok ? static_cast<int>(atomicAdd(a.sched + 2, 1u)) : a.n_zero;
+      }
+      z = __shfl_sync(0xffffffffu, z, 0);
+      if (z >= a.n_zero) break;
+      // Zero tile z: (b, h) = z % BH, then the strictly upper tile (i, j), j > i,
+      // numbered by pairing block rows i and Tt - 2 - i (Tt tiles per pair).
+      const int w = z / a.BH;
+      const int bh = z - w * a.BH;
+      const int pr = w / Tt, o = w - pr * Tt;
+      int ti, tj;
+      if (o < Tt - 1 - pr) {
+        ti = pr;
+        tj = pr + 1 + o;
+      } else {
+        ti = Tt - 2 - pr;
+        tj = ti + 1 + (o - (Tt - 1 - pr));
+      }
+      const int r0 = ti * kTile, c0 = tj * kTile;  // rows r0.. are all < T (ti <= Tt - 2)
+      if (vec) {
+        if (lane == 0) {
+          // Columns past T - 1 are clipped by the tensor map.
+          for (int rr = 0; rr < kTile; rr += kZeroRows)
+            tma_store_3d_hint(&tmap_zero, zero_buf, c0, r0 + rr, bh, once);
+          bulk_commit();
+          bulk_wait_read<1>();  // two tiles in flight at most
+        }
+        __syncwarp();
+      } else {
+        const int cols = min(kTile, T - c0);
+        float* blk = a.out + (static_cast<size_t>(bh) * T + r0) * T + c0;
+        for (int rr = 0; rr < kTile; ++rr)
+          for (int i = static_cast<int>(lane); i < cols; i += 32)
+            blk[static_cast<size_t>(rr) * T + i] = 0.0f;
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   } else {
     // ---------------------------------------------------------- epilogue --
     // Warp ew = warp - 2 owns the 32 rows of TMEM lane quarter warp % 4 and the
@@ -285,6 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t staging = base + a.off_staging + ew * a.pairs * kPairBytes;
     uint32_t pair = 0;
     const int T = a.T;
+    const uint64_t once = l2_policy_evict_first();
     int acc = 0, slot = 0;
     uint32_t acc_phase = 0, sphase = 0, stats_phase = 0;
     bool ok = true;
@@ -309,28 +415,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       decode_unit(cur, a, bh, ti);
       const int row0 = ti * kTile + q * 32;
       const int r = row0 + static_cast<int>(lane);
-      // Tiles above the diagonal hold probability 0 whatever the statistics are:
-      // store them first, so the unit's writes overlap its first pass.
-      if (row0 < T) {
-        for (int tj = ti + 1; tj < a.Tt; ++tj) {
-          const int colw = tj * kTile + slab * kSlabCols;
-          if (colw >= T) continue;
-          if (a.tma_store) {
-            if (lane == 0) {
-              tma_store_3d(&tmap_out, zero_box, colw, row0, bh);
-              if (colw + 32 < T) tma_store_3d(&tmap_out, zero_box, colw + 32, row0, bh);
-              bulk_commit();
-            }
-          } else {
-            float* orow = a.out + (static_cast<size_t>(bh) * T + row0) * T;
-            for (int rr = 0; rr < 32 && row0 + rr < T; ++rr)
-              for (int c = 0; c < 2; ++c) {
-                const int col = colw + c * 32 + static_cast<int>(lane);
-                if (col < T) orow[static_cast<size_t>(rr) * T + col] = 0.0f;
-              }
-          }
-        }
-      }
       // The unit's 2n tiles (pass 1: tj = 0..ti, then pass 2 over the same tiles)
       // come out of the accumulators in order. The TMEM load of tile k + 1 is
       // issued before tile k is processed, so its latency hides behind the
@@ -424,6 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            (m2 == -INFINITY ? 0.0f : l2 * ex2_approx(m2 - mm));
           // exp2(x - m) / l = exp2(x - (m + log2 l)): pass 2 needs one shift.
           shift = mm + log2f(ll);
+          if (ew == 0 && lane == 0) *epi_storing = 1;
           return true;
         }
         if (full) {
@@ -453,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) {
             for (int c = 0; c < nbox; ++c)
-              tma_store_3d(&tmap_out, box0 + c * kBoxBytes, colw + c * 32, row0, bh);
+              tma_store_3d_hint(&tmap_out, box0 + c * kBoxBytes, colw + c * 32, row0, bh, once);
             bulk_commit();
           }
         } else {
@@ -498,8 +583,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
       }
+      if (ew == 0 && lane == 0) *epi_storing = 0;
       if (!ok) break;
     }
+    if (ew == 0 && lane == 0) *epi_storing = 0;
     if (lane == 0) bulk_wait_all();
     __syncwarp();
   }
@@ -513,6 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __threadfence();
     if (atomicAdd(a.sched + 1, 1u) == gridDim.x - 1) {
       atomicExch(a.sched, 0u);
+      atomicExch(a.sched + 2, 0u);
       atomicExch(a.sched + 1, 0u);
     }
   }
@@ -537,8 +625,9 @@ int softmax_launch(float* out, const void* qkv, int B, int T, int C, int NH, cud
   }
   const long long BH = static_cast<long long>(B) * NH;
   const long long Tt = (static_cast<long long>(T) + kTile - 1) / kTile;
-  if (BH * Tt >= (1LL << 31) - (1LL << 20) || BH > (1LL << 30)) {
-    err = "causal_softmax_forward: too many row blocks";
+  if (BH * Tt * (Tt - 1) / 2 >= (1LL << 31) - (1LL << 20) || BH * Tt >= (1LL << 31) - (1LL << 20) ||
+      BH > (1LL << 30)) {
+    err = "causal_softmax_forward: too many tiles";
     return CSA_ERR_SHAPE;
   }
   SoftmaxArgs a{};
@@ -549,6 +638,7 @@ int softmax_launch(float* out, const void* qkv, int B, int T, int C, int NH, cud
   a.kchunks = (HS + kChunkElems - 1) / kChunkElems;
   a.ksteps = (HS + 15) / 16;
   a.n_units = static_cast<int>(BH * Tt);
+  a.n_zero = static_cast<int>(BH * Tt * (Tt - 1) / 2);
   a.scale_log2e = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(HS)));
   a.tma_store = (T % 4 == 0 && reinterpret_cast<uintptr_t>(out) % 16 == 0) ? 1u : 0u;
   a.out = out;
@@ -562,7 +652,7 @@ int softmax_launch(float* out, const void* qkv, int B, int T, int C, int NH, cud
   int staging_bytes = 0;
   for (int pairs = 2; pairs >= 1; --pairs) {
     staging_bytes = kEpiWarps * pairs * kPairBytes;
-    const int fixed = 2 * static_cast<int>(a.q_bytes) + staging_bytes + kBoxBytes + kStatsBytes +
+    const int fixed = 2 * static_cast<int>(a.q_bytes) + staging_bytes + kZeroBytes + kStatsBytes +
                       1024 + 1024;
     a.pairs = static_cast<uint32_t>(pairs);
     a.stages = std::min(4, (dev.max_smem_optin - fixed) / static_cast<int>(a.k_bytes));
@@ -575,12 +665,12 @@ int softmax_launch(float* out, const void* qkv, int B, int T, int C, int NH, cud
   a.off_k = 2u * a.q_bytes;
   a.off_staging = a.off_k + static_cast<uint32_t>(a.stages) * a.k_bytes;
   a.off_zero = a.off_staging + static_cast<uint32_t>(staging_bytes);
-  a.off_stats = a.off_zero + kBoxBytes;
+  a.off_stats = a.off_zero + kZeroBytes;
   a.off_bars = a.off_stats + kStatsBytes;
   a.off_misc = a.off_bars + 8u * static_cast<uint32_t>(10 + 2 * a.stages + 2 * kRingDepth);
   const size_t smem = a.off_misc + 16 + 4 * kRingDepth + 1024;
 
-  CUtensorMap map_qkv, map_out;
+  CUtensorMap map_qkv, map_out, map_zero;
   {
     const uint64_t dims[4] = {static_cast<uint64_t>(HS), static_cast<uint64_t>(3 * NH),
                               static_cast<uint64_t>(T), static_cast<uint64_t>(B)};
@@ -600,8 +690,13 @@ int softmax_launch(float* out, const void* qkv, int B, int T, int C, int NH, cud
     int rc = encode_tiled(&map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, out, dims, strides, box,
                           CU_TENSOR_MAP_SWIZZLE_128B, err);
     if (rc != CSA_OK) return rc;
+    const uint32_t zbox[3] = {kZeroCols, kZeroRows, 1};
+    rc = encode_tiled(&map_zero, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, out, dims, strides, zbox,
+                      CU_TENSOR_MAP_SWIZZLE_NONE, err);
+    if (rc != CSA_OK) return rc;
   } else {
     std::memset(&map_out, 0, sizeof map_out);
+    std::memset(&map_zero, 0, sizeof map_zero);
   }
   {
     static std::mutex mu;
@@ -622,7 +717,7 @@ int softmax_launch(float* out, const void* qkv, int B, int T, int C, int NH, cud
       }
       sched_base[dev.device] = static_cast<unsigned int*>(p);
     }
-    a.sched = sched_base[dev.device] + 2 * (launch_seq.fetch_add(1) % kSlots);
+    a.sched = sched_base[dev.device] + kSchedWords * (launch_seq.fetch_add(1) % kSlots);
   }
   cudaError_t e = cudaFuncSetAttribute(softmax_sm103a_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -633,7 +728,7 @@ int softmax_launch(float* out, const void* qkv, int B, int T, int C, int NH, cud
   }
   const long long grid = std::min<long long>(a.n_units, dev.sm_count);
   softmax_sm103a_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(map_qkv, map_out,
-                                                                                 a);
+                                                                                 map_zero, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     err = std::string("causal_softmax_forward: launch: ") + cudaGetErrorString(e);
