@@ -8,11 +8,13 @@
 // (B, T, 3, NH, HS) tensor (trimul_global's q/k pointers, Chapter II) with no
 // permute pass.
 //
-// Design (one persistent launch, one CTA per SM, 6 warps):
+// Design (one persistent launch, one CTA per SM, 11 warps):
 //  - tile space: for every (b, h) the ceil(T/128)^2 output tiles of 128 x 128;
 //    tiles with t2-tile <= t-tile are "lower" (MMA + epilogue), the others are
-//    "fill" tiles that only receive the mask pattern. In lower-only mode the
-//    fill tiles are not enumerated at all. Tiles are dealt round-robin to CTAs.
+//    "fill" tiles that only receive the mask pattern (not written at all in
+//    lower-only mode). The lower tiles form the work list that the producer,
+//    MMA and epilogue warps walk; the fill tiles form a separate launch-wide
+//    pool (warp 10).
 //  - warp 0 (one lane): TMA producer. A 4-D tensor map (HS, 3*NH, T, B) over
 //    the packed QKV addresses the query of head h at index h and its key at
 //    NH + h; rows past T and columns past HS arrive zero-filled. Q and K tiles
@@ -20,12 +22,19 @@
 //  - warp 1 (one lane): tcgen05.mma issuer, M=128 N=128 K=16, bf16 x bf16 ->
 //    fp32 into one of two TMEM accumulators (256 columns), so the epilogue of
 //    one tile overlaps the MMA of the next.
-//  - warps 2..5: epilogue. Each warp owns 32 rows (its TMEM lane quarter):
-//    tcgen05.ld 32 columns, multiply by 1/sqrt(HS), write the mask above the
+//  - warps 2..9: epilogue. Each warp owns 32 rows (its TMEM lane quarter) and
+//    64 columns: tcgen05.ld, multiply by 1/sqrt(HS), write the mask above the
 //    diagonal on diagonal tiles, stage through swizzled shared memory and
-//    issue 32 x 32 TMA stores (clipped at T). Fill tiles are TMA-stored from a
-//    resident 4 KB mask box. When T % 4 != 0 the output rows are not 16-byte
-//    aligned, so the same staged data is written with coalesced plain stores.
+//    issue 32 x 32 TMA stores (clipped at T). When T % 4 != 0 the output rows
+//    are not 16-byte aligned, so the same staged data is written with
+//    coalesced plain stores.
+//  - warp 10: fill writer. It takes fill tiles from the launch-wide pool while
+//    the epilogue has nothing to store (start-up, a wait on the MMA, after the
+//    last lower tile) and writes each as 128 x 16 TMA stores of a resident
+//    mask buffer, two tiles in flight at most. The operand loads queue behind
+//    the launch's writes in the memory system, so the epilogue stalls now and
+//    then; the fills keep the SM's write stream going meanwhile, and the pool
+//    evens out the end of the launch across SMs.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -56,7 +65,10 @@ constexpr int kChunkBytes = kTile * 128;  // one 128-row x 64-element operand ch
 #endif
 
 constexpr int kEpiWarps = 8;        // two per TMEM lane quarter
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kFillWarp = 2 + kEpiWarps;
+constexpr int kThreads = 64 + 32 * kEpiWarps + 32;
+constexpr int kFillCols = 128, kFillRows = 16;  // fill-writer TMA box
+constexpr int kFillBytes = kFillCols * kFillRows * 4;
 constexpr int kSlabCols = 64;       // accumulator columns per epilogue warp
 constexpr int kBoxBytes = 32 * 32 * 4;  // one 32 x 32 fp32 TMA store box
 constexpr int kTmemCols = 2 * kTile;
@@ -68,11 +80,11 @@ struct TrimulArgs {
                            // both at outer index bh / nh_div
   uint32_t causal;         // 1: triangular tiles, mask above the diagonal; 0: all tiles
   int kchunks, ksteps, stages;
-  long long n_lower;  // tiles with t2-tile <= t-tile: MMA + epilogue
-  long long n_fill;   // tiles with t2-tile > t-tile: mask stores only (0 in lower-only mode)
-  int n_total;          // n_lower + n_fill: length of the work list
+  int n_lower;  // tiles with t2-tile <= t-tile (all tiles when not causal): the work list
+  int n_fill;   // tiles with t2-tile > t-tile: the fill pool (0 in lower-only mode)
   int per_lower, per_fill;  // lower / fill tiles per (b, h)
-  unsigned int* sched;  // this launch's counter pair: [0] next position, [1] CTAs done
+  uint32_t dynamic;     // 1: work-list positions from the shared counter; 0: dealt statically
+  unsigned int* sched;  // this launch's counters: [0] next position, [1] CTAs done, [2] next fill
   float scale;
   uint32_t mask_bits;
   uint32_t lower_only;
@@ -85,10 +97,13 @@ struct TrimulArgs {
   uint32_t stage_bytes, off_staging, off_mask, off_bars, off_misc;
 };
 
-// Work-list counters, one pair per launch in flight (slot chosen by the host);
-// the last CTA of a launch resets its pair to zero.
+// Counters per launch: [0] work-list position, [1] finished CTAs, [2] fill tile.
+constexpr int kSchedWords = 4;
+
+// Work-list counters, one set per launch in flight (slot chosen by the host);
+// the last CTA of a launch resets its set to zero.
 constexpr int kSchedSlots = 256;
-__device__ unsigned int g_trimul_sched[kSchedSlots][2];
+__device__ unsigned int g_trimul_sched[kSchedSlots][kSchedWords];
 
 #ifndef CSA_TRIMUL_SCHED_DEPTH
 #define CSA_TRIMUL_SCHED_DEPTH 4
@@ -100,20 +115,12 @@ constexpr int kSchedDepth = CSA_TRIMUL_SCHED_DEPTH;  // positions buffered betwe
 constexpr int kFetchAhead = CSA_TRIMUL_FETCH_AHEAD;  // work-list fetches in flight (1..4)
 constexpr unsigned int kEntryEnd = 0xFFFFFFFFu;      // ring entry: no more work
 
-// Position p of the work list: (b, h)-major, so CTAs working at the same time
-// share Q and K tiles in L2; within one (b, h) its per_fill fill tiles are
-// spread evenly among its per_lower lower tiles (exact small-integer test).
-// Returns true for a fill tile; r is its index among the (b, h)'s fill or
-// lower tiles.
-__device__ __forceinline__ bool position_is_fill(int p, int per_lower, int per_fill, int& bh,
-                                                 int& r) {
-  const int per = per_lower + per_fill;
-  bh = p / per;
-  const int q = p - bh * per;
-  const int f0 = (q * per_fill) / per;
-  const int f1 = ((q + 1) * per_fill) / per;
-  r = (f1 > f0) ? f0 : q - f0;
-  return f1 > f0;
+// Position p of the work list: (b, h) = p / per_lower, so CTAs working at the
+// same time share Q and K tiles in L2; r = p % per_lower is the tile's number
+// among the (b, h)'s computed tiles.
+__device__ __forceinline__ void decode_position(int p, int per_lower, int& bh, int& r) {
+  bh = p / per_lower;
+  r = p - bh * per_lower;
 }
 
 // Largest i with i * (i + 1) / 2 <= r.
@@ -153,7 +160,8 @@ __device__ __forceinline__ void decode_fill(int r, int& ti, int& tj) {
 __global__ void __launch_bounds__(kThreads, 1)
     trimul_sm103a_kernel(const __grid_constant__ CUtensorMap tmap_a,
                          const __grid_constant__ CUtensorMap tmap_b,
-                         const __grid_constant__ CUtensorMap tmap_out, const TrimulArgs a) {
+                         const __grid_constant__ CUtensorMap tmap_out,
+                         const __grid_constant__ CUtensorMap tmap_fill, const TrimulArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -173,6 +181,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto sched_entry = [&](int s) { return base + a.off_misc + 16u + 4u * s; };
   const uint32_t tmem_slot = base + a.off_misc;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + a.off_misc + 4);
+  // Set while the epilogue has nothing to store; the fill writer works then.
+  volatile int* epi_idle = reinterpret_cast<volatile int*>(gbase + a.off_misc + 8);
   const uint32_t mask_box = base + a.off_mask;
   auto q_chunk = [&](int s, int kc) { return base + s * a.stage_bytes + kc * kChunkBytes; };
   auto k_chunk = [&](int s, int kc) {
@@ -196,12 +206,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(sempty_bar(s), 1 + kEpiWarps);
     }
     *abort_flag = 0;
+    *epi_idle = 1;
     fence_barrier_init();
   }
-  // The resident mask box that fill tiles are stored from.
-  for (uint32_t w = threadIdx.x; w < kBoxBytes / 4; w += kThreads)
-    st_shared_b32(mask_box + 4u * w, a.mask_bits);
-  fence_proxy_async_smem();
+  // The resident mask buffer that fill tiles are stored from.
+  if (a.n_fill > 0 && a.tma_store) {
+    for (uint32_t w = threadIdx.x; w < kFillBytes / 4; w += kThreads)
+      st_shared_b32(mask_box + 4u * w, a.mask_bits);
+    fence_proxy_async_smem();
+  }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
@@ -221,13 +234,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t issued = 0, issued_parity = 0;  // per-stage: loads that may be in flight
       bool injected = false;
       const uint32_t tx = static_cast<uint32_t>(a.kchunks) * 2u * kChunkBytes;
-      // Work list: every tile of the launch, fill tiles spread evenly among the
-      // lower ones. With fill tiles present, positions are taken from a shared
-      // counter (kFetchAhead fetches in flight), so SMs that get more memory
-      // bandwidth take more tiles; in lower-only mode every tile needs operands
-      // fetched ahead, so positions are dealt statically (c, c+G, ...) instead.
-      // Each position goes to the MMA and epilogue warps through the shared ring.
-      const bool dynamic = a.n_fill > 0;
+      // Work list: the computed tiles, (b, h)-major. Positions are taken from a
+      // shared counter (kFetchAhead fetches in flight) when a fill pool absorbs
+      // the imbalance that leaves, else dealt statically (c, c+G, ...) so that
+      // every CTA knows its operands ahead. Each position goes to the MMA and
+      // epilogue warps through the shared ring.
+      const bool dynamic = a.dynamic != 0;
       unsigned int static_next = blockIdx.x;
       auto fetch = [&]() -> unsigned int {
         if (dynamic) return atomicAdd(a.sched, 1u);
@@ -242,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t sphase = 0;
       while (true) {
         const unsigned int cur = pf[0];
-        const bool done = cur >= static_cast<unsigned int>(a.n_total);
+        const bool done = cur >= static_cast<unsigned int>(a.n_lower);
 #pragma unroll
         for (int i = 0; i < 3; ++i) pf[i] = pf[i + 1];
         if (!done) pf[kFetchAhead - 1] = fetch();
@@ -255,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (done) break;
         int bh, r, ti, tj;
-        if (position_is_fill(static_cast<int>(cur), a.per_lower, a.per_fill, bh, r)) continue;
+        decode_position(static_cast<int>(cur), a.per_lower, bh, r);
         decode_computed(r, a.causal, a.Tt2, ti, tj);
         if (!mbar_wait(empty_bar(stage), phase ^ 1u, wd, kSiteProducerEmpty)) break;
         const int outer = bh / a.nh_div, inner = bh - outer * a.nh_div;
@@ -308,8 +320,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           sphase ^= 1u;
         }
         if (cur == kEntryEnd) break;
-        int bh, r;
-        if (position_is_fill(static_cast<int>(cur), a.per_lower, a.per_fill, bh, r)) continue;
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, wd, kSiteMmaTmemEmpty)) break;
         tc_fence_after_sync();
         if (!mbar_wait(full_bar(stage), phase, wd, kSiteMmaFull)) break;
@@ -338,6 +348,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (!mbar_test(drain_bar, 0) && globaltimer_ns() - t0 < a.wait_limit_ns) {
       }
     }
+  } else if (warp == kFillWarp) {
+    // ------------------------------------------------------- fill writer --
+    const int T = a.T, T2 = a.T2;
+    const uint64_t once = l2_policy_evict_first();
+    bool ok = true;
+    while (ok) {
+      int f = 0;
+      if (lane == 0) {
+        // Wait (bounded) until the epilogue has nothing to store.
+        const uint64_t t0 = globaltimer_ns();
+        if (*abort_flag) ok = false;
+        for (uint32_t it = 0; ok && *epi_idle == 0; ++it) {
+          if (*abort_flag) {
+            ok = false;
+            break;
+          }
+          if ((it & 63u) == 63u && globaltimer_ns() - t0 > a.wait_limit_ns) {
+            *abort_flag = 1;
+            if (atomicCAS(a.status, 0, CSA_ERR_TIMEOUT) == 0) atomicExch(a.status + 1, kSiteSched);
+            ok = false;
+            break;
+          }
+          __nanosleep(64);
+        }
+        f = ok ? static_cast<int>(atomicAdd(a.sched + 2, 1u)) : a.n_fill;
+      }
+      f = __shfl_sync(0xffffffffu, f, 0);
+      if (f >= a.n_fill) break;
+      const int bh = f / a.per_fill;
+      int ti, tj;
+      decode_fill(f - bh * a.per_fill, ti, tj);
+      const int r0 = ti * kTile, c0 = tj * kTile;  // rows r0.. are all < T (ti < tj)
+      if (a.tma_store) {
+        if (lane == 0) {
+          // Columns past T2 - 1 are clipped by the tensor map.
+          for (int rr = 0; rr < kTile; rr += kFillRows)
+            tma_store_3d_hint(&tmap_fill, mask_box, c0, r0 + rr, bh, once);
+          bulk_commit();
+          bulk_wait_read<1>();  // two tiles in flight at most
+        }
+        __syncwarp();
+      } else {
+        const float m = __uint_as_float(a.mask_bits);
+        const int cols = min(kTile, T2 - c0);
+        float* blk = a.out + (static_cast<size_t>(bh) * T + r0) * T2 + c0;
+        for (int rr = 0; rr < kTile && r0 + rr < T; ++rr)
+          for (int i = static_cast<int>(lane); i < cols; i += 32)
+            blk[static_cast<size_t>(rr) * T2 + i] = m;
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   } else {
     // ---------------------------------------------------------- epilogue --
     // Warp e = warp - 2 owns the 32 rows of TMEM lane quarter warp % 4 (a warp may
@@ -371,35 +433,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         sphase ^= 1u;
       }
       int bh, rank, ti, tj;
-      const bool is_fill =
-          position_is_fill(static_cast<int>(cur), a.per_lower, a.per_fill, bh, rank);
-      if (is_fill) decode_fill(rank, ti, tj);
-      else decode_computed(rank, a.causal, a.Tt2, ti, tj);
+      decode_position(static_cast<int>(cur), a.per_lower, bh, rank);
+      decode_computed(rank, a.causal, a.Tt2, ti, tj);
       const int row0 = ti * kTile + q * 32;
       const int colw = tj * kTile + slab * kSlabCols;
-      if (is_fill) {
-        // Fill tile: mask pattern only (full mode).
-        if (row0 >= T || colw >= T2) continue;
-        if (a.tma_store) {
-          if (lane == 0) {
-            tma_store_3d(&tmap_out, mask_box, colw, row0, bh);
-            if (colw + 32 < T2) tma_store_3d(&tmap_out, mask_box, colw + 32, row0, bh);
-            bulk_commit();
-          }
-        } else {
-          float* orow = a.out + (static_cast<size_t>(bh) * T + row0) * T2;
-          const float m = __uint_as_float(a.mask_bits);
-          for (int rr = 0; rr < 32 && row0 + rr < T; ++rr) {
-            for (int c = 0; c < 2; ++c) {
-              const int col = colw + c * 32 + static_cast<int>(lane);
-              if (col < T2) orow[static_cast<size_t>(rr) * T2 + col] = m;
-            }
-          }
-        }
-        continue;
-      }
 
-      if (!mbar_wait_warp(tfull_bar(acc), acc_phase, wd, kSiteEpilogueFull)) break;
+      // Idle while the accumulator is not ready: the fill writer may store then.
+      if (ew == 0 && lane == 0) *epi_idle = 1;
+      const bool got = mbar_wait_warp(tfull_bar(acc), acc_phase, wd, kSiteEpilogueFull);
+      if (ew == 0 && lane == 0) *epi_idle = 0;
+      if (!got) break;
       tc_fence_after_sync();
       uint32_t v[kSlabCols];
       tmem_ld_64cols(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
@@ -470,6 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if (ew == 0 && lane == 0) *epi_idle = 1;
     if (lane == 0) bulk_wait_all();
     __syncwarp();
   }
@@ -484,6 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __threadfence();
     if (atomicAdd(a.sched + 1, 1u) == gridDim.x - 1) {
       atomicExch(a.sched, 0u);
+      atomicExch(a.sched + 2, 0u);
       atomicExch(a.sched + 1, 0u);
     }
   }
@@ -521,15 +566,16 @@ int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& 
                                      : static_cast<long long>(a.Tt) * a.Tt2;
   const long long per_fill =
       (causal && !lower_only) ? static_cast<long long>(a.Tt) * (a.Tt - 1) / 2 : 0;
-  a.n_lower = BH * per_lower;
-  a.n_fill = BH * per_fill;
-  if (a.n_lower + a.n_fill >= (1LL << 31) - (1LL << 20) || per_lower + per_fill >= (1LL << 20)) {
+  if (BH * per_lower >= (1LL << 31) - (1LL << 20) || BH * per_fill >= (1LL << 31) - (1LL << 20) ||
+      per_lower + per_fill >= (1LL << 20)) {
     err = name + ": too many tiles";
     return CSA_ERR_SHAPE;
   }
-  a.n_total = static_cast<int>(a.n_lower + a.n_fill);
+  a.n_lower = static_cast<int>(BH * per_lower);
+  a.n_fill = static_cast<int>(BH * per_fill);
   a.per_lower = static_cast<int>(per_lower);
   a.per_fill = static_cast<int>(per_fill);
+  a.dynamic = a.n_fill > 0 ? 1u : 0u;
   a.scale = scale;
   a.mask_bits = mask_bits;
   a.lower_only = lower_only ? 1u : 0u;
@@ -539,11 +585,11 @@ int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& 
   a.wait_limit_ns = wait_limit_ns();
   a.inject = inject ? 1 : 0;
 
-  // Shared memory: operand ring | staging boxes | mask box | barriers | misc.
+  // Shared memory: operand ring | staging boxes | mask buffer | barriers | misc.
   // Operand ring stages vs. staging depth: the most box pairs per epilogue warp
   // that still leave two ring stages, else one pair.
   a.stage_bytes = static_cast<uint32_t>(a.kchunks) * 2u * kChunkBytes;
-  const int fixed = kBoxBytes + 1024 /*bars+misc+ring*/ + 1024 /*align slack*/;
+  const int fixed = kFillBytes + 1024 /*bars+misc+ring*/ + 1024 /*align slack*/;
   int staging_bytes = 0;
   for (int groups = CSA_TRIMUL_MAX_STORE_GROUPS; groups >= 1; --groups) {
     staging_bytes = kEpiWarps * groups * 2 * kBoxBytes;
@@ -558,11 +604,11 @@ int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& 
   }
   a.off_staging = static_cast<uint32_t>(a.stages) * a.stage_bytes;
   a.off_mask = a.off_staging + static_cast<uint32_t>(staging_bytes);
-  a.off_bars = a.off_mask + kBoxBytes;
+  a.off_bars = a.off_mask + kFillBytes;
   a.off_misc = a.off_bars + 8u * static_cast<uint32_t>(2 * a.stages + 5 + 2 * kSchedDepth);
   const size_t smem = a.off_misc + 16 + 4 * kSchedDepth + 1024;
 
-  CUtensorMap map_out;
+  CUtensorMap map_out, map_fill;
   if (a.tma_store) {
     const uint64_t dims[3] = {static_cast<uint64_t>(T2), static_cast<uint64_t>(T),
                               static_cast<uint64_t>(BH)};
@@ -572,12 +618,17 @@ int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& 
     int rc = encode_tiled(&map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, out, dims, strides, box,
                           CU_TENSOR_MAP_SWIZZLE_128B, err);
     if (rc != CSA_OK) return rc;
+    const uint32_t fbox[3] = {kFillCols, kFillRows, 1};
+    rc = encode_tiled(&map_fill, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, out, dims, strides, fbox,
+                      CU_TENSOR_MAP_SWIZZLE_NONE, err);
+    if (rc != CSA_OK) return rc;
   } else {
     std::memset(&map_out, 0, sizeof map_out);
+    std::memset(&map_fill, 0, sizeof map_fill);
   }
 
   if (counters) {
-    a.sched = counters;  // caller-provided counter pair (zeroed before this launch)
+    a.sched = counters;  // caller-provided counters (zeroed before this launch)
   } else {
     static std::mutex mu;
     static unsigned int* sched_base[64] = {};
@@ -596,7 +647,7 @@ int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& 
       }
       sched_base[dev.device] = static_cast<unsigned int*>(p);
     }
-    a.sched = sched_base[dev.device] + 2 * (launch_seq.fetch_add(1) % kSchedSlots);
+    a.sched = sched_base[dev.device] + kSchedWords * (launch_seq.fetch_add(1) % kSchedSlots);
   }
   cudaError_t e = cudaFuncSetAttribute(trimul_sm103a_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -605,9 +656,10 @@ int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& 
     err = name + ": cudaFuncSetAttribute: " + cudaGetErrorString(e);
     return CSA_ERR_LAUNCH;
   }
-  const long long grid = std::min<long long>(a.n_total, dev.sm_count);
-  trimul_sm103a_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(map_a, map_b,
-                                                                                map_out, a);
+  const long long grid = std::min<long long>(static_cast<long long>(a.n_lower) + a.n_fill,
+                                            dev.sm_count);
+  trimul_sm103a_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(
+      map_a, map_b, map_out, map_fill, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     err = name + ": launch: " + cudaGetErrorString(e);
@@ -698,8 +750,8 @@ static __device__ __align__(256) unsigned int g_trimul_noalloc_scratch[kNoallocS
 int trimul_launch_noalloc(float* out, const void* qkv, int B, int T, int C, int NH,
                           uint32_t mask_bits, uint32_t flags, cudaStream_t stream,
                           const DeviceInfo& dev, std::string& err) {
-  // What this call keeps in the scratch: the two 32-bit work-list counters.
-  constexpr size_t kNeeded = 2 * sizeof(unsigned int);
+  // What this call keeps in the scratch: the kernel's 32-bit work-list counters.
+  constexpr size_t kNeeded = kSchedWords * sizeof(unsigned int);
   static_assert(kNeeded <= kNoallocScratchBytes, "scratch array too small");
   // The counters index the work list; a list beyond their range is rejected.
   const long long Tt = (static_cast<long long>(T) + kTile - 1) / kTile;
