@@ -413,6 +413,32 @@ __device__ __forceinline__ void tmem_wait_ld_64(uint32_t (&r)[64]) {
       : "memory");
 }
 
+// Packed fp32 pairs (Blackwell f32x2 arithmetic: two lanes per instruction).
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// (y0, y1) = (x0, x1) * b + c, each lane rounded once (round to nearest).
+__device__ __forceinline__ void fma_f32x2(float& y0, float& y1, float x0, float x1, uint64_t b,
+                                          uint64_t c) {
+  asm("{\n\t.reg .b64 a, d;\n\tmov.b64 a, {%2, %3};\n\tfma.rn.f32x2 d, a, %4, %5;\n\t"
+      "mov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(y0), "=f"(y1)
+      : "f"(x0), "f"(x1), "l"(b), "l"(c));
+}
+
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // 2^x by the PTX approximate base-2 exponential (results below the smallest
 // normal float flush to 0); its documented error is a few units in the last
 // place of fp32.

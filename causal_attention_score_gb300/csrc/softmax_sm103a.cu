@@ -21,7 +21,8 @@
 //    Pass 1 keeps, per row, the running maximum m and sum l of exp2 of the
 //    scores (log2 domain); the two warps holding the two halves of a row then
 //    combine (m, l) through shared memory behind a bounded mbarrier. Pass 2
-//    recomputes each tile and writes exp2(x - m) / l, staged through swizzled
+//    recomputes each tile and writes exp2((x - m) - log2 l) (the maximum and
+//    the log-sum kept apart, as the article does), staged through swizzled
 //    shared memory into 32 x 32 TMA stores (plain stores when T % 4 != 0).
 //  - warp 10: writes the tiles above the diagonal (probability 0) from a global
 //    pool of 128 x 128 zero tiles, as 128 x 16 TMA stores of a zeroed shared
@@ -421,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // arithmetic; exactly one load is outstanding whenever a buffer is in use.
       const int n = ti + 1;
       const float sc = a.scale_log2e;
-      float m = -INFINITY, l = 0.0f, shift = 0.0f;
+      float m = -INFINITY, l = 0.0f, lg = 0.0f;
       uint32_t va[kSlabCols], vb[kSlabCols];
       int held = 0;
       auto issue = [&](uint32_t(&v)[kSlabCols]) -> bool {
@@ -479,9 +480,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 8; ++e) part[e] = 0.0f;
           if (full) {
+            // Pairs of columns through the packed fp32 pipe: x * sc - m, then the
+            // partial sums, two lanes per instruction.
+            const uint64_t sc2 = pack_f32x2(sc, sc), nm2 = pack_f32x2(-m, -m);
+            uint64_t p2[4];
 #pragma unroll
-            for (int e = 0; e < kSlabCols; ++e)
-              part[e & 7] += ex2_approx(fmaf(__uint_as_float(v[e]), sc, -m));
+            for (int j = 0; j < 4; ++j) p2[j] = 0ull;
+#pragma unroll
+            for (int e = 0; e < kSlabCols; e += 2) {
+              float t0, t1;
+              fma_f32x2(t0, t1, __uint_as_float(v[e]), __uint_as_float(v[e + 1]), sc2, nm2);
+              p2[(e >> 1) & 3] = add_f32x2(p2[(e >> 1) & 3], pack_f32x2(ex2_approx(t0), ex2_approx(t1)));
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) unpack_f32x2(p2[j], part[2 * j], part[2 * j + 1]);
           } else {
 #pragma unroll
             for (int e = 0; e < kSlabCols; ++e)
@@ -506,19 +518,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float mm = fmaxf(m, m2);
           const float ll = (m == -INFINITY ? 0.0f : l * ex2_approx(m - mm)) +
                            (m2 == -INFINITY ? 0.0f : l2 * ex2_approx(m2 - mm));
-          // exp2(x - m) / l = exp2(x - (m + log2 l)): pass 2 needs one shift.
-          shift = mm + log2f(ll);
+          // Pass 2 writes exp2((x - m) - log2 l): the maximum is subtracted first
+          // and log2 l kept apart from it, since folding the two into one number
+          // loses log2 l's low bits when the maximum is large.
+          m = mm;
+          lg = log2f(ll);
           if (ew == 0 && lane == 0) *epi_storing = 1;
           return true;
         }
         if (full) {
+          const uint64_t sc2 = pack_f32x2(sc, sc), nm2 = pack_f32x2(-m, -m);
+          const uint64_t nl2 = pack_f32x2(-lg, -lg);
 #pragma unroll
-          for (int e = 0; e < kSlabCols; ++e)
-            v[e] = __float_as_uint(ex2_approx(fmaf(__uint_as_float(v[e]), sc, -shift)));
+          for (int e = 0; e < kSlabCols; e += 2) {
+            float t0, t1;
+            fma_f32x2(t0, t1, __uint_as_float(v[e]), __uint_as_float(v[e + 1]), sc2, nm2);
+            float u0, u1;
+            unpack_f32x2(add_f32x2(pack_f32x2(t0, t1), nl2), u0, u1);
+            v[e] = __float_as_uint(ex2_approx(u0));
+            v[e + 1] = __float_as_uint(ex2_approx(u1));
+          }
         } else {
 #pragma unroll
           for (int e = 0; e < kSlabCols; ++e)
-            v[e] = e <= lim ? __float_as_uint(ex2_approx(fmaf(__uint_as_float(v[e]), sc, -shift)))
+            v[e] = e <= lim ? __float_as_uint(ex2_approx(fmaf(__uint_as_float(v[e]), sc, -m) - lg))
                             : 0u;
         }
         if (row0 >= T || colw >= T) return true;
