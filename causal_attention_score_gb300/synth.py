@@ -92,6 +92,20 @@ def trimul_input(shape: TrimulShape, seed: int = 0, dist: str = "normal") -> tor
     raise ValueError(dist)
 
 
+def trimul_input_f32(shape: TrimulShape, seed: int = 0, dist: str = "uniform") -> torch.Tensor:
+    """Packed QKV (B, T, 3, NH, HS) fp32 on the CPU, not rounded to bf16.
+
+    dist="uniform": iid uniform[-1, 1] (what the page's ``main`` fills its fp32
+    input with); "normal": iid N(0, 1).
+    """
+    g = torch.Generator().manual_seed(seed)
+    if dist == "uniform":
+        return torch.rand(shape.qkv_shape, generator=g, dtype=torch.float32) * 2.0 - 1.0
+    if dist == "normal":
+        return torch.randn(shape.qkv_shape, generator=g, dtype=torch.float32)
+    raise ValueError(dist)
+
+
 def dense_input(shape: DenseShape, seed: int = 0):
     """(X [M, I], W [H, I]) bf16 iid uniform[-1, 1]; X is drawn first, then W,
     from one generator seeded with ``seed``."""

@@ -10,6 +10,8 @@ pages it follows:
 
 * ``trimul`` / ``trimul_rows``: the CPU referee ``trimul_cpu`` of
   "llm.c dev/cuda/trimat_forward.cu" (Chapter I).
+* ``trimul_f32`` / ``trimul_f32_rows``: the same referee over its own fp32
+  input type (no bf16 rounding of the inputs).
 * ``dense`` / ``dense_rows``: the dense workload ``Y = X W^T`` of
   "DietCode tests/codegen/test_1_local_padding.py" (test_local_padding
   docstring).
@@ -18,8 +20,8 @@ pages it follows:
 * ``bmm_nt``: the batched NT workload of the same file (test_local_padding_ii
   docstring), ``Y[i, j, k] = sum_l X[i, j, l] W[i, k, l]``.
 
-Inputs are bf16 tensors passed as their raw 16-bit patterns (numpy uint16);
-outputs are float64.
+Inputs are bf16 tensors passed as their raw 16-bit patterns (numpy uint16),
+or numpy float32 for the fp32-input functions; outputs are float64.
 """
 from __future__ import annotations
 
@@ -74,9 +76,12 @@ class Oracle:
         self.lib.oracle_bmm_nt.argtypes = [dp, up, up, i64, i64, i64, i64]
         self.lib.oracle_causal_softmax.argtypes = [dp, up, i64, i64, i64, i64]
         self.lib.oracle_causal_softmax_rows.argtypes = [dp, up, i64, i64, i64, i64, lp, i64]
+        fp = ctypes.POINTER(ctypes.c_float)
+        self.lib.oracle_trimul_f32.argtypes = [dp, fp, i64, i64, i64, i64, ctypes.c_int]
+        self.lib.oracle_trimul_f32_rows.argtypes = [dp, fp, i64, i64, i64, i64, lp, i64, ctypes.c_int]
         for f in ("oracle_trimul", "oracle_trimul_rows", "oracle_dense", "oracle_dense_rows",
                   "oracle_bmm_nt", "oracle_causal_softmax", "oracle_causal_softmax_rows",
-                  "oracle_num_threads"):
+                  "oracle_trimul_f32", "oracle_trimul_f32_rows", "oracle_num_threads"):
             getattr(self.lib, f).restype = ctypes.c_int
         self.lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         self.lib.oracle_set_num_threads.restype = None
@@ -113,6 +118,33 @@ class Oracle:
                                          idx.shape[0], mask)
         if rc != 0:
             raise ValueError(f"oracle_trimul_rows rejected the arguments (rc={rc})")
+        return out
+
+    # -- causal score product, fp32 inputs -------------------------------
+    def trimul_f32(self, qkv_f32: np.ndarray, B: int, T: int, C: int, NH: int,
+                   mask: int = MASK_NAN) -> np.ndarray:
+        """Scores (B, NH, T, T) float64 of the packed (B, T, 3, NH, HS) fp32 input."""
+        q = np.ascontiguousarray(qkv_f32, dtype=np.float32)
+        if q.size != B * T * 3 * C:
+            raise ValueError("qkv size does not match (B, T, 3, C)")
+        out = np.empty((B, NH, T, T), dtype=np.float64)
+        rc = self.lib.oracle_trimul_f32(_ptr(out, ctypes.c_double), _ptr(q, ctypes.c_float),
+                                        B, T, C, NH, mask)
+        if rc != 0:
+            raise ValueError(f"oracle_trimul_f32 rejected the shape (rc={rc})")
+        return out
+
+    def trimul_f32_rows(self, qkv_f32: np.ndarray, B: int, T: int, C: int, NH: int,
+                        bht: np.ndarray, mask: int = MASK_NAN) -> np.ndarray:
+        """Rows out[b, h, t, :] of the fp32-input scores for each (b, h, t) in bht."""
+        q = np.ascontiguousarray(qkv_f32, dtype=np.float32)
+        idx = np.ascontiguousarray(bht, dtype=np.int64).reshape(-1, 3)
+        out = np.empty((idx.shape[0], T), dtype=np.float64)
+        rc = self.lib.oracle_trimul_f32_rows(_ptr(out, ctypes.c_double), _ptr(q, ctypes.c_float),
+                                             B, T, C, NH, _ptr(idx, ctypes.c_int64),
+                                             idx.shape[0], mask)
+        if rc != 0:
+            raise ValueError(f"oracle_trimul_f32_rows rejected the arguments (rc={rc})")
         return out
 
     # -- dense layer -------------------------------------------------------

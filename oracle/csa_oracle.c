@@ -24,6 +24,10 @@
  *    the causal scores of trimul_cpu (whose comment says it is taken from the
  *    attention forward pass, where a softmax over t2 <= t follows), masked
  *    positions t2 > t get probability 0.
+ *  - "llm.c dev/cuda/trimat_forward.cu" again for fp32 inputs: the referee
+ *    takes `const float* inp`, and `main` fills it with fp32 random numbers;
+ *    oracle_trimul_f32 is the same definition over fp32 inputs, with no
+ *    rounding of the inputs at all (fp32 widens to double exactly).
  *  - the same file, test_local_padding_ii docstring, the batched NT workload:
  *    Y[i, j, k] += X[i, j, l] * W[i, k, l] with X [B*NH, T, H/NH],
  *    W [B*NH, T, H/NH], Y [B*NH, T, T] (the unmasked, unscaled score product;
@@ -155,6 +159,67 @@ int oracle_trimul_rows(double *out, const uint16_t *qkv, int64_t B, int64_t T,
     for (int64_t i = 0; i < n; i++)
         score_row(out + i * T, qkv, T, C, NH, bht[3 * i], bht[3 * i + 1],
                   bht[3 * i + 2], mask);
+    return 0;
+}
+
+/*
+ * The same score row over fp32 inputs (the referee's own input type):
+ * out[b][h][t][0..T-1] with Q at qkv[b][t][0][h][:] and K at qkv[b][t2][1][h][:].
+ */
+static void score_row_f32(double *dst, const float *qkv, int64_t T, int64_t C,
+                          int64_t NH, int64_t b, int64_t h, int64_t t, double mask)
+{
+    const int64_t HS = C / NH;
+    const int64_t C3 = 3 * C;
+    const float *query = qkv + b * T * C3 + t * C3 + h * HS;
+    const double root_hs = sqrt((double)HS);
+
+    for (int64_t t2 = 0; t2 <= t; t2++) {
+        const float *key = qkv + b * T * C3 + t2 * C3 + h * HS + C;
+        double acc = 0.0;
+        for (int64_t d = 0; d < HS; d++)
+            acc += (double)query[d] * (double)key[d];
+        dst[t2] = acc / root_hs;
+    }
+    for (int64_t t2 = t + 1; t2 < T; t2++)
+        dst[t2] = mask;
+}
+
+/* Full causal score tensor of fp32 inputs, (B, NH, T, T) doubles. */
+int oracle_trimul_f32(double *out, const float *qkv, int64_t B, int64_t T,
+                      int64_t C, int64_t NH, int mask_kind)
+{
+    if (check_trimul_shape(B, T, C, NH))
+        return -2;
+    const double mask = mask_value(mask_kind);
+    const int64_t rows = B * NH * T;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t r = 0; r < rows; r++) {
+        const int64_t t = r % T;
+        const int64_t h = (r / T) % NH;
+        const int64_t b = r / (T * NH);
+        score_row_f32(out + r * T, qkv, T, C, NH, b, h, t, mask);
+    }
+    return 0;
+}
+
+/* Selected rows (b, h, t) of the fp32-input score tensor, n x T doubles. */
+int oracle_trimul_f32_rows(double *out, const float *qkv, int64_t B, int64_t T,
+                           int64_t C, int64_t NH, const int64_t *bht, int64_t n,
+                           int mask_kind)
+{
+    if (check_trimul_shape(B, T, C, NH))
+        return -2;
+    for (int64_t i = 0; i < n; i++) {
+        const int64_t b = bht[3 * i], h = bht[3 * i + 1], t = bht[3 * i + 2];
+        if (b < 0 || b >= B || h < 0 || h >= NH || t < 0 || t >= T)
+            return -2;
+    }
+    const double mask = mask_value(mask_kind);
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t i = 0; i < n; i++)
+        score_row_f32(out + i * T, qkv, T, C, NH, bht[3 * i], bht[3 * i + 1],
+                      bht[3 * i + 2], mask);
     return 0;
 }
 

@@ -60,6 +60,11 @@ def _random_qkv(B, T, NH, HS, seed, dist="uniform"):
     return synth.bf16_bits(t).reshape(-1)
 
 
+def _random_qkv_f32(B, T, NH, HS, seed, dist="uniform"):
+    shape = synth.TrimulShape(B=B, T=T, C=NH * HS, NH=NH)
+    return synth.trimul_input_f32(shape, seed=seed, dist=dist).numpy().reshape(-1)
+
+
 def _split_qk(qkv_u16, B, T, NH, HS):
     f = _u16_to_f32(qkv_u16).astype(np.float64).reshape(B, T, 3, NH, HS)
     Q = f[:, :, 0].transpose(0, 2, 1, 3)  # (B, NH, T, HS)
@@ -398,6 +403,83 @@ def pin_softmax_causality_and_rows(o):
         assert np.array_equal(rows[i], P[b, h, t])
 
 
+# ------------------------------------------ score product, fp32 inputs pins --
+
+def pin_trimul_f32_exact_rational(o):
+    """fp32 inputs finer than bf16, through exact rationals, then one division by sqrt(HS)."""
+    for (B, T, NH, HS, seed) in [(2, 6, 2, 8, 11), (1, 4, 1, 12, 12)]:
+        C = NH * HS
+        x = _random_qkv_f32(B, T, NH, HS, seed)
+        assert np.any(x.view(np.uint32) & 0xFFFF), "inputs must not all be bf16 values"
+        f = x.reshape(B, T, 3, NH, HS)
+        out = o.trimul_f32(x, B, T, C, NH, MASK_NAN)
+        root = math.sqrt(HS)
+        for b in range(B):
+            for h in range(NH):
+                for t in range(T):
+                    for t2 in range(T):
+                        if t2 > t:
+                            assert math.isnan(out[b, h, t, t2])
+                            continue
+                        exact = sum(Fraction(float(f[b, t, 0, h, d])) * Fraction(float(f[b, t2, 1, h, d]))
+                                    for d in range(HS))
+                        want = float(exact) / root
+                        assert abs(out[b, h, t, t2] - want) <= 1e-15 * (1.0 + abs(want))
+
+
+def pin_trimul_f32_matmul_identity(o):
+    """Lower triangle of torch.matmul(Q, K^T) in float64 over the fp32 inputs, over
+    sqrt(HS); -inf above (mask kind 1)."""
+    B, T, NH, HS = 2, 33, 3, 20
+    x = _random_qkv_f32(B, T, NH, HS, 13, "normal")
+    out = torch.from_numpy(o.trimul_f32(x, B, T, NH * HS, NH, MASK_NEG_INF))
+    f = torch.from_numpy(x.reshape(B, T, 3, NH, HS).astype(np.float64))
+    Q = f[:, :, 0].permute(0, 2, 1, 3)
+    K = f[:, :, 1].permute(0, 2, 1, 3)
+    ref = torch.matmul(Q, K.transpose(-1, -2)) / math.sqrt(HS)
+    lower = torch.tril(torch.ones(T, T, dtype=torch.bool))
+    assert torch.allclose(out[..., lower], ref[..., lower], rtol=1e-13, atol=1e-13)
+    assert torch.all(torch.isneginf(out[..., ~lower]))
+
+
+def pin_trimul_f32_agrees_with_bf16_referee(o):
+    """On inputs that are bf16 values, the fp32-input and bf16-input referees are the
+    same function, to the bit (both widen exactly and sum in the same order)."""
+    B, T, NH, HS = 2, 40, 2, 16
+    u16 = _random_qkv(B, T, NH, HS, 14)
+    a = o.trimul_f32(_u16_to_f32(u16), B, T, NH * HS, NH, MASK_NAN)
+    b = o.trimul(u16, B, T, NH * HS, NH, MASK_NAN)
+    assert np.array_equal(a, b, equal_nan=True)
+
+
+def pin_trimul_f32_causality_and_rows(o):
+    """Changing key row s changes exactly column s of rows t >= s; changing query row t
+    changes exactly row t's columns t2 <= t; sampled rows match."""
+    B, T, NH, HS = 2, 9, 2, 8
+    x = _random_qkv_f32(B, T, NH, HS, 15)
+    P = o.trimul_f32(x, B, T, NH * HS, NH, MASK_NAN)
+    f = x.reshape(B, T, 3, NH, HS)
+    s = 4
+    k2 = f.copy()
+    k2[1, s, 1, 0] += 0.375
+    P2 = o.trimul_f32(k2.reshape(-1), B, T, NH * HS, NH, MASK_NAN)
+    diff = ~((P2 == P) | (np.isnan(P2) & np.isnan(P)))
+    want = np.zeros_like(diff)
+    want[1, 0, s:, s] = True
+    assert np.array_equal(diff, want)
+    q2 = f.copy()
+    q2[0, s, 0, 1] -= 0.25
+    P3 = o.trimul_f32(q2.reshape(-1), B, T, NH * HS, NH, MASK_NAN)
+    diff = ~((P3 == P) | (np.isnan(P3) & np.isnan(P)))
+    want = np.zeros_like(diff)
+    want[0, 1, s, :s + 1] = True
+    assert np.array_equal(diff, want)
+    bht = np.array([[0, 0, 0], [1, 1, 8], [0, 1, 4]])
+    rows = o.trimul_f32_rows(x, B, T, NH * HS, NH, bht, MASK_NAN)
+    for i, (b, h, t) in enumerate(bht):
+        assert np.array_equal(rows[i], P[b, h, t], equal_nan=True)
+
+
 SOFTMAX_PINS = [pin_softmax_matches_library_softmax, pin_softmax_large_scores_and_closed_form,
                 pin_softmax_causality_and_rows]
 
@@ -409,4 +491,7 @@ TRIMUL_PINS = [pin_trimul_exact_rational, pin_trimul_matmul_identity, pin_trimul
                pin_trimul_rows]
 DENSE_PINS = [pin_dense_exact_rational, pin_dense_matmul_identity, pin_dense_integer_exact,
               pin_dense_local_padding]
-ALL_PINS = TRIMUL_PINS + DENSE_PINS + BMM_PINS + SOFTMAX_PINS
+TRIMUL_F32_PINS = [pin_trimul_f32_exact_rational, pin_trimul_f32_matmul_identity,
+                   pin_trimul_f32_agrees_with_bf16_referee, pin_trimul_f32_causality_and_rows]
+
+ALL_PINS = TRIMUL_PINS + DENSE_PINS + BMM_PINS + SOFTMAX_PINS + TRIMUL_F32_PINS

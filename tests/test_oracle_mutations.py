@@ -48,6 +48,18 @@ MUTATIONS = [
     ("softmax_multiplies", "dst[t2] /= sum", "dst[t2] *= sum", oracle_pins.SOFTMAX_PINS),
     ("softmax_upper_not_zero", "dst[t2] = 0.0;\n}", "dst[t2] = 1e-30;\n}", oracle_pins.SOFTMAX_PINS),
     ("softmax_counts_terms", "sum += dst[t2];", "sum += 1.0;", oracle_pins.SOFTMAX_PINS),
+    ("f32_diagonal_dropped", "t2 <= t; t2++) {\n        const float *key", "t2 < t; t2++) {\n        const float *key",
+     oracle_pins.TRIMUL_F32_PINS),
+    ("f32_key_read_from_value", "const float *key = qkv + b * T * C3 + t2 * C3 + h * HS + C;",
+     "const float *key = qkv + b * T * C3 + t2 * C3 + h * HS + 2 * C;", oracle_pins.TRIMUL_F32_PINS),
+    ("f32_key_read_from_query", "acc += (double)query[d] * (double)key[d];",
+     "acc += (double)query[d] * (double)query[d];", oracle_pins.TRIMUL_F32_PINS),
+    ("f32_scale_by_hs", "acc += (double)query[d] * (double)key[d];\n        dst[t2] = acc / root_hs;",
+     "acc += (double)query[d] * (double)key[d];\n        dst[t2] = acc / (double)HS;", oracle_pins.TRIMUL_F32_PINS),
+    ("f32_batch_ignored", "const float *query = qkv + b * T * C3 + t * C3 + h * HS;",
+     "const float *query = qkv + t * C3 + h * HS;", oracle_pins.TRIMUL_F32_PINS),
+    ("f32_input_rounded_to_bf16", "acc += (double)query[d] * (double)key[d];",
+     "acc += (double)(float)(__bf16)query[d] * (double)(float)(__bf16)key[d];", oracle_pins.TRIMUL_F32_PINS),
     ("dense_bf16_truncated", "(uint32_t)h << 16", "((uint32_t)h << 16) & 0xFFFE0000u",
      oracle_pins.ALL_PINS),
 ]
