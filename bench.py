@@ -50,11 +50,11 @@ def dense_flops(M, I, H):
     return 2 * M * I * H
 
 
-def trimul_algorithmic_bytes(B, T, C, NH, lower_only=False):
+def trimul_algorithmic_bytes(B, T, C, NH, lower_only=False, in_bytes=2):
     """Minimum HBM traffic of one trimul_forward: every output element written once
-    (fp32), Q and K read once (bf16); V is never touched."""
+    (fp32), Q and K read once (bf16, or fp32 with in_bytes=4); V is never touched."""
     out = B * NH * (T * (T + 1) // 2 if lower_only else T * T) * 4
-    qk = 2 * B * T * C * 2
+    qk = 2 * B * T * C * in_bytes
     return out + qk
 
 
@@ -224,8 +224,11 @@ class Workload:
     the useful flops of a step, the dominant kernel's roofline terms, and the
     host<->device copies of the end-to-end variant."""
 
-    def __init__(self, name, config, parts, flops, roof, h2d, d2h):
+    def __init__(self, name, config, parts, flops, roof, h2d, d2h, dtype="bf16",
+                 data="synthetic (seeded N(0,1) / uniform[-1,1], rounded to bf16)"):
         self.name = name          # human-readable workload string (config.workload)
+        self.dtype = dtype        # arithmetic type of the path
+        self.data = data
         self.config = config      # extra config keys
         self.parts = parts        # [(label, fn(stream))]
         self.flops = flops        # useful flops per step
@@ -258,10 +261,10 @@ def make_workload(name, dev):
     def pinned_like(t):
         return torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
 
-    def finish(wl_name, config, parts, flops, roof, h2d, outs):
+    def finish(wl_name, config, parts, flops, roof, h2d, outs, **kw):
         h2d = [(d, h.pin_memory()) for d, h in h2d]
         d2h = [(pinned_like(o), o) for o in outs]
-        return Workload(wl_name, config, parts, flops, roof, h2d, d2h)
+        return Workload(wl_name, config, parts, flops, roof, h2d, d2h, **kw)
 
     ts, ds = synth.TRIMUL_GPT2, synth.DENSE_RAGGED
     if name == "step":
@@ -291,6 +294,24 @@ def make_workload(name, dev):
             {"part": 0, "kernel": "trimul_sm103a_kernel", "bound": "hbm",
              "per_launch": trimul_algorithmic_bytes(shape.B, shape.T, shape.C, shape.NH, lower)},
             th, to)
+    if name in ("trimul_f32_gpt2", "trimul_f32_long"):
+        shape = synth.TRIMUL_GPT2 if "gpt2" in name else synth.TRIMUL_LONG
+        qkv_h = synth.trimul_input_f32(shape, seed=0, dist="uniform")
+        qkv = qkv_h.to(dev)
+        out = torch.empty(shape.out_shape, dtype=torch.float32, device=dev)
+        fn = lambda st: csa.trimul_forward_f32(out, qkv, shape.B, shape.T, shape.C, shape.NH,
+                                               stream=st)
+        return finish(
+            f"trimul over fp32 inputs (3 x tf32), {'GPT-2-small' if 'gpt2' in name else 'long context'}"
+            f" (B={shape.B},T={shape.T},C={shape.C},NH={shape.NH},HS={shape.HS})",
+            {"trimul_f32": {"B": shape.B, "T": shape.T, "C": shape.C, "NH": shape.NH,
+                            "mask": "NaN"}},
+            [("trimul_f32", fn)], trimul_flops(shape.B, shape.T, shape.C, shape.NH),
+            {"part": 0, "kernel": "trimul_sm103a_kernel<fp32>", "bound": "hbm",
+             "per_launch": trimul_algorithmic_bytes(shape.B, shape.T, shape.C, shape.NH,
+                                                    in_bytes=4)},
+            [(qkv, qkv_h)], [out], dtype="tf32x3",
+            data="synthetic (seeded uniform[-1,1] fp32, not rounded)")
     if name in ("softmax_gpt2", "softmax_long"):
         shape = synth.TRIMUL_GPT2 if name == "softmax_gpt2" else synth.TRIMUL_LONG
         qkv_h = synth.trimul_input(shape, seed=0, dist="normal")
@@ -348,7 +369,8 @@ def make_workload(name, dev):
 
 
 WORKLOADS = ["step", "trimul_gpt2", "trimul_long", "trimul_gpt2_lower", "trimul_long_lower",
-             "dense_ragged", "dense_sweep", "bmm_nt", "softmax_gpt2", "softmax_long"]
+             "dense_ragged", "dense_sweep", "bmm_nt", "softmax_gpt2", "softmax_long",
+             "trimul_f32_gpt2", "trimul_f32_long"]
 
 
 def run_ours(args, rank, world, local):
@@ -482,8 +504,8 @@ def run_ours(args, rank, world, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) / uniform[-1,1], rounded to bf16)",
+        "dtype": wl.dtype,
+        "data": wl.data,
         "config": config,
         "pct_of_bf16_peak": round(100 * value / world / bf16_peak, 3),
         "roofline": roofline,

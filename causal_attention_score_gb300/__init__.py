@@ -3,6 +3,7 @@
 Public API (all compute runs in libcsa_gb300.so; see include/csa.h):
 
 * ``trimul_forward(out, qkv, B, T, C, NH, mask="nan", lower_only=False)``
+* ``trimul_forward_f32(out, qkv_f32, B, T, C, NH, mask="nan", lower_only=False)``
 * ``dense_xwt(Y, X, W, M, I, H)``
 * ``batch_matmul_nt(Y, X, W, batch, T1, T2, D)``
 * ``causal_softmax_forward(att, qkv, B, T, C, NH)``
@@ -15,10 +16,11 @@ from ._lib import (CSA_ERR_ALIGN, CSA_ERR_ARCH, CSA_ERR_CUDA, CSA_ERR_LAUNCH, CS
                    CSA_ERR_SHAPE, CSA_ERR_TIMEOUT, CSA_ERR_UNSUPPORTED, CSA_MASK_NAN,
                    CSA_MASK_NEG_INF, CSA_OK, CsaError)
 from .ops import (batch_matmul_nt, causal_softmax, causal_softmax_forward, debug_inject, dense,
-                  dense_xwt, get_status, set_wait_limit_ns, trimul, trimul_forward, version)
+                  dense_xwt, get_status, set_wait_limit_ns, trimul, trimul_forward,
+                  trimul_forward_f32, version)
 
 __all__ = [
-    "trimul_forward", "dense_xwt", "batch_matmul_nt", "causal_softmax_forward",
+    "trimul_forward", "trimul_forward_f32", "dense_xwt", "batch_matmul_nt", "causal_softmax_forward",
     "causal_softmax", "trimul", "dense", "get_status", "set_wait_limit_ns",
     "debug_inject", "version", "CsaError", "CSA_OK", "CSA_ERR_NULL", "CSA_ERR_SHAPE",
     "CSA_ERR_ALIGN", "CSA_ERR_UNSUPPORTED", "CSA_ERR_ARCH", "CSA_ERR_LAUNCH", "CSA_ERR_TIMEOUT",

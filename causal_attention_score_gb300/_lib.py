@@ -34,6 +34,7 @@ SIGNATURES = {
     "trimul_forward": (_i, [_vp, _vp, _i, _i, _i, _i]),
     "trimul_forward_ex": (_i, [_vp, _vp, _i, _i, _i, _i, _u32, _u32, _vp]),
     "trimul_forward_noalloc": (_i, [_vp, _vp, _i, _i, _i, _i, _u32, _u32, _vp]),
+    "trimul_forward_f32": (_i, [_vp, _vp, _i, _i, _i, _i, _u32, _u32, _vp]),
     "dense_xwt": (_i, [_vp, _vp, _vp, _i, _i, _i]),
     "batch_matmul_nt": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "causal_softmax_forward": (_i, [_vp, _vp, _i, _i, _i, _i, _vp]),

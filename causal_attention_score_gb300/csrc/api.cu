@@ -157,6 +157,31 @@ csa_status trimul_forward_ex(float* out, const void* qkv, int B, int T, int C, i
   return CSA_OK;
 }
 
+csa_status trimul_forward_f32(float* out, const float* qkv, int B, int T, int C, int NH,
+                              uint32_t mask_bits, uint32_t flags, void* stream) {
+  t_last_error.clear();
+  if (!out || !qkv) return set_error(CSA_ERR_NULL, "trimul_forward_f32: null pointer");
+  if (B <= 0 || T <= 0 || C <= 0 || NH <= 0)
+    return set_error(CSA_ERR_SHAPE, "trimul_forward_f32: B, T, C, NH must be >= 1");
+  if (C % NH != 0) return set_error(CSA_ERR_SHAPE, "trimul_forward_f32: C % NH != 0");
+  if (flags & ~CSA_TRIMUL_LOWER_ONLY)
+    return set_error(CSA_ERR_UNSUPPORTED, "trimul_forward_f32: unknown flags");
+  const int HS = C / NH;
+  if (HS % 4 != 0)
+    return set_error(CSA_ERR_ALIGN, "trimul_forward_f32: HS = C/NH must be a multiple of 4");
+  if (HS > 256) return set_error(CSA_ERR_UNSUPPORTED, "trimul_forward_f32: HS > 256");
+  if (reinterpret_cast<uintptr_t>(qkv) % 16 != 0 || reinterpret_cast<uintptr_t>(out) % 4 != 0)
+    return set_error(CSA_ERR_ALIGN, "trimul_forward_f32: qkv must be 16-byte aligned, out 4-byte");
+  DeviceInfo dev;
+  std::string err;
+  int rc = current_device(dev, err);
+  if (rc != CSA_OK) return set_error(rc, err);
+  rc = trimul_f32_launch(out, qkv, B, T, C, NH, mask_bits, flags,
+                         static_cast<cudaStream_t>(stream), dev, err);
+  if (rc != CSA_OK) return set_error(rc, err);
+  return CSA_OK;
+}
+
 csa_status trimul_forward_noalloc(float* out, const void* qkv, int B, int T, int C, int NH,
                                   uint32_t mask_bits, uint32_t flags, void* stream) {
   t_last_error.clear();

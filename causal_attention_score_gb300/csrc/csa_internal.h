@@ -43,6 +43,9 @@ int trimul_launch_noalloc(float* out, const void* qkv, int B, int T, int C, int 
                           uint32_t mask_bits, uint32_t flags, cudaStream_t stream,
                           const DeviceInfo& dev, std::string& err);
 
+int trimul_f32_launch(float* out, const float* qkv, int B, int T, int C, int NH,
+                      uint32_t mask_bits, uint32_t flags, cudaStream_t stream, const DeviceInfo& dev,
+                      std::string& err);
 int bmm_nt_launch(float* Y, const void* X, const void* W, int batch, int T1, int T2, int D,
                   cudaStream_t stream, const DeviceInfo& dev, std::string& err);
 

@@ -28,6 +28,14 @@
 //    issue 32 x 32 TMA stores (clipped at T). When T % 4 != 0 the output rows
 //    are not 16-byte aligned, so the same staged data is written with
 //    coalesced plain stores.
+//  - fp32 inputs ("kind::tf32" form, trimul_forward_f32): the referee's own
+//    input type, computed to fp32 accuracy with three tf32 products: each
+//    input x splits exactly into hi = x with its low 13 mantissa bits cleared
+//    (a tf32 value) and lo = x - hi (an fp32 value; its tf32 rounding costs
+//    2^-21 |x|), and each tile accumulates hi.hi + hi.lo + lo.hi (lo.lo is
+//    below 2^-20 |q.k|). A stage holds one 32-element chunk of the Q and K
+//    tiles; warps 11-14 split it in shared memory (hi in place, lo beside it)
+//    before the MMA warp reads it.
 //  - warp 10: fill writer. It takes fill tiles from the launch-wide pool while
 //    the epilogue has nothing to store (start-up, a wait on the MMA, after the
 //    last lower tile) and writes each as 128 x 16 TMA stores of a resident
@@ -54,6 +62,7 @@ namespace {
 
 constexpr int kTile = 128;          // output tile edge
 constexpr int kChunkElems = 64;     // bf16 per 128-byte swizzle row
+constexpr int kChunkElemsF32 = 32;  // fp32 per 128-byte swizzle row
 constexpr int kChunkBytes = kTile * 128;  // one 128-row x 64-element operand chunk
 // Tuning constants (compile-time): operand ring depth and staging box pairs per
 // epilogue warp; the host picks the deepest staging that still leaves two stages.
@@ -67,12 +76,16 @@ constexpr int kChunkBytes = kTile * 128;  // one 128-row x 64-element operand ch
 constexpr int kEpiWarps = 8;        // two per TMEM lane quarter
 constexpr int kFillWarp = 2 + kEpiWarps;
 constexpr int kThreads = 64 + 32 * kEpiWarps + 32;
+constexpr int kConvWarps = 4;  // fp32 form: warps 11-14 split each stage into hi and lo
+constexpr int kFirstConvWarp = kFillWarp + 1;
+constexpr int kThreadsF32 = kThreads + 32 * kConvWarps;
 constexpr int kFillCols = 128, kFillRows = 16;  // fill-writer TMA box
 constexpr int kFillBytes = kFillCols * kFillRows * 4;
 constexpr int kSlabCols = 64;       // accumulator columns per epilogue warp
 constexpr int kBoxBytes = 32 * 32 * 4;  // one 32 x 32 fp32 TMA store box
 constexpr int kTmemCols = 2 * kTile;
 constexpr uint32_t kIdesc = idesc_bf16_f32(kTile, kTile);
+constexpr uint32_t kIdescTf32 = idesc_tf32_f32(kTile, kTile);
 
 struct TrimulArgs {
   int T, T2, BH, Tt, Tt2;  // rows / columns of each (b, h) output and their tile counts
@@ -95,6 +108,9 @@ struct TrimulArgs {
   int inject;
   uint32_t store_groups;  // staging box pairs per epilogue warp (1 or 2)
   uint32_t stage_bytes, off_staging, off_mask, off_bars, off_misc;
+  // Operand chunks (128-byte rows) per stage, and stages per tile: bf16 keeps a
+  // whole tile's chunks in one stage; the fp32 form streams one chunk per stage.
+  int stage_chunks, tile_stages, chunk_elems;
 };
 
 // Counters per launch: [0] work-list position, [1] finished CTAs, [2] fill tile.
@@ -157,7 +173,8 @@ __device__ __forceinline__ void decode_fill(int r, int& ti, int& tj) {
   tj = i;                         // column tile
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool kF32>
+__global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
     trimul_sm103a_kernel(const __grid_constant__ CUtensorMap tmap_a,
                          const __grid_constant__ CUtensorMap tmap_b,
                          const __grid_constant__ CUtensorMap tmap_out,
@@ -178,6 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t drain_bar = bars + 8u * (2 * a.stages + 4);
   auto sfull_bar = [&](int s) { return bars + 8u * (2 * a.stages + 5 + s); };
   auto sempty_bar = [&](int s) { return bars + 8u * (2 * a.stages + 5 + kSchedDepth + s); };
+  // fp32 form: stage s split into hi / lo and ready for the MMA.
+  auto conv_bar = [&](int s) { return bars + 8u * (2 * a.stages + 5 + 2 * kSchedDepth + s); };
+  constexpr int kBlockThreads = kF32 ? kThreadsF32 : kThreads;
   auto sched_entry = [&](int s) { return base + a.off_misc + 16u + 4u * s; };
   const uint32_t tmem_slot = base + a.off_misc;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + a.off_misc + 4);
@@ -186,8 +206,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t mask_box = base + a.off_mask;
   auto q_chunk = [&](int s, int kc) { return base + s * a.stage_bytes + kc * kChunkBytes; };
   auto k_chunk = [&](int s, int kc) {
-    return base + s * a.stage_bytes + (a.kchunks + kc) * kChunkBytes;
+    return base + s * a.stage_bytes + (a.stage_chunks + kc) * kChunkBytes;
   };
+  // fp32 form: the lo parts of a stage's Q and K chunks follow its hi parts.
+  auto lo_chunk = [&](uint32_t hi) { return hi + 2u * kChunkBytes; };
 
   const Watchdog wd{a.wait_limit_ns, a.status, abort_flag};
 
@@ -203,15 +225,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain_bar, 1);
     for (int s = 0; s < kSchedDepth; ++s) {
       mbar_init(sfull_bar(s), 1);
-      mbar_init(sempty_bar(s), 1 + kEpiWarps);
+      mbar_init(sempty_bar(s), 1 + kEpiWarps + (kF32 ? kConvWarps : 0));
     }
+    if (kF32)
+      for (int s = 0; s < a.stages; ++s) mbar_init(conv_bar(s), kConvWarps);
     *abort_flag = 0;
     *epi_idle = 1;
     fence_barrier_init();
   }
   // The resident mask buffer that fill tiles are stored from.
   if (a.n_fill > 0 && a.tma_store) {
-    for (uint32_t w = threadIdx.x; w < kFillBytes / 4; w += kThreads)
+    for (uint32_t w = threadIdx.x; w < kFillBytes / 4; w += kBlockThreads)
       st_shared_b32(mask_box + 4u * w, a.mask_bits);
     fence_proxy_async_smem();
   }
@@ -233,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;  // per-stage: loads that may be in flight
       bool injected = false;
-      const uint32_t tx = static_cast<uint32_t>(a.kchunks) * 2u * kChunkBytes;
+      const uint32_t tx = static_cast<uint32_t>(a.stage_chunks) * 2u * kChunkBytes;
       // Work list: the computed tiles, (b, h)-major. Positions are taken from a
       // shared counter (kFetchAhead fetches in flight) when a fill pool absorbs
       // the imbalance that leaves, else dealt statically (c, c+G, ...) so that
@@ -269,26 +293,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         int bh, r, ti, tj;
         decode_position(static_cast<int>(cur), a.per_lower, bh, r);
         decode_computed(r, a.causal, a.Tt2, ti, tj);
-        if (!mbar_wait(empty_bar(stage), phase ^ 1u, wd, kSiteProducerEmpty)) break;
         const int outer = bh / a.nh_div, inner = bh - outer * a.nh_div;
-        mbar_arrive_expect_tx(full_bar(stage), tx);
-        if (a.inject && !injected) {
-          injected = true;  // withhold this CTA's first loads: its consumer's wait must run out
-          issued &= ~(1u << stage);
-        } else {
-          for (int kc = 0; kc < a.kchunks; ++kc) {
-            tma_load_4d(q_chunk(stage, kc), &tmap_a, full_bar(stage), kc * kChunkElems, inner,
-                        ti * kTile, outer);
-            tma_load_4d(k_chunk(stage, kc), &tmap_b, full_bar(stage), kc * kChunkElems,
-                        a.b_off + inner, tj * kTile, outer);
+        bool ok = true;
+        for (int ts = 0; ts < a.tile_stages; ++ts) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, wd, kSiteProducerEmpty)) {
+            ok = false;
+            break;
           }
-          issued |= 1u << stage;
-          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          mbar_arrive_expect_tx(full_bar(stage), tx);
+          if (a.inject && !injected) {
+            injected = true;  // withhold this CTA's first loads: its consumer's wait must run out
+            issued &= ~(1u << stage);
+          } else {
+            for (int kc = 0; kc < a.stage_chunks; ++kc) {
+              const int x = (ts * a.stage_chunks + kc) * a.chunk_elems;
+              tma_load_4d(q_chunk(stage, kc), &tmap_a, full_bar(stage), x, inner, ti * kTile,
+                          outer);
+              tma_load_4d(k_chunk(stage, kc), &tmap_b, full_bar(stage), x, a.b_off + inner,
+                          tj * kTile, outer);
+            }
+            issued |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          }
+          if (++stage == a.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
-        if (++stage == a.stages) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        if (!ok) break;
       }
       if (*abort_flag) {
         // Let every load still in flight land before shared memory goes away.
@@ -322,21 +354,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (cur == kEntryEnd) break;
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, wd, kSiteMmaTmemEmpty)) break;
         tc_fence_after_sync();
-        if (!mbar_wait(full_bar(stage), phase, wd, kSiteMmaFull)) break;
-        tc_fence_after_sync();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kTile);
-        for (int k = 0; k < a.ksteps; ++k) {
-          const uint32_t off = static_cast<uint32_t>(k & 3) * 32u;  // 16 bf16 = 32 B along K
-          const uint64_t ad = umma_desc_k_sw128(q_chunk(stage, k >> 2) + off);
-          const uint64_t bd = umma_desc_k_sw128(k_chunk(stage, k >> 2) + off);
-          umma_bf16(d, ad, bd, kIdesc, k > 0 ? 1u : 0u);
+        bool ok = true;
+        for (int ts = 0; ts < a.tile_stages; ++ts) {
+          if (!mbar_wait(kF32 ? conv_bar(stage) : full_bar(stage), phase, wd, kSiteMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          if constexpr (kF32) {
+            // One 32-element chunk: 4 steps of 8 along K, each hi.hi + hi.lo + lo.hi.
+            const uint32_t qh = q_chunk(stage, 0), kh = k_chunk(stage, 0);
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t off = static_cast<uint32_t>(k) * 32u;  // 8 tf32 = 32 B along K
+              const uint64_t qhi = umma_desc_k_sw128(qh + off), khi = umma_desc_k_sw128(kh + off);
+              umma_tf32(d, qhi, khi, kIdescTf32, (ts > 0 || k > 0) ? 1u : 0u);
+              umma_tf32(d, qhi, umma_desc_k_sw128(lo_chunk(kh) + off), kIdescTf32, 1u);
+              umma_tf32(d, umma_desc_k_sw128(lo_chunk(qh) + off), khi, kIdescTf32, 1u);
+            }
+          } else {
+            for (int k = 0; k < a.ksteps; ++k) {
+              const uint32_t off = static_cast<uint32_t>(k & 3) * 32u;  // 16 bf16 = 32 B along K
+              const uint64_t ad = umma_desc_k_sw128(q_chunk(stage, k >> 2) + off);
+              const uint64_t bd = umma_desc_k_sw128(k_chunk(stage, k >> 2) + off);
+              umma_bf16(d, ad, bd, kIdesc, k > 0 ? 1u : 0u);
+            }
+          }
+          umma_commit(empty_bar(stage));  // operands consumed -> slot free
+          if (++stage == a.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
-        umma_commit(empty_bar(stage));  // operands consumed -> slot free
-        umma_commit(tfull_bar(acc));    // accumulator ready -> epilogue
-        if (++stage == a.stages) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        if (!ok) break;
+        umma_commit(tfull_bar(acc));  // accumulator ready -> epilogue
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
@@ -346,6 +397,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(drain_bar);
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_test(drain_bar, 0) && globaltimer_ns() - t0 < a.wait_limit_ns) {
+      }
+    }
+  } else if (kF32 && warp >= kFirstConvWarp) {
+    // ---------------------------------------------------------- splitter --
+    // For every stage of every computed tile (the work ring tells how many):
+    // once its fp32 Q and K chunks have landed, rewrite each value x as
+    // hi = x with the low 13 mantissa bits cleared and store lo = x - hi beside
+    // it, then hand the stage to the MMA warp.
+    const uint32_t cw = warp - kFirstConvWarp;
+    int stage = 0, slot = 0;
+    uint32_t phase = 0, sphase = 0;
+    bool ok = true;
+    while (ok) {
+      int got = 1;
+      unsigned int cur = 0;
+      if (lane == 0) {
+        got = mbar_wait(sfull_bar(slot), sphase, wd, kSiteSched) ? 1 : 0;
+        if (got) {
+          cur = ld_shared_b32(sched_entry(slot));
+          mbar_arrive(sempty_bar(slot));
+        }
+      }
+      got = __shfl_sync(0xffffffffu, got, 0);
+      cur = __shfl_sync(0xffffffffu, cur, 0);
+      if (!got || cur == kEntryEnd) break;
+      if (++slot == kSchedDepth) {
+        slot = 0;
+        sphase ^= 1u;
+      }
+      for (int ts = 0; ts < a.tile_stages; ++ts) {
+        if (!mbar_wait_warp(full_bar(stage), phase, wd, kSiteMmaFull)) {
+          ok = false;
+          break;
+        }
+        // The stage's Q and K chunks are 2 x 16 KB, contiguous: 2048 16-byte words,
+        // 16 per lane of the 4 splitter warps.
+        const uint32_t hi0 = q_chunk(stage, 0);
+        for (uint32_t i = cw * 32u + lane; i < 2u * kChunkBytes / 16u; i += 32u * kConvWarps) {
+          const uint32_t addr = hi0 + 16u * i;
+          uint32_t x[4];
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
+                       : "r"(addr));
+          uint32_t h[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            h[e] = x[e] & 0xFFFFE000u;
+            lo[e] = __float_as_uint(__uint_as_float(x[e]) - __uint_as_float(h[e]));
+          }
+          st_shared_v4(addr, h[0], h[1], h[2], h[3]);
+          st_shared_v4(lo_chunk(addr), lo[0], lo[1], lo[2], lo[3]);
+        }
+        fence_proxy_async_smem();  // generic smem writes -> visible to tcgen05.mma
+        __syncwarp();
+        if (lane == 0) mbar_arrive(conv_bar(stage));
+        if (++stage == a.stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
     }
   } else if (warp == kFillWarp) {
@@ -544,7 +654,7 @@ int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& 
                   long long BH, int T, int T2, int D, int nh_div, int b_off, bool causal,
                   bool lower_only, float scale, uint32_t mask_bits, bool inject,
                   cudaStream_t stream, const DeviceInfo& dev, std::string& err,
-                  unsigned int* counters) {
+                  unsigned int* counters, bool f32 = false) {
   const std::string name(who);
   if (BH > (1LL << 30) || static_cast<long long>(T) > (1LL << 30) ||
       static_cast<long long>(T2) > (1LL << 30)) {
@@ -560,8 +670,13 @@ int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& 
   a.nh_div = nh_div;
   a.b_off = b_off;
   a.causal = causal ? 1u : 0u;
-  a.kchunks = (D + kChunkElems - 1) / kChunkElems;
+  // bf16: a stage holds all of a tile's 64-element chunks. fp32 (3xtf32): a
+  // stage holds one 32-element chunk of Q and K plus their lo parts.
+  a.chunk_elems = f32 ? kChunkElemsF32 : kChunkElems;
+  a.kchunks = (D + a.chunk_elems - 1) / a.chunk_elems;
   a.ksteps = (D + 15) / 16;
+  a.stage_chunks = f32 ? 1 : a.kchunks;
+  a.tile_stages = f32 ? a.kchunks : 1;
   const long long per_lower = causal ? static_cast<long long>(a.Tt) * (a.Tt + 1) / 2
                                      : static_cast<long long>(a.Tt) * a.Tt2;
   const long long per_fill =
@@ -588,7 +703,7 @@ int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& 
   // Shared memory: operand ring | staging boxes | mask buffer | barriers | misc.
   // Operand ring stages vs. staging depth: the most box pairs per epilogue warp
   // that still leave two ring stages, else one pair.
-  a.stage_bytes = static_cast<uint32_t>(a.kchunks) * 2u * kChunkBytes;
+  a.stage_bytes = f32 ? 4u * kChunkBytes : static_cast<uint32_t>(a.kchunks) * 2u * kChunkBytes;
   const int fixed = kFillBytes + 1024 /*bars+misc+ring*/ + 1024 /*align slack*/;
   int staging_bytes = 0;
   for (int groups = CSA_TRIMUL_MAX_STORE_GROUPS; groups >= 1; --groups) {
@@ -605,7 +720,7 @@ int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& 
   a.off_staging = static_cast<uint32_t>(a.stages) * a.stage_bytes;
   a.off_mask = a.off_staging + static_cast<uint32_t>(staging_bytes);
   a.off_bars = a.off_mask + kFillBytes;
-  a.off_misc = a.off_bars + 8u * static_cast<uint32_t>(2 * a.stages + 5 + 2 * kSchedDepth);
+  a.off_misc = a.off_bars + 8u * static_cast<uint32_t>(3 * a.stages + 5 + 2 * kSchedDepth);
   const size_t smem = a.off_misc + 16 + 4 * kSchedDepth + 1024;
 
   CUtensorMap map_out, map_fill;
@@ -649,8 +764,8 @@ int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& 
     }
     a.sched = sched_base[dev.device] + kSchedWords * (launch_seq.fetch_add(1) % kSchedSlots);
   }
-  cudaError_t e = cudaFuncSetAttribute(trimul_sm103a_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto* kernel = f32 ? trimul_sm103a_kernel<true> : trimul_sm103a_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) {
     err = name + ": cudaFuncSetAttribute: " + cudaGetErrorString(e);
@@ -658,7 +773,7 @@ int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& 
   }
   const long long grid = std::min<long long>(static_cast<long long>(a.n_lower) + a.n_fill,
                                             dev.sm_count);
-  trimul_sm103a_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(
+  kernel<<<static_cast<unsigned>(grid), f32 ? kThreadsF32 : kThreads, smem, stream>>>(
       map_a, map_b, map_out, map_fill, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
@@ -703,6 +818,40 @@ int trimul_launch(float* out, const void* qkv, int B, int T, int C, int NH, uint
   return launch_scores("trimul_forward", map_qkv, map_qkv, out, static_cast<long long>(B) * NH, T,
                        T, HS, NH, NH, true, (flags & CSA_TRIMUL_LOWER_ONLY) != 0, scale,
                        mask_bits, take_inject(), stream, dev, err, counters);
+}
+
+int trimul_f32_launch(float* out, const float* qkv, int B, int T, int C, int NH,
+                      uint32_t mask_bits, uint32_t flags, cudaStream_t stream, const DeviceInfo& dev,
+                      std::string& err) {
+  const int HS = C / NH;
+  if (HS % 4 != 0) {
+    err = "trimul_forward_f32: HS = C/NH must be a multiple of 4 (TMA row pitch of a head)";
+    return CSA_ERR_ALIGN;
+  }
+  if (HS > 256) {
+    err = "trimul_forward_f32: HS > 256 is not supported";
+    return CSA_ERR_UNSUPPORTED;
+  }
+  if (reinterpret_cast<uintptr_t>(qkv) % 16 != 0 || reinterpret_cast<uintptr_t>(out) % 4 != 0) {
+    err = "trimul_forward_f32: qkv must be 16-byte aligned and out 4-byte aligned";
+    return CSA_ERR_ALIGN;
+  }
+  // The packed fp32 tensor read in place: Q of head h at index h, K at NH + h.
+  CUtensorMap map_qkv;
+  {
+    const uint64_t dims[4] = {static_cast<uint64_t>(HS), static_cast<uint64_t>(3 * NH),
+                              static_cast<uint64_t>(T), static_cast<uint64_t>(B)};
+    const uint64_t strides[3] = {static_cast<uint64_t>(HS) * 4, static_cast<uint64_t>(C) * 12,
+                                 static_cast<uint64_t>(T) * C * 12};
+    const uint32_t box[4] = {kChunkElemsF32, 1, kTile, 1};
+    int rc = encode_tiled(&map_qkv, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, qkv, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B, err);
+    if (rc != CSA_OK) return rc;
+  }
+  const float scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(HS)));
+  return launch_scores("trimul_forward_f32", map_qkv, map_qkv, out, static_cast<long long>(B) * NH,
+                       T, T, HS, NH, NH, true, (flags & CSA_TRIMUL_LOWER_ONLY) != 0, scale,
+                       mask_bits, take_inject(), stream, dev, err, nullptr, true);
 }
 
 int bmm_nt_launch(float* Y, const void* X, const void* W, int batch, int T1, int T2, int D,

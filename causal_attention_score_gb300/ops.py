@@ -51,6 +51,18 @@ def trimul_forward(out: torch.Tensor, qkv: torch.Tensor, B: int, T: int, C: int,
     _lib.check(rc, "trimul_forward")
 
 
+def trimul_forward_f32(out: torch.Tensor, qkv: torch.Tensor, B: int, T: int, C: int, NH: int,
+                       mask="nan", lower_only: bool = False, stream=None) -> None:
+    """Causal scores into ``out`` (fp32, (B, NH, T, T)) from packed fp32 ``qkv``
+    ((B, T, 3, NH, HS), not rounded to bf16); see trimul_forward_f32 in include/csa.h."""
+    _need(qkv, "qkv", torch.float32, B * T * 3 * C)
+    _need(out, "out", torch.float32, B * NH * T * T)
+    flags = CSA_TRIMUL_LOWER_ONLY if lower_only else CSA_TRIMUL_FULL
+    rc = _lib.load().trimul_forward_f32(out.data_ptr(), qkv.data_ptr(), B, T, C, NH,
+                                        _mask_bits(mask), flags, _stream_ptr(stream))
+    _lib.check(rc, "trimul_forward_f32")
+
+
 def dense_xwt(Y: torch.Tensor, X: torch.Tensor, W: torch.Tensor, M: int, I: int, H: int,
               stream=None) -> None:
     """Y = X W^T into ``Y`` (fp32 [M, H]) from bf16 X [M, I] and W [H, I]."""

@@ -96,6 +96,32 @@ csa_status trimul_forward_ex(float* out, const void* qkv, int B, int T, int C, i
                              uint32_t mask_bits, uint32_t flags, void* stream);
 
 /*
+ * trimul_forward_f32 -- the causal score product over fp32 inputs, the
+ * referee's own input type ("llm.c dev/cuda/trimat_forward.cu": trimul_cpu
+ * takes const float* inp, and main fills it with fp32 random numbers), with no
+ * rounding of the inputs to bf16.
+ *
+ *   out        device, fp32, (B, NH, T, T) contiguous; every element written
+ *              (or only t2 <= t with CSA_TRIMUL_LOWER_ONLY).
+ *   qkv        device, fp32, (B, T, 3, NH, HS) contiguous, HS = C / NH; read only.
+ *   mask_bits, flags, stream   as trimul_forward_ex.
+ *
+ * Arithmetic: tcgen05 kind::tf32 with three products per input pair. Each
+ * input x is split exactly into hi (x with its 13 lowest mantissa bits
+ * cleared, a tf32 value) and lo = x - hi; each score accumulates
+ * hi_q.hi_k + hi_q.lo_k + lo_q.hi_k in fp32, leaving out lo_q.lo_k, so each
+ * product carries a relative error of a few units of 2^-20 on top of the fp32
+ * accumulation, and the result is multiplied by the fp32 value of 1/sqrt(HS).
+ *
+ * Requirements (else CSA_ERR_ALIGN / CSA_ERR_UNSUPPORTED): qkv 16-byte and out
+ * 4-byte aligned; HS % 4 == 0 (the TMA row pitch of a head is HS*4 bytes);
+ * HS <= 256. Any T >= 1. Errors as trimul_forward_ex; nothing is written on
+ * an argument error. The caller owns every buffer; nothing is allocated.
+ */
+csa_status trimul_forward_f32(float* out, const float* qkv, int B, int T, int C, int NH,
+                              uint32_t mask_bits, uint32_t flags, void* stream);
+
+/*
  * trimul_forward_noalloc -- trimul_forward_ex for callers that must not
  * allocate device memory. No passage of the pages has a counterpart: this
  * entry point exists for deployment, not for the method.
