@@ -33,9 +33,11 @@
 //    input x splits exactly into hi = x with its low 13 mantissa bits cleared
 //    (a tf32 value) and lo = x - hi (an fp32 value; its tf32 rounding costs
 //    2^-21 |x|), and each tile accumulates hi.hi + hi.lo + lo.hi (lo.lo is
-//    below 2^-20 |q.k|). A stage holds one 32-element chunk of the Q and K
-//    tiles; warps 11-14 split it in shared memory (hi in place, lo beside it)
-//    before the MMA warp reads it.
+//    below 2^-20 |q.k|). The tensor core reads only the top 19 bits of an fp32
+//    operand, so the loaded x serves as hi as it is (measured: bit-identical
+//    results to explicitly cleared operands). A stage holds one 32-element
+//    chunk of the Q and K tiles; warps 11-14 write its lo parts beside it
+//    before the MMA warp reads both.
 //  - warp 10: fill writer. It takes fill tiles from the launch-wide pool while
 //    the epilogue has nothing to store (start-up, a wait on the MMA, after the
 //    last lower tile) and writes each as 128 x 16 TMA stores of a resident
@@ -402,9 +404,9 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
   } else if (kF32 && warp >= kFirstConvWarp) {
     // ---------------------------------------------------------- splitter --
     // For every stage of every computed tile (the work ring tells how many):
-    // once its fp32 Q and K chunks have landed, rewrite each value x as
-    // hi = x with the low 13 mantissa bits cleared and store lo = x - hi beside
-    // it, then hand the stage to the MMA warp.
+    // once its fp32 Q and K chunks have landed, store lo = x - hi beside each
+    // value x (hi = x with the low 13 mantissa bits cleared, which is what the
+    // tensor core reads of x itself), then hand the stage to the MMA warp.
     const uint32_t cw = warp - kFirstConvWarp;
     int stage = 0, slot = 0;
     uint32_t phase = 0, sphase = 0;
@@ -432,22 +434,28 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
           break;
         }
         // The stage's Q and K chunks are 2 x 16 KB, contiguous: 2048 16-byte words,
-        // 16 per lane of the 4 splitter warps.
+        // 16 per lane of the 4 splitter warps, four loads in flight per lane.
         const uint32_t hi0 = q_chunk(stage, 0);
-        for (uint32_t i = cw * 32u + lane; i < 2u * kChunkBytes / 16u; i += 32u * kConvWarps) {
-          const uint32_t addr = hi0 + 16u * i;
-          uint32_t x[4];
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
-                       : "r"(addr));
-          uint32_t h[4], lo[4];
+        for (uint32_t i0 = cw * 32u + lane; i0 < 2u * kChunkBytes / 16u;
+             i0 += 4u * 32u * kConvWarps) {
+          uint32_t x[4][4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            h[e] = x[e] & 0xFFFFE000u;
-            lo[e] = __float_as_uint(__uint_as_float(x[e]) - __uint_as_float(h[e]));
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t addr = hi0 + 16u * (i0 + u * 32u * kConvWarps);
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(x[u][0]), "=r"(x[u][1]), "=r"(x[u][2]), "=r"(x[u][3])
+                         : "r"(addr));
           }
-          st_shared_v4(addr, h[0], h[1], h[2], h[3]);
-          st_shared_v4(lo_chunk(addr), lo[0], lo[1], lo[2], lo[3]);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint32_t l4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              l4[e] = __float_as_uint(__uint_as_float(x[u][e]) -
+                                      __uint_as_float(x[u][e] & 0xFFFFE000u));
+            st_shared_v4(lo_chunk(hi0 + 16u * (i0 + u * 32u * kConvWarps)), l4[0], l4[1], l4[2],
+                         l4[3]);
+          }
         }
         fence_proxy_async_smem();  // generic smem writes -> visible to tcgen05.mma
         __syncwarp();

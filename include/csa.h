@@ -108,7 +108,8 @@ csa_status trimul_forward_ex(float* out, const void* qkv, int B, int T, int C, i
  *
  * Arithmetic: tcgen05 kind::tf32 with three products per input pair. Each
  * input x is split exactly into hi (x with its 13 lowest mantissa bits
- * cleared, a tf32 value) and lo = x - hi; each score accumulates
+ * cleared, a tf32 value: what the tensor core reads of x) and lo = x - hi;
+ * each score accumulates
  * hi_q.hi_k + hi_q.lo_k + lo_q.hi_k in fp32, leaving out lo_q.lo_k, so each
  * product carries a relative error of a few units of 2^-20 on top of the fp32
  * accumulation, and the result is multiplied by the fp32 value of 1/sqrt(HS).
