@@ -98,9 +98,95 @@ int current_device(DeviceInfo& info, std::string& err) {
   return CSA_OK;
 }
 
+namespace {
+
+// Tensor maps are pure functions of their encoding parameters, so a map built
+// once serves every later call with the same parameters (a buffer freed and
+// reallocated at the same address with the same shape gets the same map).
+// Direct-mapped cache of 256 entries, indexed by a hash of the parameters.
+struct MapKey {
+  uint64_t addr;
+  uint64_t dims[5];
+  uint64_t strides[4];
+  uint32_t box[5];
+  uint32_t dtype, rank, swizzle, pad;
+};
+
+struct MapEntry {
+  bool valid = false;
+  MapKey key{};
+  CUtensorMap map{};
+};
+
+constexpr int kMapCacheSize = 256;
+std::mutex g_map_mu;
+MapEntry g_map_cache[kMapCacheSize];
+
+uint64_t hash_key(const MapKey& k) {
+  // FNV-1a over the key bytes.
+  const unsigned char* p = reinterpret_cast<const unsigned char*>(&k);
+  uint64_t h = 1469598103934665603ull;
+  for (size_t i = 0; i < sizeof k; ++i) h = (h ^ p[i]) * 1099511628211ull;
+  return h;
+}
+
+std::mutex g_smem_mu;
+struct SmemSetting {
+  const void* fn;
+  int device;
+  int bytes;
+};
+SmemSetting g_smem_set[64];
+int g_smem_count = 0;
+
+}  // namespace
+
+int set_max_dynamic_smem(const void* kernel, int bytes, int device, std::string& err) {
+  std::lock_guard<std::mutex> lock(g_smem_mu);
+  for (int i = 0; i < g_smem_count; ++i) {
+    SmemSetting& e = g_smem_set[i];
+    if (e.fn == kernel && e.device == device) {
+      if (e.bytes >= bytes) return CSA_OK;
+      cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+      if (r != cudaSuccess) {
+        err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(r);
+        return CSA_ERR_LAUNCH;
+      }
+      e.bytes = bytes;
+      return CSA_OK;
+    }
+  }
+  cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (r != cudaSuccess) {
+    err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(r);
+    return CSA_ERR_LAUNCH;
+  }
+  if (g_smem_count < 64) g_smem_set[g_smem_count++] = SmemSetting{kernel, device, bytes};
+  return CSA_OK;
+}
+
 int encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, const void* addr,
                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
                  CUtensorMapSwizzle swizzle, std::string& err) {
+  MapKey key{};
+  key.addr = reinterpret_cast<uint64_t>(addr);
+  key.dtype = static_cast<uint32_t>(dtype);
+  key.rank = rank;
+  key.swizzle = static_cast<uint32_t>(swizzle);
+  for (uint32_t i = 0; i < rank && i < 5; ++i) {
+    key.dims[i] = dims[i];
+    key.box[i] = box[i];
+    if (i + 1 < rank) key.strides[i] = strides_bytes[i];
+  }
+  const int slot = static_cast<int>(hash_key(key) % kMapCacheSize);
+  {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    const MapEntry& e = g_map_cache[slot];
+    if (e.valid && std::memcmp(&e.key, &key, sizeof key) == 0) {
+      *map = e.map;
+      return CSA_OK;
+    }
+  }
   cuuint64_t d[5], s[4];
   cuuint32_t b[5], es[5];
   for (uint32_t i = 0; i < rank; ++i) {
@@ -115,6 +201,13 @@ int encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, con
   if (r != CUDA_SUCCESS) {
     err = "cuTensorMapEncodeTiled failed (code " + std::to_string(static_cast<int>(r)) + ")";
     return CSA_ERR_ALIGN;
+  }
+  {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    MapEntry& e = g_map_cache[slot];
+    e.valid = true;
+    e.key = key;
+    e.map = *map;
   }
   return CSA_OK;
 }

@@ -23,10 +23,15 @@ struct DeviceInfo {
 // Fills `info` for the current device. Returns CSA_OK, CSA_ERR_CUDA or CSA_ERR_ARCH.
 int current_device(DeviceInfo& info, std::string& err);
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link),
+// with a cache of maps keyed by every encoding parameter.
 int encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, const void* addr,
                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
                  CUtensorMapSwizzle swizzle, std::string& err);
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per kernel, device and
+// larger size; later calls needing no more are free.
+int set_max_dynamic_smem(const void* kernel, int bytes, int device, std::string& err);
 
 uint64_t wait_limit_ns();
 bool take_inject();

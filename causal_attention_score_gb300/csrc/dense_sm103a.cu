@@ -480,13 +480,15 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
     if (rc != CSA_OK) return rc;
   }
 
-  cudaError_t e = cudaFuncSetAttribute(dense_sm103a_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) {
-    err = std::string("dense_xwt: cudaFuncSetAttribute: ") + cudaGetErrorString(e);
-    return CSA_ERR_LAUNCH;
+  {
+    int rc = set_max_dynamic_smem(reinterpret_cast<const void*>(dense_sm103a_kernel),
+                                  static_cast<int>(smem), dev.device, err);
+    if (rc != CSA_OK) {
+      err = "dense_xwt: " + err;
+      return rc;
+    }
   }
+  cudaError_t e;
   const long long grid = std::min<long long>(a.num_tiles, dev.sm_count);
   dense_sm103a_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(map_x, map_w,
                                                                                map_y, a);

@@ -742,13 +742,15 @@ int softmax_launch(float* out, const void* qkv, int B, int T, int C, int NH, cud
     }
     a.sched = sched_base[dev.device] + kSchedWords * (launch_seq.fetch_add(1) % kSlots);
   }
-  cudaError_t e = cudaFuncSetAttribute(softmax_sm103a_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) {
-    err = std::string("causal_softmax_forward: cudaFuncSetAttribute: ") + cudaGetErrorString(e);
-    return CSA_ERR_LAUNCH;
+  {
+    int rc = set_max_dynamic_smem(reinterpret_cast<const void*>(softmax_sm103a_kernel),
+                                  static_cast<int>(smem), dev.device, err);
+    if (rc != CSA_OK) {
+      err = "causal_softmax_forward: " + err;
+      return rc;
+    }
   }
+  cudaError_t e;
   const long long grid = std::min<long long>(a.n_units, dev.sm_count);
   softmax_sm103a_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(map_qkv, map_out,
                                                                                  map_zero, a);

@@ -773,12 +773,15 @@ int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& 
     a.sched = sched_base[dev.device] + kSchedWords * (launch_seq.fetch_add(1) % kSchedSlots);
   }
   auto* kernel = f32 ? trimul_sm103a_kernel<true> : trimul_sm103a_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) {
-    err = name + ": cudaFuncSetAttribute: " + cudaGetErrorString(e);
-    return CSA_ERR_LAUNCH;
+  {
+    int rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kernel), static_cast<int>(smem),
+                                  dev.device, err);
+    if (rc != CSA_OK) {
+      err = name + ": " + err;
+      return rc;
+    }
   }
+  cudaError_t e;
   const long long grid = std::min<long long>(static_cast<long long>(a.n_lower) + a.n_fill,
                                             dev.sm_count);
   kernel<<<static_cast<unsigned>(grid), f32 ? kThreadsF32 : kThreads, smem, stream>>>(
