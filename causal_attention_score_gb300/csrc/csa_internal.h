@@ -33,7 +33,26 @@ int encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, con
 // larger size; later calls needing no more are free.
 int set_max_dynamic_smem(const void* kernel, int bytes, int device, std::string& err);
 
-uint64_t wait_limit_ns();
+// Launches `kernel` with programmatic stream serialization: it may start while
+// the previous kernel in the stream finishes, and waits for it (griddepcontrol)
+// before it touches global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_programmatic(void (*kernel)(KArgs...), unsigned grid, unsigned block,
+                                size_t smem, cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
+uint64_t wait_limit_ns();uint64_t wait_limit_ns();
 bool take_inject();
 
 // Kernel launchers; each validates what is specific to its kernel.

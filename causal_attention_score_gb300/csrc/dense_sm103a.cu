@@ -170,6 +170,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = ld_shared_b32(tmem_slot);
 
+  // Nothing global has been touched yet: the kernel ahead in the stream may still
+  // be running (programmatic launch), so wait for it here.
+  grid_dependency_wait();
+
   if (warp < kLoaderWarps) {
     // ------------------------------------------------------------ Fetch --
     if (a.tma_load) {
@@ -490,9 +494,9 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
   }
   cudaError_t e;
   const long long grid = std::min<long long>(a.num_tiles, dev.sm_count);
-  dense_sm103a_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(map_x, map_w,
-                                                                               map_y, a);
-  e = cudaGetLastError();
+  e = launch_programmatic(dense_sm103a_kernel, static_cast<unsigned>(grid), kThreads, smem, stream,
+                          map_x, map_w, map_y, a);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     err = std::string("dense_xwt: launch: ") + cudaGetErrorString(e);
     return CSA_ERR_LAUNCH;

@@ -46,6 +46,15 @@ struct Watchdog {
   volatile int* abort_flag;  // shared memory, per CTA
 };
 
+// ------------------------------------------------- programmatic launches --
+// With a programmatic launch the kernel may start while the one before it in
+// the stream is still running; it must not touch global memory before the wait
+// (which returns once that kernel has completed and its writes are visible).
+// Without one, the wait returns at once.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier --
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

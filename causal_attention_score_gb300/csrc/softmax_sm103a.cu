@@ -169,6 +169,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = ld_shared_b32(tmem_slot);
 
+  // Nothing global has been touched yet: the kernel ahead in the stream may still
+  // be running (programmatic launch), so wait for it here.
+  grid_dependency_wait();
+
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0) {
@@ -752,9 +756,9 @@ int softmax_launch(float* out, const void* qkv, int B, int T, int C, int NH, cud
   }
   cudaError_t e;
   const long long grid = std::min<long long>(a.n_units, dev.sm_count);
-  softmax_sm103a_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(map_qkv, map_out,
-                                                                                 map_zero, a);
-  e = cudaGetLastError();
+  e = launch_programmatic(softmax_sm103a_kernel, static_cast<unsigned>(grid), kThreads, smem,
+                          stream, map_qkv, map_out, map_zero, a);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     err = std::string("causal_softmax_forward: launch: ") + cudaGetErrorString(e);
     return CSA_ERR_LAUNCH;

@@ -250,6 +250,10 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = ld_shared_b32(tmem_slot);
 
+  // Nothing global has been touched yet: the kernel ahead in the stream may still
+  // be running (programmatic launch), so wait for it here.
+  grid_dependency_wait();
+
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0) {
@@ -784,9 +788,9 @@ int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& 
   cudaError_t e;
   const long long grid = std::min<long long>(static_cast<long long>(a.n_lower) + a.n_fill,
                                             dev.sm_count);
-  kernel<<<static_cast<unsigned>(grid), f32 ? kThreadsF32 : kThreads, smem, stream>>>(
-      map_a, map_b, map_out, map_fill, a);
-  e = cudaGetLastError();
+  e = launch_programmatic(kernel, static_cast<unsigned>(grid), f32 ? kThreadsF32 : kThreads, smem,
+                          stream, map_a, map_b, map_out, map_fill, a);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     err = name + ": launch: " + cudaGetErrorString(e);
     return CSA_ERR_LAUNCH;
