@@ -58,6 +58,7 @@ struct DenseArgs {
   long long num_tiles;
   uint32_t tma_load, tma_store, vec2;
   int load_depth;  // cp.async stages in flight per loader warp (2..4, <= stages)
+  int inject;      // withhold each CTA's first operand hand-off (watchdog tests)
   uint32_t idesc;
   const uint16_t* X;
   const uint16_t* W;
@@ -195,10 +196,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             mbar_arrive_expect_tx(full_bar(stage), tx);
-            tma_load_2d(a_tile(stage), &tmap_x, full_bar(stage), kb * kBK, mb * kBM);
-            tma_load_2d(b_tile(stage), &tmap_w, full_bar(stage), kb * kBK, nb * a.BN);
-            issued |= 1u << stage;
-            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+            if (a.inject && tile == blockIdx.x && kb == 0) {
+              issued &= ~(1u << stage);  // withheld: the MMA warp's wait must run out
+            } else {
+              tma_load_2d(a_tile(stage), &tmap_x, full_bar(stage), kb * kBK, mb * kBM);
+              tma_load_2d(b_tile(stage), &tmap_w, full_bar(stage), kb * kBK, nb * a.BN);
+              issued |= 1u << stage;
+              issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+            }
             if (++stage == a.stages) {
               stage = 0;
               phase ^= 1u;
@@ -221,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the MMA warp (proxy fence + arrive) once this warp's copies into it have
       // completed, while later stages are still in flight.
       const int depth = a.load_depth;
-      int stage = 0, oldest = 0, pending = 0;
+      int stage = 0, oldest = 0, pending = 0, arrivals = 0;
       uint32_t phase = 0;
       bool aborted = false;
       for (long long tile = blockIdx.x; tile < a.num_tiles && !aborted; tile += gridDim.x) {
@@ -242,7 +247,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             else cp_async_wait<1>();
             fence_proxy_async_smem();  // completed generic-proxy writes -> tcgen05.mma
             __syncwarp();
-            if (lane == 0) mbar_arrive(full_bar(oldest));
+            // (watchdog tests: the first stage is never handed over)
+            if (lane == 0 && !(a.inject && arrivals == 0)) mbar_arrive(full_bar(oldest));
+            ++arrivals;
             if (++oldest == a.stages) oldest = 0;
             --pending;
           }
@@ -257,7 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (!aborted) {
         for (; pending > 0; --pending) {
-          if (lane == 0) mbar_arrive(full_bar(oldest));
+          if (lane == 0 && !(a.inject && arrivals == 0)) mbar_arrive(full_bar(oldest));
+          ++arrivals;
           if (++oldest == a.stages) oldest = 0;
         }
       }
@@ -278,7 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           load_block<false>(a.W, a.H, nb * a.BN, a.BN, a.I, k, b_tile(stage), warp, lane);
           fence_proxy_async_smem();  // generic smem writes -> visible to tcgen05.mma
           __syncwarp();
-          if (lane == 0) mbar_arrive(full_bar(stage));
+          // (watchdog tests: the first stage is never handed over)
+          if (lane == 0 && !(a.inject && tile == blockIdx.x && kb == 0)) mbar_arrive(full_bar(stage));
           if (++stage == a.stages) {
             stage = 0;
             phase ^= 1u;
@@ -442,6 +451,7 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
   a.Y = Y;
   a.status = dev.status_word;
   a.wait_limit_ns = wait_limit_ns();
+  a.inject = take_inject() ? 1 : 0;
   a.tmem_cols = static_cast<uint32_t>(2 * a.BN);
 
   a.stage_bytes = static_cast<uint32_t>(kBM + a.BN) * 128u;

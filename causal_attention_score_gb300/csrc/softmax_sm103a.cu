@@ -86,6 +86,7 @@ struct SoftmaxArgs {
   int* status;
   unsigned long long wait_limit_ns;
   unsigned int* sched;
+  int inject;  // withhold each CTA's first Q load (watchdog tests)
   uint32_t q_bytes, k_bytes;
   uint32_t off_k, off_staging, off_zero, off_stats, off_bars, off_misc;
 };
@@ -196,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       unsigned int p0 = atomicAdd(a.sched, 1u), p1 = atomicAdd(a.sched, 1u);
       prefetch_unit(p1);
-      bool ok = true;
+      bool ok = true, injected = false;
       while (ok) {
         const unsigned int cur = p0;
         const bool done = cur >= static_cast<unsigned int>(a.n_units);
@@ -218,11 +219,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = bh / a.NH, h = bh - b * a.NH;
         if (!mbar_wait(qempty_bar(qb), qphase ^ 1u, wd, kSiteProducerEmpty)) break;
         mbar_arrive_expect_tx(qfull_bar(qb), qtx);
-        for (int kc = 0; kc < a.kchunks; ++kc)
-          tma_load_4d_hint(q_chunk(qb, kc), &tmap_qkv, qfull_bar(qb), kc * kChunkElems, h,
-                           ti * kTile, b, once);
-        qissued |= 1u << qb;
-        qparity = (qparity & ~(1u << qb)) | (qphase << qb);
+        if (a.inject && !injected) {
+          injected = true;  // withhold this CTA's first Q tile: the MMA warp's wait must run out
+          qissued &= ~(1u << qb);
+        } else {
+          for (int kc = 0; kc < a.kchunks; ++kc)
+            tma_load_4d_hint(q_chunk(qb, kc), &tmap_qkv, qfull_bar(qb), kc * kChunkElems, h,
+                             ti * kTile, b, once);
+          qissued |= 1u << qb;
+          qparity = (qparity & ~(1u << qb)) | (qphase << qb);
+        }
         if (++qb == 2) {
           qb = 0;
           qphase ^= 1u;
@@ -671,6 +677,7 @@ int softmax_launch(float* out, const void* qkv, int B, int T, int C, int NH, cud
   a.out = out;
   a.status = dev.status_word;
   a.wait_limit_ns = wait_limit_ns();
+  a.inject = take_inject() ? 1 : 0;
 
   // Shared memory: Q (2 buffers) | K ring | staging | zero box | stats | barriers | misc.
   a.q_bytes = static_cast<uint32_t>(a.kchunks) * kChunkBytes;

@@ -223,10 +223,12 @@ const char* csa_version(void);
  *
  * csa_set_wait_limit_ns -- upper bound, in nanoseconds of %globaltimer, on
  *   every spin-wait inside the kernels (default 2e9 = 2 s; 0 restores it).
- * csa_debug_inject -- when nonzero, the next trimul_forward_ex launch withholds
- *   the first operand load of every CTA that gets a lower tile, so the MMA
- *   warp's bounded wait runs out; the kernel records CSA_ERR_TIMEOUT and
- *   returns with its output incomplete. Consumed by that launch.
+ * csa_debug_inject -- when nonzero, the next kernel launch (any entry point)
+ *   withholds one hand-off in every CTA: the first operand load (score
+ *   products, the softmax's first Q tile, the dense layer's TMA form) or the
+ *   first stage arrival (the dense layer's loader-warp forms), so a bounded wait
+ *   downstream runs out; the kernel records CSA_ERR_TIMEOUT and returns with its
+ *   output incomplete. Consumed by that launch.
  */
 void csa_set_wait_limit_ns(uint64_t ns);
 void csa_debug_inject(int enable);

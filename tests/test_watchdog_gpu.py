@@ -31,3 +31,69 @@ def test_withheld_load_times_out_and_recovers(oracle_lib):
     ref = oracle_lib.trimul(synth.bf16_bits(qkv.cpu()).reshape(-1), shape.B, shape.T, shape.C,
                             shape.NH, 0)
     check_trimul_full(f32_bits(out), out.cpu().numpy(), ref, NAN_BITS, "after timeout")
+
+
+def _timeout_then_recover(run, check):
+    """run() once with the first hand-off withheld: CSA_ERR_TIMEOUT, read-and-clear;
+    then run() again normally and check() its result."""
+    assert csa.get_status() == 0
+    csa.set_wait_limit_ns(20_000_000)  # 20 ms
+    try:
+        csa.debug_inject(True)
+        run()
+        assert csa.get_status() == csa.CSA_ERR_TIMEOUT
+        assert csa.get_status() == 0
+    finally:
+        csa.set_wait_limit_ns(0)
+        csa.debug_inject(False)
+    run()
+    assert csa.get_status() == 0
+    check()
+
+
+def test_withheld_load_fp32_scores(oracle_lib):
+    shape = synth.TrimulShape(B=1, T=200, C=128, NH=2)
+    qkv = synth.trimul_input_f32(shape, seed=4)
+    q = qkv.cuda()
+    out = torch.empty(shape.out_shape, dtype=torch.float32, device="cuda")
+
+    def check():
+        ref = oracle_lib.trimul_f32(qkv.numpy().reshape(-1), shape.B, shape.T, shape.C,
+                                    shape.NH, 0)
+        check_trimul_full(f32_bits(out), out.cpu().numpy(), ref, NAN_BITS, "fp32 after timeout")
+
+    _timeout_then_recover(lambda: csa.trimul_forward_f32(out, q, shape.B, shape.T, shape.C,
+                                                         shape.NH), check)
+
+
+def test_withheld_load_softmax(oracle_lib):
+    shape = synth.TrimulShape(B=1, T=300, C=128, NH=2)
+    qkv = synth.trimul_input(shape, seed=5)
+    q = qkv.cuda()
+    att = torch.empty(shape.out_shape, dtype=torch.float32, device="cuda")
+
+    def check():
+        from gpu_util import assert_close
+        ref = oracle_lib.causal_softmax(synth.bf16_bits(qkv).reshape(-1), shape.B, shape.T,
+                                        shape.C, shape.NH)
+        assert_close(att.cpu().numpy(), ref, "softmax after timeout")
+
+    _timeout_then_recover(lambda: csa.causal_softmax_forward(att, q, shape.B, shape.T, shape.C,
+                                                             shape.NH), check)
+
+
+@pytest.mark.parametrize("M,I,H", [(960, 770, 768),   # loader warps, 4-byte cp.async
+                                   (300, 768, 512),   # TMA fetch
+                                   (130, 771, 200)])  # loader warps, 2-byte loads
+def test_withheld_hand_off_dense(oracle_lib, M, I, H):
+    X, W = synth.dense_input(synth.DenseShape(M=M, I=I, H=H), seed=6)
+    Xd, Wd = X.cuda(), W.cuda()
+    Y = torch.empty((M, H), dtype=torch.float32, device="cuda")
+
+    def check():
+        from gpu_util import assert_close
+        ref = oracle_lib.dense(synth.bf16_bits(X).reshape(-1), synth.bf16_bits(W).reshape(-1),
+                               M, I, H)
+        assert_close(Y.cpu().numpy(), ref, f"dense {M}x{I}x{H} after timeout")
+
+    _timeout_then_recover(lambda: csa.dense_xwt(Y, Xd, Wd, M, I, H), check)
