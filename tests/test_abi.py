@@ -96,3 +96,53 @@ def test_binding_refuses_cpu_tensors(lib):
 ])
 def test_noalloc_argument_errors(lib, args, code):
     assert lib.trimul_forward_noalloc(*args) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    ((None, 16, 1, 1, 8, 1, 0, 0, None), _lib.CSA_ERR_NULL),
+    ((16, None, 1, 1, 8, 1, 0, 0, None), _lib.CSA_ERR_NULL),
+    ((16, 16, 0, 1, 8, 1, 0, 0, None), _lib.CSA_ERR_SHAPE),
+    ((16, 16, 1, 1, 10, 3, 0, 0, None), _lib.CSA_ERR_SHAPE),      # C % NH != 0
+    ((16, 16, 1, 1, 6, 1, 0, 0, None), _lib.CSA_ERR_ALIGN),       # HS = 6 (fp32 needs HS % 4)
+    ((16, 16, 1, 1, 260, 1, 0, 0, None), _lib.CSA_ERR_UNSUPPORTED),  # HS = 260
+    ((16, 8, 1, 1, 64, 1, 0, 0, None), _lib.CSA_ERR_ALIGN),       # qkv not 16-byte aligned
+    ((18, 16, 1, 1, 64, 1, 0, 0, None), _lib.CSA_ERR_ALIGN),      # out not 4-byte aligned
+    ((16, 16, 1, 1, 64, 1, 0, 2, None), _lib.CSA_ERR_UNSUPPORTED),  # unknown flag
+])
+def test_trimul_f32_argument_errors(lib, args, code):
+    assert lib.trimul_forward_f32(*args) == code
+    assert lib.csa_last_error()
+
+
+@pytest.mark.parametrize("args,code", [
+    ((None, 16, 1, 1, 8, 1, None), _lib.CSA_ERR_NULL),
+    ((16, None, 1, 1, 8, 1, None), _lib.CSA_ERR_NULL),
+    ((16, 16, 1, 0, 8, 1, None), _lib.CSA_ERR_SHAPE),
+    ((16, 16, 1, 1, 10, 3, None), _lib.CSA_ERR_SHAPE),
+    ((16, 16, 1, 1, 12, 1, None), _lib.CSA_ERR_ALIGN),             # HS = 12
+    ((16, 16, 1, 1, 256, 1, None), _lib.CSA_ERR_UNSUPPORTED),      # HS = 256 (softmax: <= 128)
+    ((16, 8, 1, 1, 64, 1, None), _lib.CSA_ERR_ALIGN),
+])
+def test_softmax_argument_errors(lib, args, code):
+    assert lib.causal_softmax_forward(*args) == code
+    assert lib.csa_last_error()
+
+
+@pytest.mark.parametrize("args,code", [
+    ((None, 16, 16, 1, 1, 1, 8, None), _lib.CSA_ERR_NULL),
+    ((16, 16, 16, 0, 1, 1, 8, None), _lib.CSA_ERR_SHAPE),
+    ((16, 16, 16, 1, 1, 1, 12, None), _lib.CSA_ERR_ALIGN),         # D = 12
+    ((16, 16, 16, 1, 1, 1, 264, None), _lib.CSA_ERR_UNSUPPORTED),  # D = 264
+    ((16, 8, 16, 1, 1, 1, 64, None), _lib.CSA_ERR_ALIGN),          # X not 16-byte aligned
+])
+def test_bmm_nt_argument_errors(lib, args, code):
+    assert lib.batch_matmul_nt(*args) == code
+
+
+def test_no_device_for_the_other_entry_points(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    assert lib.trimul_forward_f32(1024, 1024, 1, 64, 128, 2, 0, 0, None) == _lib.CSA_ERR_CUDA
+    assert lib.causal_softmax_forward(1024, 1024, 1, 64, 128, 2, None) == _lib.CSA_ERR_CUDA
+    assert lib.batch_matmul_nt(1024, 1024, 1024, 2, 8, 8, 64, None) == _lib.CSA_ERR_CUDA
