@@ -716,7 +716,9 @@ int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& 
   // Operand ring stages vs. staging depth: the most box pairs per epilogue warp
   // that still leave two ring stages, else one pair.
   a.stage_bytes = f32 ? 4u * kChunkBytes : static_cast<uint32_t>(a.kchunks) * 2u * kChunkBytes;
-  const int fixed = kFillBytes + 1024 /*bars+misc+ring*/ + 1024 /*align slack*/;
+  // The mask buffer only exists when there are fill tiles (full causal mode).
+  const int fill_bytes = a.n_fill > 0 ? kFillBytes : 0;
+  const int fixed = fill_bytes + 1024 /*bars+misc+ring*/ + 1024 /*align slack*/;
   int staging_bytes = 0;
   for (int groups = CSA_TRIMUL_MAX_STORE_GROUPS; groups >= 1; --groups) {
     staging_bytes = kEpiWarps * groups * 2 * kBoxBytes;
@@ -731,7 +733,7 @@ int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& 
   }
   a.off_staging = static_cast<uint32_t>(a.stages) * a.stage_bytes;
   a.off_mask = a.off_staging + static_cast<uint32_t>(staging_bytes);
-  a.off_bars = a.off_mask + kFillBytes;
+  a.off_bars = a.off_mask + static_cast<uint32_t>(fill_bytes);
   a.off_misc = a.off_bars + 8u * static_cast<uint32_t>(3 * a.stages + 5 + 2 * kSchedDepth);
   const size_t smem = a.off_misc + 16 + 4 * kSchedDepth + 1024;
 
