@@ -52,7 +52,9 @@ cudaError_t launch_programmatic(void (*kernel)(KArgs...), unsigned grid, unsigne
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
-uint64_t wait_limit_ns();uint64_t wait_limit_ns();
+// Bound (ns of %globaltimer) on every mbarrier/flag wait in the kernels.
+uint64_t wait_limit_ns();
+// True once after csa_debug_inject armed it: the next launch withholds one arrival.
 bool take_inject();
 
 // Kernel launchers; each validates what is specific to its kernel.
