@@ -31,6 +31,7 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 std::atomic<uint64_t> g_wait_limit_ns{0};
 std::atomic<int> g_inject{0};
+std::atomic<int> g_dense_fetch{CSA_DENSE_FETCH_AUTO};
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 
 int set_error(int code, const std::string& msg) {
@@ -218,6 +219,7 @@ uint64_t wait_limit_ns() {
 }
 
 bool take_inject() { return g_inject.exchange(0) != 0; }
+int dense_fetch_mode() { return g_dense_fetch.load(); }
 
 }  // namespace csa
 
@@ -414,5 +416,12 @@ const char* csa_version(void) { return "0.1.0 sm_103a"; }
 void csa_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns); }
 
 void csa_debug_inject(int enable) { g_inject.store(enable ? 1 : 0); }
+
+csa_status csa_set_dense_fetch(int mode) {
+  if (mode != CSA_DENSE_FETCH_AUTO && mode != CSA_DENSE_FETCH_LOADERS)
+    return set_error(CSA_ERR_SHAPE, "csa_set_dense_fetch: unknown mode " + std::to_string(mode));
+  g_dense_fetch.store(mode);
+  return CSA_OK;
+}
 
 }  // extern "C"

@@ -56,6 +56,8 @@ cudaError_t launch_programmatic(void (*kernel)(KArgs...), unsigned grid, unsigne
 uint64_t wait_limit_ns();
 // True once after csa_debug_inject armed it: the next launch withholds one arrival.
 bool take_inject();
+// The dense layer's fetch mode set by csa_set_dense_fetch (CSA_DENSE_FETCH_*).
+int dense_fetch_mode();
 
 // Kernel launchers; each validates what is specific to its kernel.
 // `counters`: work-list counter pair to use instead of the library's per-launch

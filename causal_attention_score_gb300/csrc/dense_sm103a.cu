@@ -13,10 +13,16 @@
 //  - Fetch, two forms:
 //      * TMA (I*2 % 16 == 0, 16-byte aligned X and W): warp 0 issues 2-D tiled
 //        loads; rows >= M / H and columns >= I are zero-filled by the TMA unit.
-//      * loader warps (any other I, e.g. I = 770 whose 1540-byte rows no
-//        tensor map can describe): warps 0-3 read 4-byte (or 2-byte) pairs
-//        with plain loads, substitute zeros out of range, and write them into
-//        the same 128-byte-swizzled K-major layout the TMA would produce.
+//        Rows that no tensor map can describe (e.g. I = 770: 1540-byte rows)
+//        are first copied by realign_rows_kernel into a scratch copy whose
+//        rows start on 16-byte boundaries (pitch I rounded up to 8 elements);
+//        the tiles are then fetched from that copy by TMA, with the same zero
+//        fill at the edges. The copy only moves rows: no padding to tile
+//        multiples is materialised.
+//      * loader warps (rows no tensor map can describe, with no scratch copy):
+//        warps 0-3 read 4-byte (or 2-byte) pairs with plain loads, substitute
+//        zeros out of range, and write them into the same 128-byte-swizzled
+//        K-major layout the TMA would produce.
 //  - Compute: warp 4 issues tcgen05.mma M=128 N=BN K=16 into one of two TMEM
 //    accumulators; no bounds logic at all.
 //  - Writeback: warps 5-8 read TMEM 32 columns at a time and store 32 x 32
@@ -28,6 +34,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "csa_internal.h"
@@ -405,6 +412,95 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Rows of X [M, I], then of W [H, I], copied into rows of pitch P (I rounded
+// up to a multiple of 8 elements) so that each copied row starts on a 16-byte
+// boundary. Columns I..P-1 of a copied row are written as zeros (tensor maps
+// with extent I never read them). One warp per row, one 16-byte destination
+// chunk per lane and step, four steps' loads issued before their stores.
+// `pairs`: the source rows are 4-byte aligned (I even, X and W 4-byte
+// aligned) and are read as bf16 pairs, else one element at a time.
+constexpr int kRealignThreads = 256;
+
+__global__ void __launch_bounds__(kRealignThreads)
+    realign_rows_kernel(const uint16_t* __restrict__ X, const uint16_t* __restrict__ W,
+                        uint16_t* __restrict__ Xp, uint16_t* __restrict__ Wp, int M, int H, int I,
+                        int P, int pairs) {
+  // X and W may be written by the kernel ahead in the stream (programmatic launch).
+  grid_dependency_wait();
+  const long long rows = static_cast<long long>(M) + H;
+  const int lane = static_cast<int>(threadIdx.x & 31u);
+  const long long warps_per_grid = static_cast<long long>(gridDim.x) * (kRealignThreads / 32);
+  const int chunks = P / 8;
+  for (long long r = static_cast<long long>(blockIdx.x) * (kRealignThreads / 32) +
+                     (threadIdx.x >> 5);
+       r < rows; r += warps_per_grid) {
+    const bool is_x = r < M;
+    const uint16_t* src = is_x ? X + r * I : W + (r - M) * I;
+    uint16_t* dst = is_x ? Xp + r * P : Wp + (r - M) * P;
+    for (int c0 = lane; c0 < chunks; c0 += 4 * 32) {
+      uint32_t w[4][4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int k = (c0 + 32 * u) * 8;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int e = k + 2 * j;
+          if (pairs) {
+            w[u][j] = e < I ? __ldg(reinterpret_cast<const unsigned int*>(src + e)) : 0u;
+          } else {
+            const uint32_t lo = e < I ? __ldg(reinterpret_cast<const unsigned short*>(src + e)) : 0u;
+            const uint32_t hi =
+                e + 1 < I ? __ldg(reinterpret_cast<const unsigned short*>(src + e + 1)) : 0u;
+            w[u][j] = lo | (hi << 16);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = c0 + 32 * u;
+        if (c < chunks)
+          *reinterpret_cast<uint4*>(dst + c * 8) = make_uint4(w[u][0], w[u][1], w[u][2], w[u][3]);
+      }
+    }
+  }
+}
+
+// Library-owned memory pool of the scratch copies, one per device, created on
+// first use and kept for the life of the process. Allocations and frees are
+// stream-ordered on the caller's stream; up to 256 MiB of freed scratch stays
+// reserved in the pool between calls.
+int scratch_pool(int device, cudaMemPool_t* out, std::string& err) {
+  static std::mutex mu;
+  static cudaMemPool_t pools[64] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (device < 0 || device >= 64) {
+    err = "dense_xwt: device ordinal out of range";
+    return CSA_ERR_CUDA;
+  }
+  if (!pools[device]) {
+    cudaMemPoolProps props{};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = device;
+    cudaMemPool_t pool = nullptr;
+    cudaError_t e = cudaMemPoolCreate(&pool, &props);
+    if (e != cudaSuccess) {
+      err = std::string("dense_xwt: cudaMemPoolCreate: ") + cudaGetErrorString(e);
+      return CSA_ERR_CUDA;
+    }
+    uint64_t keep = 256ull << 20;
+    e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    if (e != cudaSuccess) {
+      cudaMemPoolDestroy(pool);
+      err = std::string("dense_xwt: cudaMemPoolSetAttribute: ") + cudaGetErrorString(e);
+      return CSA_ERR_CUDA;
+    }
+    pools[device] = pool;
+  }
+  *out = pools[device];
+  return CSA_OK;
+}
+
 // Tile width along H: the largest BN whose wave count times tile cost is
 // smallest (tile cost ~ BN plus a fixed per-tile overhead).
 int choose_bn(int M, int H, int sms) {
@@ -445,6 +541,35 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
   a.tma_load = ((static_cast<long long>(I) * 2) % 16 == 0 && px % 16 == 0 && pw % 16 == 0) ? 1u : 0u;
   a.tma_store = ((static_cast<long long>(H) * 4) % 16 == 0 && py % 16 == 0) ? 1u : 0u;
   a.vec2 = (I % 2 == 0 && px % 4 == 0 && pw % 4 == 0) ? 1u : 0u;
+
+  // Rows no tensor map can describe: copy them to 16-byte-aligned rows first
+  // (unless the caller asked for the loader-warp fetch, or no scratch is had).
+  const void* X_tma = X;
+  const void* W_tma = W;
+  long long pitch = I;
+  void* scratch = nullptr;
+  if (!a.tma_load && dense_fetch_mode() == CSA_DENSE_FETCH_AUTO) {
+    const long long P = (static_cast<long long>(I) + 7) / 8 * 8;
+    const size_t bytes_x = (static_cast<size_t>(M) * P * 2 + 255) / 256 * 256;
+    const size_t bytes = bytes_x + static_cast<size_t>(H) * P * 2;
+    cudaMemPool_t pool = nullptr;
+    int rc = scratch_pool(dev.device, &pool, err);
+    if (rc != CSA_OK) return rc;
+    if (cudaMallocFromPoolAsync(&scratch, bytes, pool, stream) != cudaSuccess) {
+      (void)cudaGetLastError();  // out of memory: fetch with loader warps instead
+      scratch = nullptr;
+    } else {
+      X_tma = scratch;
+      W_tma = static_cast<uint8_t*>(scratch) + bytes_x;
+      pitch = P;
+      a.tma_load = 1u;
+    }
+  }
+  // Releases the scratch copy in stream order after the product's launch.
+  auto release = [&](int rc) {
+    if (scratch) cudaFreeAsync(scratch, stream);
+    return rc;
+  };
   a.idesc = idesc_bf16_f32(kBM, a.BN);
   a.X = static_cast<const uint16_t*>(X);
   a.W = static_cast<const uint16_t*>(W);
@@ -461,7 +586,7 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
   a.load_depth = std::min(a.stages, 4);
   if (a.stages < 2) {
     err = "dense_xwt: not enough shared memory";
-    return CSA_ERR_UNSUPPORTED;
+    return release(CSA_ERR_UNSUPPORTED);
   }
   a.off_staging = static_cast<uint32_t>(a.stages) * a.stage_bytes;
   a.off_bars = a.off_staging + kStagingBytes;
@@ -475,15 +600,15 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
   if (a.tma_load) {
     const uint64_t dx[2] = {static_cast<uint64_t>(I), static_cast<uint64_t>(M)};
     const uint64_t dw[2] = {static_cast<uint64_t>(I), static_cast<uint64_t>(H)};
-    const uint64_t st[1] = {static_cast<uint64_t>(I) * 2};
+    const uint64_t st[1] = {static_cast<uint64_t>(pitch) * 2};
     const uint32_t bx[2] = {kBK, kBM};
     const uint32_t bw[2] = {kBK, static_cast<uint32_t>(a.BN)};
-    int rc = encode_tiled(&map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X, dx, st, bx,
+    int rc = encode_tiled(&map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X_tma, dx, st, bx,
                           CU_TENSOR_MAP_SWIZZLE_128B, err);
-    if (rc != CSA_OK) return rc;
-    rc = encode_tiled(&map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, dw, st, bw,
+    if (rc != CSA_OK) return release(rc);
+    rc = encode_tiled(&map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W_tma, dw, st, bw,
                       CU_TENSOR_MAP_SWIZZLE_128B, err);
-    if (rc != CSA_OK) return rc;
+    if (rc != CSA_OK) return release(rc);
   }
   if (a.tma_store) {
     const uint64_t dy[2] = {static_cast<uint64_t>(H), static_cast<uint64_t>(M)};
@@ -491,7 +616,7 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
     const uint32_t by[2] = {32, 32};
     int rc = encode_tiled(&map_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, Y, dy, st, by,
                           CU_TENSOR_MAP_SWIZZLE_128B, err);
-    if (rc != CSA_OK) return rc;
+    if (rc != CSA_OK) return release(rc);
   }
 
   {
@@ -499,19 +624,35 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
                                   static_cast<int>(smem), dev.device, err);
     if (rc != CSA_OK) {
       err = "dense_xwt: " + err;
-      return rc;
+      return release(rc);
     }
   }
   cudaError_t e;
+  if (scratch) {
+    // The realigned copy, launched last of all so that a call that fails a
+    // check launches nothing.
+    const long long rows = static_cast<long long>(M) + H;
+    const long long blocks = std::min<long long>(
+        (rows + kRealignThreads / 32 - 1) / (kRealignThreads / 32), 16LL * dev.sm_count);
+    e = launch_programmatic(realign_rows_kernel, static_cast<unsigned>(blocks), kRealignThreads,
+                            0, stream, a.X, a.W, static_cast<uint16_t*>(const_cast<void*>(X_tma)),
+                            static_cast<uint16_t*>(const_cast<void*>(W_tma)), M, H, I,
+                            static_cast<int>(pitch), a.vec2 ? 1 : 0);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) {
+      err = std::string("dense_xwt: launch: ") + cudaGetErrorString(e);
+      return release(CSA_ERR_LAUNCH);
+    }
+  }
   const long long grid = std::min<long long>(a.num_tiles, dev.sm_count);
   e = launch_programmatic(dense_sm103a_kernel, static_cast<unsigned>(grid), kThreads, smem, stream,
                           map_x, map_w, map_y, a);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     err = std::string("dense_xwt: launch: ") + cudaGetErrorString(e);
-    return CSA_ERR_LAUNCH;
+    return release(CSA_ERR_LAUNCH);
   }
-  return CSA_OK;
+  return release(CSA_OK);
 }
 
 }  // namespace csa

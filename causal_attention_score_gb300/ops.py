@@ -141,5 +141,16 @@ def debug_inject(enable: bool = True) -> None:
     _lib.load().csa_debug_inject(1 if enable else 0)
 
 
+DENSE_FETCH_AUTO = 0
+DENSE_FETCH_LOADERS = 1
+
+
+def set_dense_fetch(mode: int) -> None:
+    """Process-wide fetch mode of ``dense_xwt`` for rows no tensor map can describe:
+    ``DENSE_FETCH_AUTO`` (realigned scratch copy + TMA) or ``DENSE_FETCH_LOADERS``
+    (loader warps, no scratch)."""
+    _lib.check(_lib.load().csa_set_dense_fetch(int(mode)), "csa_set_dense_fetch")
+
+
 def version() -> str:
     return _lib.load().csa_version().decode()

@@ -158,16 +158,37 @@ csa_status trimul_forward_noalloc(float* out, const void* qkv, int B, int T, int
  *   M, I, H >= 1, any values (no tile-multiple requirement).
  *
  * X and W need only 2-byte alignment: when I*2 is a multiple of 16 and both
- * are 16-byte aligned, tiles are fetched by TMA; otherwise loader warps fetch
- * them with plain loads. Y is written by TMA when H*4 is a multiple of 16 and
+ * are 16-byte aligned, tiles are fetched by TMA. Otherwise (fetch mode
+ * CSA_DENSE_FETCH_AUTO, the default) a first kernel copies the rows of X and W
+ * into a scratch copy whose rows start on 16-byte boundaries, and the tiles
+ * are fetched from it by TMA; the scratch, (M + H) * ceil8(I) * 2 bytes plus
+ * at most 256, comes from a memory pool the library owns (one per device) and
+ * is allocated and released in order on the call's stream, so the call may
+ * be captured in a CUDA graph. If it cannot be had, or in mode
+ * CSA_DENSE_FETCH_LOADERS, loader warps fetch the tiles with plain loads
+ * instead (no scratch). Y is written by TMA when H*4 is a multiple of 16 and
  * Y is 16-byte aligned (4-byte alignment required otherwise).
- * Sums are fp32 accumulations of exact bf16 products.
+ * Sums are fp32 accumulations of exact bf16 products, in the same order on
+ * every fetch path (results are bit-identical).
  */
 csa_status dense_xwt(float* Y, const void* X, const void* W, int M, int I, int H);
 
 /* dense_xwt_ex -- as dense_xwt on `stream` (cudaStream_t as void*). */
 csa_status dense_xwt_ex(float* Y, const void* X, const void* W, int M, int I, int H,
                         void* stream);
+
+/*
+ * csa_set_dense_fetch -- process-wide fetch mode of dense_xwt for rows that no
+ * tensor map can describe (I*2 not a multiple of 16, or X / W not 16-byte
+ * aligned):
+ *   CSA_DENSE_FETCH_AUTO     copy the rows to 16-byte-aligned scratch, then TMA
+ *                            (loader warps if the scratch cannot be had);
+ *   CSA_DENSE_FETCH_LOADERS  loader warps inside the product kernel, no scratch.
+ * Returns CSA_OK, or CSA_ERR_SHAPE for an unknown mode (the mode is unchanged).
+ */
+#define CSA_DENSE_FETCH_AUTO    0
+#define CSA_DENSE_FETCH_LOADERS 1
+csa_status csa_set_dense_fetch(int mode);
 
 /*
  * causal_softmax_forward -- the causal score rows of trimul_forward followed by

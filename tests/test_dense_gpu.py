@@ -103,10 +103,84 @@ def test_dense_sweep(oracle_lib):
         assert bool(torch.all(torch.isfinite(Y)))
 
 
+@pytest.fixture(params=["auto", "loaders"])
+def fetch_mode(request):
+    """Both fetch paths for rows no tensor map can describe: the realigned scratch
+    copy + TMA (default) and the loader warps (no scratch)."""
+    mode = csa.DENSE_FETCH_AUTO if request.param == "auto" else csa.DENSE_FETCH_LOADERS
+    csa.set_dense_fetch(mode)
+    yield request.param
+    csa.set_dense_fetch(csa.DENSE_FETCH_AUTO)
+
+
+# Shapes whose rows no tensor map can describe (I * 2 % 16 != 0): even and odd I,
+# rows shorter than one 16-byte chunk, ragged tiles on every axis.
+MISALIGNED_ROWS = [(960, 770, 768), (17, 770, 768), (129, 65, 129), (33, 21, 7), (5, 2, 3),
+                   (7, 10, 9), (131, 258, 129), (300, 1002, 770), (1, 1, 1)]
+
+
+@pytest.mark.parametrize("M,I,H", MISALIGNED_ROWS)
+def test_dense_fetch_paths(oracle_lib, fetch_mode, M, I, H):
+    X, W = synth.dense_input(synth.DenseShape(M=M, I=I, H=H), seed=3 * M + I)
+    ref = oracle_lib.dense(synth.bf16_bits(X).reshape(-1), synth.bf16_bits(W).reshape(-1), M, I, H)
+    Y = _run(X, W)
+    assert_close(Y.cpu().numpy(), ref, f"dense{(M, I, H)} fetch={fetch_mode}")
+
+
+@pytest.mark.parametrize("M,I,H", [(960, 770, 768), (257, 129, 255), (40, 1000, 3072)])
+def test_dense_fetch_paths_bit_identical(M, I, H):
+    """The realigned copy and the loader warps feed the same tiles in the same
+    order: the two results are equal bit for bit."""
+    X, W = synth.dense_input(synth.DenseShape(M=M, I=I, H=H), seed=11)
+    try:
+        csa.set_dense_fetch(csa.DENSE_FETCH_LOADERS)
+        y_loaders = _run(X, W)
+    finally:
+        csa.set_dense_fetch(csa.DENSE_FETCH_AUTO)
+    y_auto = _run(X, W)
+    assert np.array_equal(f32_bits(y_auto), f32_bits(y_loaders))
+
+
+def test_dense_fetch_mode_rejects_unknown():
+    with pytest.raises(csa.CsaError):
+        csa.set_dense_fetch(7)
+
+
+def test_dense_realigned_on_streams_and_graph(oracle_lib):
+    """The scratch copy is stream-ordered: calls on two streams at once, and the
+    call captured in a CUDA graph and replayed, give the oracle's result."""
+    M, I, H = 300, 770, 512
+    X, W = synth.dense_input(synth.DenseShape(M=M, I=I, H=H), seed=21)
+    ref = oracle_lib.dense(synth.bf16_bits(X).reshape(-1), synth.bf16_bits(W).reshape(-1), M, I, H)
+    Xd, Wd = X.cuda(), W.cuda()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    ys = [poisoned((M, H)), poisoned((M, H))]
+    torch.cuda.synchronize()
+    for _ in range(4):
+        for st, y in zip(streams, ys):
+            csa.dense_xwt(y, Xd, Wd, M, I, H, stream=st)
+    torch.cuda.synchronize()
+    for y in ys:
+        assert_close(y.cpu().numpy(), ref, "dense on two streams")
+    side = torch.cuda.Stream()
+    yg = poisoned((M, H))
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        csa.dense_xwt(yg, Xd, Wd, M, I, H, stream=side)
+    for _ in range(3):
+        yg.fill_(float("nan"))
+        g.replay()
+    torch.cuda.synchronize()
+    assert csa.get_status() == 0
+    assert_close(yg.cpu().numpy(), ref, "dense replayed from a graph")
+
+
 @pytest.mark.parametrize("offset", [1, 2])
-def test_dense_misaligned_views(oracle_lib, offset):
+def test_dense_misaligned_views(oracle_lib, fetch_mode, offset):
     """X and W views starting 2 or 4 bytes into their storage: not 16-byte aligned,
-    so the plain-load fetch runs (2-byte pairs or 4-byte pairs)."""
+    so they are read 2 bytes or 4 bytes at a time (by the realigning copy or by
+    the loader warps)."""
     M, I, H = 130, 770, 70
     Xb, Wb = synth.dense_input(synth.DenseShape(M=M, I=I + offset, H=H), seed=9)
     Xf = Xb.reshape(-1)[offset:offset + M * I].reshape(M, I)

@@ -82,10 +82,13 @@ def test_withheld_load_softmax(oracle_lib):
                                                              shape.NH), check)
 
 
-@pytest.mark.parametrize("M,I,H", [(960, 770, 768),   # loader warps, 4-byte cp.async
-                                   (300, 768, 512),   # TMA fetch
-                                   (130, 771, 200)])  # loader warps, 2-byte loads
-def test_withheld_hand_off_dense(oracle_lib, M, I, H):
+@pytest.mark.parametrize("M,I,H,mode", [
+    (960, 770, 768, csa.DENSE_FETCH_LOADERS),  # loader warps, 4-byte cp.async
+    (300, 768, 512, csa.DENSE_FETCH_AUTO),     # TMA fetch
+    (130, 771, 200, csa.DENSE_FETCH_LOADERS),  # loader warps, 2-byte loads
+    (960, 770, 768, csa.DENSE_FETCH_AUTO),     # realigned scratch copy, then TMA
+])
+def test_withheld_hand_off_dense(oracle_lib, M, I, H, mode):
     X, W = synth.dense_input(synth.DenseShape(M=M, I=I, H=H), seed=6)
     Xd, Wd = X.cuda(), W.cuda()
     Y = torch.empty((M, H), dtype=torch.float32, device="cuda")
@@ -96,4 +99,8 @@ def test_withheld_hand_off_dense(oracle_lib, M, I, H):
                                M, I, H)
         assert_close(Y.cpu().numpy(), ref, f"dense {M}x{I}x{H} after timeout")
 
-    _timeout_then_recover(lambda: csa.dense_xwt(Y, Xd, Wd, M, I, H), check)
+    csa.set_dense_fetch(mode)
+    try:
+        _timeout_then_recover(lambda: csa.dense_xwt(Y, Xd, Wd, M, I, H), check)
+    finally:
+        csa.set_dense_fetch(csa.DENSE_FETCH_AUTO)
