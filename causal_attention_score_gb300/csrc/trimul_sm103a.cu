@@ -35,9 +35,15 @@
 //    2^-21 |x|), and each tile accumulates hi.hi + hi.lo + lo.hi (lo.lo is
 //    below 2^-20 |q.k|). The tensor core reads only the top 19 bits of an fp32
 //    operand, so the loaded x serves as hi as it is (measured: bit-identical
-//    results to explicitly cleared operands). A stage holds one 32-element
-//    chunk of the Q and K tiles; warps 11-14 write its lo parts beside it
-//    before the MMA warp reads both.
+//    results to explicitly cleared operands). With HS <= 128 the Q tile of a
+//    row block lives in TMEM as the MMA's A operand: its hi and lo parts take
+//    2 * HS of the 512 columns beside the two accumulators, written once per
+//    row block by warps 11-14 (one per lane quarter, tcgen05.st) from Q
+//    chunks that pass through the ring, so the ring carries only K, one
+//    32-element chunk per stage with its lo part beside it (written by the
+//    same warps), and each CTA walks one contiguous run of the work list so
+//    that consecutive tiles share their Q. With 128 < HS <= 256 a stage holds
+//    one 32-element chunk of both Q and K and their lo parts.
 //  - warp 10: fill writer. It takes fill tiles from the launch-wide pool while
 //    the epilogue has nothing to store (start-up, a wait on the MMA, after the
 //    last lower tile) and writes each as 128 x 16 TMA stores of a resident
@@ -73,6 +79,13 @@ constexpr int kChunkBytes = kTile * 128;  // one 128-row x 64-element operand ch
 #endif
 #ifndef CSA_TRIMUL_MAX_STORE_GROUPS
 #define CSA_TRIMUL_MAX_STORE_GROUPS 1
+#endif
+// fp32 form with Q in TMEM: raw-chunk ring depth and K lo ring slots.
+#ifndef CSA_TRIMUL_MAX_STAGES_QT
+#define CSA_TRIMUL_MAX_STAGES_QT 8
+#endif
+#ifndef CSA_TRIMUL_LO_SLOTS
+#define CSA_TRIMUL_LO_SLOTS 3
 #endif
 
 constexpr int kEpiWarps = 8;        // two per TMEM lane quarter
@@ -113,6 +126,16 @@ struct TrimulArgs {
   // Operand chunks (128-byte rows) per stage, and stages per tile: bf16 keeps a
   // whole tile's chunks in one stage; the fp32 form streams one chunk per stage.
   int stage_chunks, tile_stages, chunk_elems;
+  // fp32 form with HS <= 128: Q's hi / lo parts held in TMEM (the MMA's A
+  // operand) for a whole row block; a ring stage then holds one K chunk and
+  // its lo part, or a Q chunk on its way to TMEM.
+  uint32_t q_tmem;
+  uint32_t contig;  // static deal as one contiguous run of the work list per CTA
+  int tmem_cols;    // TMEM columns allocated: 256, or 512 with q_tmem
+  // With q_tmem the ring holds raw chunks only; the lo parts of K chunks go to
+  // a separate ring of lo_slots chunks at off_lo, freed by the MMA's commit.
+  int lo_slots;
+  uint32_t off_lo;
 };
 
 // Counters per launch: [0] work-list position, [1] finished CTAs, [2] fill tile.
@@ -199,6 +222,11 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
   auto sempty_bar = [&](int s) { return bars + 8u * (2 * a.stages + 5 + kSchedDepth + s); };
   // fp32 form: stage s split into hi / lo and ready for the MMA.
   auto conv_bar = [&](int s) { return bars + 8u * (2 * a.stages + 5 + 2 * kSchedDepth + s); };
+  // Q in TMEM: the MMAs reading the current Q are complete (it may be replaced).
+  const uint32_t qfree_bar = bars + 8u * (3 * a.stages + 5 + 2 * kSchedDepth);
+  // Q in TMEM: lo slot l of the K lo ring is free again.
+  auto lofree_bar = [&](int l) { return bars + 8u * (3 * a.stages + 6 + 2 * kSchedDepth + l); };
+  auto lo_slot = [&](int l) { return base + a.off_lo + static_cast<uint32_t>(l) * kChunkBytes; };
   constexpr int kBlockThreads = kF32 ? kThreadsF32 : kThreads;
   auto sched_entry = [&](int s) { return base + a.off_misc + 16u + 4u * s; };
   const uint32_t tmem_slot = base + a.off_misc;
@@ -210,8 +238,12 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
   auto k_chunk = [&](int s, int kc) {
     return base + s * a.stage_bytes + (a.stage_chunks + kc) * kChunkBytes;
   };
-  // fp32 form: the lo parts of a stage's Q and K chunks follow its hi parts.
+  // fp32 form without Q in TMEM: the lo parts of a stage's Q and K chunks
+  // follow its raw chunks.
   auto lo_chunk = [&](uint32_t hi) { return hi + 2u * kChunkBytes; };
+  // Q in TMEM: columns of its hi and lo parts (after the two accumulators).
+  const uint32_t qhi_col = kTmemCols;
+  const uint32_t qlo_col = kTmemCols + 32u * static_cast<uint32_t>(a.kchunks);
 
   const Watchdog wd{a.wait_limit_ns, a.status, abort_flag};
 
@@ -229,8 +261,11 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
       mbar_init(sfull_bar(s), 1);
       mbar_init(sempty_bar(s), 1 + kEpiWarps + (kF32 ? kConvWarps : 0));
     }
-    if (kF32)
+    if (kF32) {
       for (int s = 0; s < a.stages; ++s) mbar_init(conv_bar(s), kConvWarps);
+      mbar_init(qfree_bar, 1);
+      for (int l = 0; l < a.lo_slots; ++l) mbar_init(lofree_bar(l), 1);
+    }
     *abort_flag = 0;
     *epi_idle = 1;
     fence_barrier_init();
@@ -242,7 +277,7 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
     fence_proxy_async_smem();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_alloc(tmem_slot, static_cast<uint32_t>(a.tmem_cols));
     tmem_relinquish();
     tc_fence_before_sync();
   }
@@ -263,20 +298,32 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;  // per-stage: loads that may be in flight
       bool injected = false;
-      const uint32_t tx = static_cast<uint32_t>(a.stage_chunks) * 2u * kChunkBytes;
+      // Bytes per stage: one chunk with Q in TMEM (a K chunk, or a Q chunk on its
+      // way to TMEM), else the stage's Q and K chunks.
+      const uint32_t tx = a.q_tmem ? static_cast<uint32_t>(kChunkBytes)
+                                   : static_cast<uint32_t>(a.stage_chunks) * 2u * kChunkBytes;
       // Work list: the computed tiles, (b, h)-major. Positions are taken from a
       // shared counter (kFetchAhead fetches in flight) when a fill pool absorbs
       // the imbalance that leaves, else dealt statically (c, c+G, ...) so that
       // every CTA knows its operands ahead. Each position goes to the MMA and
       // epilogue warps through the shared ring.
       const bool dynamic = a.dynamic != 0;
-      unsigned int static_next = blockIdx.x;
+      // Static deals: c, c+G, c+2G, ...; or (contig) the run [c*n/G, (c+1)*n/G),
+      // whose consecutive tiles mostly share a row block.
+      const long long n_lower = a.n_lower;
+      unsigned int static_next =
+          a.contig ? static_cast<unsigned int>(blockIdx.x * n_lower / gridDim.x) : blockIdx.x;
+      const unsigned int static_end =
+          static_cast<unsigned int>((blockIdx.x + 1ll) * n_lower / gridDim.x);
       auto fetch = [&]() -> unsigned int {
         if (dynamic) return atomicAdd(a.sched, 1u);
+        if (a.contig)
+          return static_next < static_end ? static_next++ : static_cast<unsigned int>(a.n_lower);
         const unsigned int v = static_next;
         static_next += gridDim.x;
         return v;
       };
+      int q_bh = -1, q_ti = -1;  // the row block whose Q is in TMEM
       unsigned int pf[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) pf[i] = i < kFetchAhead ? fetch() : 0u;
@@ -300,8 +347,15 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
         decode_position(static_cast<int>(cur), a.per_lower, bh, r);
         decode_computed(r, a.causal, a.Tt2, ti, tj);
         const int outer = bh / a.nh_div, inner = bh - outer * a.nh_div;
+        // Q in TMEM: a new row block first sends its Q chunks through the ring.
+        const bool new_q = a.q_tmem && (bh != q_bh || ti != q_ti);
+        if (new_q) {
+          q_bh = bh;
+          q_ti = ti;
+        }
+        const int q_stages = new_q ? a.kchunks : 0;
         bool ok = true;
-        for (int ts = 0; ts < a.tile_stages; ++ts) {
+        for (int ts = 0; ts < q_stages + a.tile_stages; ++ts) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, wd, kSiteProducerEmpty)) {
             ok = false;
             break;
@@ -310,6 +364,16 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
           if (a.inject && !injected) {
             injected = true;  // withhold this CTA's first loads: its consumer's wait must run out
             issued &= ~(1u << stage);
+          } else if (a.q_tmem) {
+            const bool is_q = ts < q_stages;
+            const int x = (is_q ? ts : ts - q_stages) * a.chunk_elems;
+            if (is_q)
+              tma_load_4d(q_chunk(stage, 0), &tmap_a, full_bar(stage), x, inner, ti * kTile, outer);
+            else
+              tma_load_4d(q_chunk(stage, 0), &tmap_b, full_bar(stage), x, a.b_off + inner,
+                          tj * kTile, outer);
+            issued |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           } else {
             for (int kc = 0; kc < a.stage_chunks; ++kc) {
               const int x = (ts * a.stage_chunks + kc) * a.chunk_elems;
@@ -349,6 +413,9 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
       uint32_t acc_phase = 0;
       int slot = 0;
       uint32_t sphase = 0;
+      int q_bh = -1, q_ti = -1;  // Q in TMEM: the row block it holds, and how many so far
+      uint32_t n_q = 0;
+      int lo = 0;  // Q in TMEM: next slot of the K lo ring
       while (true) {
         if (!mbar_wait(sfull_bar(slot), sphase, wd, kSiteSched)) break;
         const unsigned int cur = ld_shared_b32(sched_entry(slot));
@@ -358,6 +425,35 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
           sphase ^= 1u;
         }
         if (cur == kEntryEnd) break;
+        if constexpr (kF32) {
+          if (a.q_tmem) {
+            int bh, r, ti, tj;
+            decode_position(static_cast<int>(cur), a.per_lower, bh, r);
+            decode_computed(r, a.causal, a.Tt2, ti, tj);
+            if (bh != q_bh || ti != q_ti) {
+              q_bh = bh;
+              q_ti = ti;
+              // The splitter may overwrite Q once the MMAs reading it are complete.
+              if (n_q > 0) umma_commit(qfree_bar);
+              ++n_q;
+              // The row block's Q chunks: written to TMEM by the splitter, which
+              // then hands each ring slot back through this thread.
+              bool q_ok = true;
+              for (int c = 0; c < a.kchunks; ++c) {
+                if (!mbar_wait(conv_bar(stage), phase, wd, kSiteMmaFull)) {
+                  q_ok = false;
+                  break;
+                }
+                mbar_arrive(empty_bar(stage));
+                if (++stage == a.stages) {
+                  stage = 0;
+                  phase ^= 1u;
+                }
+              }
+              if (!q_ok) break;
+            }
+          }
+        }
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, wd, kSiteMmaTmemEmpty)) break;
         tc_fence_after_sync();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kTile);
@@ -369,6 +465,27 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
           }
           tc_fence_after_sync();
           if constexpr (kF32) {
+            if (a.q_tmem) {
+              // One 32-element K chunk against Q's hi / lo columns in TMEM: 4 steps
+              // of 8 along K, each hi.hi + hi.lo + lo.hi.
+              // Descriptors built once per stage; a step of 8 tf32 along K adds 32 B
+              // (2 in the descriptor's address field) and 8 TMEM columns.
+              const uint64_t khi = umma_desc_k_sw128(q_chunk(stage, 0));
+              const uint64_t klo = umma_desc_k_sw128(lo_slot(lo));
+              const uint32_t ahi = tmem_base + qhi_col + static_cast<uint32_t>(ts) * 32u;
+              const uint32_t alo = tmem_base + qlo_col + static_cast<uint32_t>(ts) * 32u;
+              umma_tf32_ts(d, ahi, khi, kIdescTf32, ts > 0 ? 1u : 0u);
+              umma_tf32_ts(d, ahi, klo, kIdescTf32, 1u);
+              umma_tf32_ts(d, alo, khi, kIdescTf32, 1u);
+#pragma unroll
+              for (uint32_t k = 1; k < 4; ++k) {
+                umma_tf32_ts(d, ahi + 8u * k, khi + 2u * k, kIdescTf32, 1u);
+                umma_tf32_ts(d, ahi + 8u * k, klo + 2u * k, kIdescTf32, 1u);
+                umma_tf32_ts(d, alo + 8u * k, khi + 2u * k, kIdescTf32, 1u);
+              }
+              umma_commit(lofree_bar(lo));  // lo slot read -> the splitter may refill it
+              if (++lo == a.lo_slots) lo = 0;
+            } else {
             // One 32-element chunk: 4 steps of 8 along K, each hi.hi + hi.lo + lo.hi.
             const uint32_t qh = q_chunk(stage, 0), kh = k_chunk(stage, 0);
             for (int k = 0; k < 4; ++k) {
@@ -377,6 +494,7 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
               umma_tf32(d, qhi, khi, kIdescTf32, (ts > 0 || k > 0) ? 1u : 0u);
               umma_tf32(d, qhi, umma_desc_k_sw128(lo_chunk(kh) + off), kIdescTf32, 1u);
               umma_tf32(d, umma_desc_k_sw128(lo_chunk(qh) + off), khi, kIdescTf32, 1u);
+            }
             }
           } else {
             for (int k = 0; k < a.ksteps; ++k) {
@@ -411,9 +529,16 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
     // once its fp32 Q and K chunks have landed, store lo = x - hi beside each
     // value x (hi = x with the low 13 mantissa bits cleared, which is what the
     // tensor core reads of x itself), then hand the stage to the MMA warp.
+    // With Q in TMEM, the same warps first write each new row block's Q: warp w
+    // owns TMEM lane quarter w % 4, i.e. Q rows 32 (w % 4) .. + 31.
     const uint32_t cw = warp - kFirstConvWarp;
+    const uint32_t quarter = warp & 3u;
     int stage = 0, slot = 0;
     uint32_t phase = 0, sphase = 0;
+    int q_bh = -1, q_ti = -1;
+    uint32_t n_q = 0;
+    int lo = 0;  // Q in TMEM: next slot of the K lo ring, and its pass parity
+    uint32_t lo_phase = 0;
     bool ok = true;
     while (ok) {
       int got = 1;
@@ -432,16 +557,78 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
         slot = 0;
         sphase ^= 1u;
       }
+      if (a.q_tmem) {
+        int bh, r, ti, tj;
+        decode_position(static_cast<int>(cur), a.per_lower, bh, r);
+        decode_computed(r, a.causal, a.Tt2, ti, tj);
+        if (bh != q_bh || ti != q_ti) {
+          q_bh = bh;
+          q_ti = ti;
+          // The previous Q may be overwritten once the MMAs reading it are complete.
+          if (n_q > 0 && !mbar_wait_warp(qfree_bar, (n_q - 1u) & 1u, wd, kSiteMmaFull)) break;
+          tc_fence_after_sync();
+          ++n_q;
+          const uint32_t row = quarter * 32u + lane;  // this lane's Q row and TMEM lane
+          const uint32_t lane_addr = tmem_base + ((quarter * 32u) << 16);
+          for (int c = 0; c < a.kchunks; ++c) {
+            if (!mbar_wait_warp(full_bar(stage), phase, wd, kSiteMmaFull)) {
+              ok = false;
+              break;
+            }
+            // Row `row` of the 128-byte-swizzled chunk: 16-byte unit j sits at
+            // position j ^ (row % 8).
+            const uint32_t rowp = q_chunk(stage, 0) + row * 128u;
+            uint32_t hi[32], lo[32];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              uint32_t x[4];
+              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
+                           : "r"(rowp + ((static_cast<uint32_t>(j) ^ (row & 7u)) << 4)));
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                hi[4 * j + e] = x[e] & 0xFFFFE000u;
+                lo[4 * j + e] = __float_as_uint(__uint_as_float(x[e]) -
+                                                __uint_as_float(hi[4 * j + e]));
+              }
+            }
+            tmem_st_32cols(lane_addr + qhi_col + 32u * static_cast<uint32_t>(c), hi);
+            tmem_st_32cols(lane_addr + qlo_col + 32u * static_cast<uint32_t>(c), lo);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(conv_bar(stage));
+            if (++stage == a.stages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+        }
+      }
       for (int ts = 0; ts < a.tile_stages; ++ts) {
         if (!mbar_wait_warp(full_bar(stage), phase, wd, kSiteMmaFull)) {
           ok = false;
           break;
         }
-        // The stage's Q and K chunks are 2 x 16 KB, contiguous: 2048 16-byte words,
-        // 16 per lane of the 4 splitter warps, four loads in flight per lane.
+        // The stage's raw chunks (K alone with Q in TMEM, else Q and K: 16 or
+        // 32 KB contiguous) as 16-byte words over the lanes of the 4 splitter
+        // warps, four loads in flight per lane. The lo parts go to the same
+        // offsets of the lo ring's next slot (Q in TMEM) or after the raw chunks.
         const uint32_t hi0 = q_chunk(stage, 0);
-        for (uint32_t i0 = cw * 32u + lane; i0 < 2u * kChunkBytes / 16u;
-             i0 += 4u * 32u * kConvWarps) {
+        uint32_t lo0 = lo_chunk(hi0);
+        const uint32_t words = (a.q_tmem ? 1u : 2u) * kChunkBytes / 16u;
+        if (a.q_tmem) {
+          if (!mbar_wait_warp(lofree_bar(lo), lo_phase ^ 1u, wd, kSiteMmaFull)) {
+            ok = false;
+            break;
+          }
+          lo0 = lo_slot(lo);
+          if (++lo == a.lo_slots) {
+            lo = 0;
+            lo_phase ^= 1u;
+          }
+        }
+        for (uint32_t i0 = cw * 32u + lane; i0 < words; i0 += 4u * 32u * kConvWarps) {
           uint32_t x[4][4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -457,8 +644,7 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
             for (int e = 0; e < 4; ++e)
               l4[e] = __float_as_uint(__uint_as_float(x[u][e]) -
                                       __uint_as_float(x[u][e] & 0xFFFFE000u));
-            st_shared_v4(lo_chunk(hi0 + 16u * (i0 + u * 32u * kConvWarps)), l4[0], l4[1], l4[2],
-                         l4[3]);
+            st_shared_v4(lo0 + 16u * (i0 + u * 32u * kConvWarps), l4[0], l4[1], l4[2], l4[3]);
           }
         }
         fence_proxy_async_smem();  // generic smem writes -> visible to tcgen05.mma
@@ -643,7 +829,7 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc(tmem_base, static_cast<uint32_t>(a.tmem_cols));
   }
   if (threadIdx.x == 0) {
     // Every fetch of this CTA is done; the last CTA to get here resets the pair.
@@ -702,7 +888,13 @@ int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& 
   a.n_fill = static_cast<int>(BH * per_fill);
   a.per_lower = static_cast<int>(per_lower);
   a.per_fill = static_cast<int>(per_fill);
-  a.dynamic = a.n_fill > 0 ? 1u : 0u;
+  // fp32 with HS <= 128: Q's hi / lo parts (2 x 32 columns per chunk) fit in
+  // TMEM beside the two accumulators; CTAs then take contiguous runs of tiles.
+  const bool q_tmem = f32 && a.kchunks <= (512 - kTmemCols) / 64;
+  a.q_tmem = q_tmem ? 1u : 0u;
+  a.contig = q_tmem ? 1u : 0u;
+  a.tmem_cols = q_tmem ? 512 : kTmemCols;
+  a.dynamic = (!q_tmem && a.n_fill > 0) ? 1u : 0u;
   a.scale = scale;
   a.mask_bits = mask_bits;
   a.lower_only = lower_only ? 1u : 0u;
@@ -715,26 +907,32 @@ int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& 
   // Shared memory: operand ring | staging boxes | mask buffer | barriers | misc.
   // Operand ring stages vs. staging depth: the most box pairs per epilogue warp
   // that still leave two ring stages, else one pair.
-  a.stage_bytes = f32 ? 4u * kChunkBytes : static_cast<uint32_t>(a.kchunks) * 2u * kChunkBytes;
+  a.stage_bytes = f32 ? (q_tmem ? 1u : 4u) * kChunkBytes
+                      : static_cast<uint32_t>(a.kchunks) * 2u * kChunkBytes;
+  a.lo_slots = q_tmem ? CSA_TRIMUL_LO_SLOTS : 0;
+  const int lo_bytes = a.lo_slots * kChunkBytes;
   // The mask buffer only exists when there are fill tiles (full causal mode).
   const int fill_bytes = a.n_fill > 0 ? kFillBytes : 0;
-  const int fixed = fill_bytes + 1024 /*bars+misc+ring*/ + 1024 /*align slack*/;
+  const int fixed = fill_bytes + lo_bytes + 1024 /*bars+misc+ring*/ + 1024 /*align slack*/;
+  const int max_stages = q_tmem ? CSA_TRIMUL_MAX_STAGES_QT : CSA_TRIMUL_MAX_STAGES;
   int staging_bytes = 0;
   for (int groups = CSA_TRIMUL_MAX_STORE_GROUPS; groups >= 1; --groups) {
     staging_bytes = kEpiWarps * groups * 2 * kBoxBytes;
     a.store_groups = static_cast<uint32_t>(groups);
-    a.stages = std::min(CSA_TRIMUL_MAX_STAGES, (dev.max_smem_optin - fixed - staging_bytes) /
-                                                   static_cast<int>(a.stage_bytes));
+    a.stages = std::min(max_stages, (dev.max_smem_optin - fixed - staging_bytes) /
+                                        static_cast<int>(a.stage_bytes));
     if (a.stages >= 2) break;
   }
   if (a.stages < 1) {
     err = name + ": not enough shared memory for one operand stage";
     return CSA_ERR_UNSUPPORTED;
   }
-  a.off_staging = static_cast<uint32_t>(a.stages) * a.stage_bytes;
+  a.off_lo = static_cast<uint32_t>(a.stages) * a.stage_bytes;
+  a.off_staging = a.off_lo + static_cast<uint32_t>(lo_bytes);
   a.off_mask = a.off_staging + static_cast<uint32_t>(staging_bytes);
   a.off_bars = a.off_mask + static_cast<uint32_t>(fill_bytes);
-  a.off_misc = a.off_bars + 8u * static_cast<uint32_t>(3 * a.stages + 5 + 2 * kSchedDepth);
+  a.off_misc =
+      a.off_bars + 8u * static_cast<uint32_t>(3 * a.stages + 6 + 2 * kSchedDepth + a.lo_slots);
   const size_t smem = a.off_misc + 16 + 4 * kSchedDepth + 1024;
 
   CUtensorMap map_out, map_fill;
