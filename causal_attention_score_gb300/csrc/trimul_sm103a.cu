@@ -87,6 +87,10 @@ constexpr int kChunkBytes = kTile * 128;  // one 128-row x 64-element operand ch
 #ifndef CSA_TRIMUL_LO_SLOTS
 #define CSA_TRIMUL_LO_SLOTS 3
 #endif
+// fp32 form with Q in TMEM: Q buffers when two fit (1 or 2).
+#ifndef CSA_TRIMUL_Q_BUFS
+#define CSA_TRIMUL_Q_BUFS 2
+#endif
 
 constexpr int kEpiWarps = 8;        // two per TMEM lane quarter
 constexpr int kFillWarp = 2 + kEpiWarps;
@@ -136,6 +140,9 @@ struct TrimulArgs {
   // a separate ring of lo_slots chunks at off_lo, freed by the MMA's commit.
   int lo_slots;
   uint32_t off_lo;
+  // Q buffers in TMEM (1, or 2 when two fit: HS <= 64), so that the next row
+  // block's Q is written while the MMAs still read the current one.
+  int q_bufs;
 };
 
 // Counters per launch: [0] work-list position, [1] finished CTAs, [2] fill tile.
@@ -222,10 +229,10 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
   auto sempty_bar = [&](int s) { return bars + 8u * (2 * a.stages + 5 + kSchedDepth + s); };
   // fp32 form: stage s split into hi / lo and ready for the MMA.
   auto conv_bar = [&](int s) { return bars + 8u * (2 * a.stages + 5 + 2 * kSchedDepth + s); };
-  // Q in TMEM: the MMAs reading the current Q are complete (it may be replaced).
-  const uint32_t qfree_bar = bars + 8u * (3 * a.stages + 5 + 2 * kSchedDepth);
+  // Q in TMEM: the MMAs reading the Q in buffer b are complete (it may be replaced).
+  auto qfree_bar = [&](uint32_t b) { return bars + 8u * (3 * a.stages + 5 + 2 * kSchedDepth + b); };
   // Q in TMEM: lo slot l of the K lo ring is free again.
-  auto lofree_bar = [&](int l) { return bars + 8u * (3 * a.stages + 6 + 2 * kSchedDepth + l); };
+  auto lofree_bar = [&](int l) { return bars + 8u * (3 * a.stages + 7 + 2 * kSchedDepth + l); };
   auto lo_slot = [&](int l) { return base + a.off_lo + static_cast<uint32_t>(l) * kChunkBytes; };
   constexpr int kBlockThreads = kF32 ? kThreadsF32 : kThreads;
   auto sched_entry = [&](int s) { return base + a.off_misc + 16u + 4u * s; };
@@ -241,9 +248,10 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
   // fp32 form without Q in TMEM: the lo parts of a stage's Q and K chunks
   // follow its raw chunks.
   auto lo_chunk = [&](uint32_t hi) { return hi + 2u * kChunkBytes; };
-  // Q in TMEM: columns of its hi and lo parts (after the two accumulators).
-  const uint32_t qhi_col = kTmemCols;
-  const uint32_t qlo_col = kTmemCols + 32u * static_cast<uint32_t>(a.kchunks);
+  // Q in TMEM: columns of buffer b's hi and lo parts (after the two accumulators).
+  const uint32_t q_cols = 32u * static_cast<uint32_t>(a.kchunks);
+  auto qhi_col = [&](uint32_t b) { return kTmemCols + 2u * q_cols * b; };
+  auto qlo_col = [&](uint32_t b) { return kTmemCols + 2u * q_cols * b + q_cols; };
 
   const Watchdog wd{a.wait_limit_ns, a.status, abort_flag};
 
@@ -263,7 +271,8 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
     }
     if (kF32) {
       for (int s = 0; s < a.stages; ++s) mbar_init(conv_bar(s), kConvWarps);
-      mbar_init(qfree_bar, 1);
+      mbar_init(qfree_bar(0), 1);
+      mbar_init(qfree_bar(1), 1);
       for (int l = 0; l < a.lo_slots; ++l) mbar_init(lofree_bar(l), 1);
     }
     *abort_flag = 0;
@@ -324,6 +333,7 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
         return v;
       };
       int q_bh = -1, q_ti = -1;  // the row block whose Q is in TMEM
+      const uint64_t l2_keep = l2_policy_evict_last(), l2_once = l2_policy_evict_first();
       unsigned int pf[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) pf[i] = i < kFetchAhead ? fetch() : 0u;
@@ -365,13 +375,17 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
             injected = true;  // withhold this CTA's first loads: its consumer's wait must run out
             issued &= ~(1u << stage);
           } else if (a.q_tmem) {
+            // CTAs walk separate runs of the list here, so a K tile's later uses
+            // come from other rows after much output has streamed through L2:
+            // K is kept there (evict_last), Q is read once per row block.
             const bool is_q = ts < q_stages;
             const int x = (is_q ? ts : ts - q_stages) * a.chunk_elems;
             if (is_q)
-              tma_load_4d(q_chunk(stage, 0), &tmap_a, full_bar(stage), x, inner, ti * kTile, outer);
+              tma_load_4d_hint(q_chunk(stage, 0), &tmap_a, full_bar(stage), x, inner, ti * kTile,
+                               outer, l2_once);
             else
-              tma_load_4d(q_chunk(stage, 0), &tmap_b, full_bar(stage), x, a.b_off + inner,
-                          tj * kTile, outer);
+              tma_load_4d_hint(q_chunk(stage, 0), &tmap_b, full_bar(stage), x, a.b_off + inner,
+                               tj * kTile, outer, l2_keep);
             issued |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           } else {
@@ -415,7 +429,8 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
       uint32_t sphase = 0;
       int q_bh = -1, q_ti = -1;  // Q in TMEM: the row block it holds, and how many so far
       uint32_t n_q = 0;
-      int lo = 0;  // Q in TMEM: next slot of the K lo ring
+      int lo = 0;         // Q in TMEM: next slot of the K lo ring
+      uint32_t qbuf = 0;  // Q in TMEM: the buffer the current Q is in
       while (true) {
         if (!mbar_wait(sfull_bar(slot), sphase, wd, kSiteSched)) break;
         const unsigned int cur = ld_shared_b32(sched_entry(slot));
@@ -433,8 +448,11 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
             if (bh != q_bh || ti != q_ti) {
               q_bh = bh;
               q_ti = ti;
-              // The splitter may overwrite Q once the MMAs reading it are complete.
-              if (n_q > 0) umma_commit(qfree_bar);
+              // The splitter may overwrite the previous Q's buffer once the MMAs
+              // reading it are complete.
+              const bool two = a.q_bufs == 2;
+              if (n_q > 0) umma_commit(qfree_bar(two ? ((n_q - 1u) & 1u) : 0u));
+              qbuf = two ? (n_q & 1u) : 0u;
               ++n_q;
               // The row block's Q chunks: written to TMEM by the splitter, which
               // then hands each ring slot back through this thread.
@@ -472,8 +490,8 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
               // (2 in the descriptor's address field) and 8 TMEM columns.
               const uint64_t khi = umma_desc_k_sw128(q_chunk(stage, 0));
               const uint64_t klo = umma_desc_k_sw128(lo_slot(lo));
-              const uint32_t ahi = tmem_base + qhi_col + static_cast<uint32_t>(ts) * 32u;
-              const uint32_t alo = tmem_base + qlo_col + static_cast<uint32_t>(ts) * 32u;
+              const uint32_t ahi = tmem_base + qhi_col(qbuf) + static_cast<uint32_t>(ts) * 32u;
+              const uint32_t alo = tmem_base + qlo_col(qbuf) + static_cast<uint32_t>(ts) * 32u;
               umma_tf32_ts(d, ahi, khi, kIdescTf32, ts > 0 ? 1u : 0u);
               umma_tf32_ts(d, ahi, klo, kIdescTf32, 1u);
               umma_tf32_ts(d, alo, khi, kIdescTf32, 1u);
@@ -564,8 +582,14 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
         if (bh != q_bh || ti != q_ti) {
           q_bh = bh;
           q_ti = ti;
-          // The previous Q may be overwritten once the MMAs reading it are complete.
-          if (n_q > 0 && !mbar_wait_warp(qfree_bar, (n_q - 1u) & 1u, wd, kSiteMmaFull)) break;
+          // Q number n_q goes to buffer n_q % q_bufs, once the MMAs reading the Q
+          // that used it before (number n_q - q_bufs) are complete.
+          const bool two = a.q_bufs == 2;
+          const uint32_t nb = two ? 2u : 1u;
+          const uint32_t qb = two ? (n_q & 1u) : 0u;
+          const uint32_t par = two ? (((n_q >> 1) - 1u) & 1u) : ((n_q - 1u) & 1u);
+          if (n_q >= nb && !mbar_wait_warp(qfree_bar(qb), par, wd, kSiteMmaFull))
+            break;
           tc_fence_after_sync();
           ++n_q;
           const uint32_t row = quarter * 32u + lane;  // this lane's Q row and TMEM lane
@@ -592,8 +616,8 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
                                                 __uint_as_float(hi[4 * j + e]));
               }
             }
-            tmem_st_32cols(lane_addr + qhi_col + 32u * static_cast<uint32_t>(c), hi);
-            tmem_st_32cols(lane_addr + qlo_col + 32u * static_cast<uint32_t>(c), lo);
+            tmem_st_32cols(lane_addr + qhi_col(qb) + 32u * static_cast<uint32_t>(c), hi);
+            tmem_st_32cols(lane_addr + qlo_col(qb) + 32u * static_cast<uint32_t>(c), lo);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(conv_bar(stage));
@@ -894,6 +918,8 @@ int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& 
   a.q_tmem = q_tmem ? 1u : 0u;
   a.contig = q_tmem ? 1u : 0u;
   a.tmem_cols = q_tmem ? 512 : kTmemCols;
+  // Two Q buffers when both fit beside the accumulators (2 x 64 columns per chunk).
+  a.q_bufs = (q_tmem && CSA_TRIMUL_Q_BUFS > 1 && kTmemCols + 2 * 64 * a.kchunks <= 512) ? 2 : 1;
   a.dynamic = (!q_tmem && a.n_fill > 0) ? 1u : 0u;
   a.scale = scale;
   a.mask_bits = mask_bits;
@@ -932,7 +958,7 @@ int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& 
   a.off_mask = a.off_staging + static_cast<uint32_t>(staging_bytes);
   a.off_bars = a.off_mask + static_cast<uint32_t>(fill_bytes);
   a.off_misc =
-      a.off_bars + 8u * static_cast<uint32_t>(3 * a.stages + 6 + 2 * kSchedDepth + a.lo_slots);
+      a.off_bars + 8u * static_cast<uint32_t>(3 * a.stages + 7 + 2 * kSchedDepth + a.lo_slots);
   const size_t smem = a.off_misc + 16 + 4 * kSchedDepth + 1024;
 
   CUtensorMap map_out, map_fill;
