@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
           static_cast<unsigned int>((blockIdx.x + 1ll) * n_lower / gridDim.x);
       auto fetch = [&]() -> unsigned int {
         if (dynamic) return atomicAdd(a.sched, 1u);
-        if (a.contig)
+        if (kF32 && a.contig)
           return static_next < static_end ? static_next++ : static_cast<unsigned int>(a.n_lower);
         const unsigned int v = static_next;
         static_next += gridDim.x;
@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
         decode_computed(r, a.causal, a.Tt2, ti, tj);
         const int outer = bh / a.nh_div, inner = bh - outer * a.nh_div;
         // Q in TMEM: a new row block first sends its Q chunks through the ring.
-        const bool new_q = a.q_tmem && (bh != q_bh || ti != q_ti);
+        const bool new_q = kF32 && a.q_tmem && (bh != q_bh || ti != q_ti);
         if (new_q) {
           q_bh = bh;
           q_ti = ti;
@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
           if (a.inject && !injected) {
             injected = true;  // withhold this CTA's first loads: its consumer's wait must run out
             issued &= ~(1u << stage);
-          } else if (a.q_tmem) {
+          } else if (kF32 && a.q_tmem) {
             // CTAs walk separate runs of the list here, so a K tile's later uses
             // come from other rows after much output has streamed through L2:
             // K is kept there (evict_last), Q is read once per row block.
