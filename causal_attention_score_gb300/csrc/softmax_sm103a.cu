@@ -73,12 +73,29 @@ constexpr uint32_t kIdesc = idesc_bf16_f32(kTile, kTile);
 constexpr int kSchedWords = 4;
 __device__ unsigned int g_softmax_sched[kSlots][kSchedWords];
 constexpr int kPrefetchK = 4;  // K tiles of the next unit prefetched into L2
+// Staging pairs per epilogue warp (at most) and K ring depth (at most).
+#ifndef CSA_SOFTMAX_MAX_PAIRS
+#define CSA_SOFTMAX_MAX_PAIRS 1
+#endif
+#ifndef CSA_SOFTMAX_MAX_STAGES
+#define CSA_SOFTMAX_MAX_STAGES 8
+#endif
+#ifndef CSA_SOFTMAX_ZERO_PACE
+#define CSA_SOFTMAX_ZERO_PACE 1
+#endif
+constexpr bool kZeroPace = CSA_SOFTMAX_ZERO_PACE != 0;  // pace the zero writer (zero_share_q16)
+constexpr uint32_t kZeroSlack = 2;                      // zero tiles ahead of the share
 
 struct SoftmaxArgs {
   int T, NH, BH, Tt;
   int kchunks, ksteps, stages;
   int n_units;
   int n_zero;  // zero tiles: BH * Tt * (Tt - 1) / 2
+  // Zero tiles per computed (lower) tile, 16.16 fixed point: a CTA's zero writer
+  // keeps its count within this share of the pass-1 tiles its epilogue has
+  // started (plus kZeroSlack), so the pool lasts through the launch instead of
+  // running dry while the later units' pass 1 leaves the SM with nothing to store.
+  uint32_t zero_share_q16;
   float scale_log2e;  // log2(e) / sqrt(HS)
   uint32_t tma_store;
   uint32_t pairs;  // staging pairs per epilogue warp (1 or 2)
@@ -128,6 +145,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Set while the epilogue is in pass 2 (storing), read by the zero writer.
   volatile int* epi_storing = reinterpret_cast<volatile int*>(gbase + a.off_misc + 8);
   auto ring_entry = [&](int s) { return base + a.off_misc + 16u + 4u * s; };
+  // Pass-1 tiles the epilogue has started, and set once it has no more units
+  // (the zero writer's pacing; see zero_share_q16).
+  volatile int* p1_started =
+      reinterpret_cast<volatile int*>(gbase + a.off_misc + 16u + 4u * kRingDepth);
+  volatile int* epi_done =
+      reinterpret_cast<volatile int*>(gbase + a.off_misc + 20u + 4u * kRingDepth);
   auto q_chunk = [&](int qb, int kc) { return base + qb * a.q_bytes + kc * kChunkBytes; };
   auto k_chunk = [&](int s, int kc) { return base + a.off_k + s * a.k_bytes + kc * kChunkBytes; };
   const uint32_t stats = base + a.off_stats;
@@ -154,6 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     *abort_flag = 0;
     *epi_storing = 0;
+    *p1_started = 0;
+    *epi_done = 0;
     fence_barrier_init();
   }
   if (a.tma_store) {
@@ -333,14 +358,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool vec = a.tma_store != 0;  // T % 4 == 0 and a 16-byte aligned output
     const uint64_t once = l2_policy_evict_first();
     const int Tt = a.Tt;
+    int taken = 0;
     bool ok = true;
     while (ok) {
-      // Yield to the epilogue while it stores (bounded: the epilogue leaves pass 2
-      // within the wait limit, or the CTA aborts).
+      // Yield to the epilogue while it stores, and keep within this CTA's share of
+      // zero tiles until its epilogue has no more units (bounded: the epilogue
+      // leaves pass 2, starts a unit or finishes within the wait limit, or the
+      // CTA aborts).
       int z = 0;
       if (lane == 0) {
         const uint64_t t0 = globaltimer_ns();
-        for (uint32_t it = 0; *epi_storing != 0; ++it) {
+        auto hold = [&]() {
+          if (*epi_storing != 0) return true;
+          if (!kZeroPace || *epi_done != 0) return false;
+          const uint32_t quota = static_cast<uint32_t>(
+              (static_cast<unsigned long long>(*p1_started) * a.zero_share_q16) >> 16);
+          return static_cast<uint32_t>(taken) >= quota + kZeroSlack;
+        };
+        for (uint32_t it = 0; hold(); ++it) {
           if (*abort_flag) {
             ok = false;
             break;
@@ -357,6 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       z = __shfl_sync(0xffffffffu, z, 0);
       if (z >= a.n_zero) break;
+      ++taken;
       // Zero tile z: (b, h) = z % BH, then the strictly upper tile (i, j), j > i,
       // numbered by pairing block rows i and Tt - 2 - i (Tt tiles per pair).
       const int w = z / a.BH;
@@ -424,6 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int bh, ti;
       decode_unit(cur, a, bh, ti);
+      if (ew == 0 && lane == 0) *p1_started = *p1_started + ti + 1;
       const int row0 = ti * kTile + q * 32;
       const int r = row0 + static_cast<int>(lane);
       // The unit's 2n tiles (pass 1: tj = 0..ti, then pass 2 over the same tiles)
@@ -619,7 +656,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ew == 0 && lane == 0) *epi_storing = 0;
       if (!ok) break;
     }
-    if (ew == 0 && lane == 0) *epi_storing = 0;
+    if (ew == 0 && lane == 0) {
+      *epi_storing = 0;
+      *epi_done = 1;
+    }
     if (lane == 0) bulk_wait_all();
     __syncwarp();
   }
@@ -672,6 +712,8 @@ int softmax_launch(float* out, const void* qkv, int B, int T, int C, int NH, cud
   a.ksteps = (HS + 15) / 16;
   a.n_units = static_cast<int>(BH * Tt);
   a.n_zero = static_cast<int>(BH * Tt * (Tt - 1) / 2);
+  a.zero_share_q16 = static_cast<uint32_t>((static_cast<unsigned long long>(Tt - 1) << 16) /
+                                           static_cast<unsigned long long>(Tt + 1));
   a.scale_log2e = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(HS)));
   a.tma_store = (T % 4 == 0 && reinterpret_cast<uintptr_t>(out) % 16 == 0) ? 1u : 0u;
   a.out = out;
@@ -682,14 +724,15 @@ int softmax_launch(float* out, const void* qkv, int B, int T, int C, int NH, cud
   // Shared memory: Q (2 buffers) | K ring | staging | zero box | stats | barriers | misc.
   a.q_bytes = static_cast<uint32_t>(a.kchunks) * kChunkBytes;
   a.k_bytes = a.q_bytes;
-  // Two staging pairs per epilogue warp when that still leaves two K stages.
+  // The most staging pairs per epilogue warp (up to CSA_SOFTMAX_MAX_PAIRS) that
+  // still leave two K stages; the rest of shared memory deepens the K ring.
   int staging_bytes = 0;
-  for (int pairs = 2; pairs >= 1; --pairs) {
+  for (int pairs = CSA_SOFTMAX_MAX_PAIRS; pairs >= 1; --pairs) {
     staging_bytes = kEpiWarps * pairs * kPairBytes;
     const int fixed = 2 * static_cast<int>(a.q_bytes) + staging_bytes + kZeroBytes + kStatsBytes +
                       1024 + 1024;
     a.pairs = static_cast<uint32_t>(pairs);
-    a.stages = std::min(4, (dev.max_smem_optin - fixed) / static_cast<int>(a.k_bytes));
+    a.stages = std::min(CSA_SOFTMAX_MAX_STAGES, (dev.max_smem_optin - fixed) / static_cast<int>(a.k_bytes));
     if (a.stages >= 2) break;
   }
   if (a.stages < 2) {
@@ -702,7 +745,7 @@ int softmax_launch(float* out, const void* qkv, int B, int T, int C, int NH, cud
   a.off_stats = a.off_zero + kZeroBytes;
   a.off_bars = a.off_stats + kStatsBytes;
   a.off_misc = a.off_bars + 8u * static_cast<uint32_t>(10 + 2 * a.stages + 2 * kRingDepth);
-  const size_t smem = a.off_misc + 16 + 4 * kRingDepth + 1024;
+  const size_t smem = a.off_misc + 16 + 4 * kRingDepth + 8 + 1024;
 
   CUtensorMap map_qkv, map_out, map_zero;
   {
