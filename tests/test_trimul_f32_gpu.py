@@ -145,3 +145,44 @@ def test_trimul_f32_gpt2_full_size(oracle_lib):
         err = np.abs(got[i, :t + 1] - ref[i, :t + 1])
         assert float(err.max()) <= 1e-4, (b, h, t, float(err.max()))
         assert np.all(err <= F32_REL * ref_abs[i, :t + 1] + 1e-30), (b, h, t)
+
+
+@pytest.mark.parametrize("B,T,NH,HS", [
+    (2, 1024, 8, 128),   # Q in TMEM, one buffer, 4 chunks
+    (1, 1024, 20, 96),   # Q in TMEM, one buffer, 3 chunks
+    (1, 1000, 24, 64),   # Q in TMEM, two buffers, ragged T
+    (1, 1024, 4, 160),   # HS > 128: Q and K chunks through the ring
+])
+def test_trimul_f32_many_row_blocks_per_cta(oracle_lib, B, T, NH, HS):
+    """Enough tiles that every CTA walks several row blocks, so Q is reloaded (and, with
+    two buffers, alternates) many times: the mask everywhere, sampled rows on both sides
+    of every row-block edge within the 3 x tf32 bound, and lower-only equal bit for bit on
+    and below the diagonal with nothing written above it."""
+    shape, qkv = _case(B, T, NH, HS, seed=T + HS)
+    out = poisoned(shape.out_shape)
+    csa.trimul_forward_f32(out, qkv.cuda(), B, T, shape.C, NH)
+    torch.cuda.synchronize()
+    assert csa.get_status() == 0
+    upper = torch.triu(torch.ones((T, T), dtype=torch.bool, device="cuda"), diagonal=1)
+    bits = out.view(torch.int32)
+    assert bool(torch.all(bits[..., upper] == NAN_BITS))
+    assert bool(torch.all(torch.isfinite(out[..., ~upper])))
+    rng = np.random.default_rng(T * HS)
+    edges = sorted({0, T - 1, *range(127, T, 128), *range(128, T, 128)})
+    bht = np.array([(b, h, t) for b in range(B) for h in range(NH)
+                    for t in sorted(set(edges[:: max(1, len(edges) // 6)]) |
+                                    set(rng.integers(0, T, size=3).tolist()))],
+                   dtype=np.int64)
+    x = qkv.numpy().reshape(-1)
+    ref = oracle_lib.trimul_f32_rows(x, B, T, shape.C, NH, bht, 0)
+    ref_abs = oracle_lib.trimul_f32_rows(np.abs(x), B, T, shape.C, NH, bht, 0)
+    got = out[torch.from_numpy(bht[:, 0]).cuda(), torch.from_numpy(bht[:, 1]).cuda(),
+              torch.from_numpy(bht[:, 2]).cuda()].cpu().numpy()
+    _check_f32_bound(got, ref, ref_abs, f"f32 rows {(B, T, NH, HS)}")
+    out2 = poisoned(shape.out_shape)
+    csa.trimul_forward_f32(out2, qkv.cuda(), B, T, shape.C, NH, lower_only=True)
+    torch.cuda.synchronize()
+    assert csa.get_status() == 0
+    bits2 = out2.view(torch.int32)
+    assert bool(torch.all(bits2[..., upper] == POISON_BITS - (1 << 32)))  # as int32
+    assert bool(torch.equal(bits2[..., ~upper], bits[..., ~upper]))
