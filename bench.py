@@ -357,6 +357,21 @@ def make_workload(name, dev):
                       "I=768, H=3072", {"dense_sweep": {"calls": len(xs_h), "I": I, "H": H}},
                       parts, flops, {"part": None, "kernel": "dense_sm103a_kernel",
                                      "bound": "tensor", "per_launch": flops}, h2d, outs)
+    if name == "dense_sweep_grouped":
+        # The same 32 problems as dense_sweep, in one dense_xwt_grouped launch per step.
+        xs_h, W_h = synth.dense_sweep_inputs(seed=0)
+        W = W_h.to(dev)
+        H, I = W_h.shape
+        Xs = [X_h.to(dev) for X_h in xs_h]
+        Ys = [torch.empty((X.shape[0], H), dtype=torch.float32, device=dev) for X in Xs]
+        flops = sum(dense_flops(X.shape[0], I, H) for X in Xs)
+        fn = lambda st: csa.dense_xwt_grouped(Ys, Xs, W, I, H, stream=st)
+        return finish("dense dynamic-shape sweep, grouped: the same 32 problems (M = 16*T, "
+                      "T ~ U{1..128}, seed 0, I=768, H=3072) in one dense_xwt_grouped launch",
+                      {"dense_sweep": {"calls": len(xs_h), "I": I, "H": H, "grouped": True}},
+                      [("grouped", fn)], flops,
+                      {"part": 0, "kernel": "dense_sm103a_kernel<true>", "bound": "tensor",
+                       "per_launch": flops}, [(W, W_h)] + list(zip(Xs, xs_h)), Ys)
     if name == "bmm_nt":
         bs = synth.BMM_NT_RAGGED
         X_h, W_h = synth.bmm_input(bs, seed=0)
@@ -374,7 +389,8 @@ def make_workload(name, dev):
 
 
 WORKLOADS = ["step", "trimul_gpt2", "trimul_long", "trimul_gpt2_lower", "trimul_long_lower",
-             "dense_ragged", "dense_sweep", "bmm_nt", "softmax_gpt2", "softmax_long",
+             "dense_ragged", "dense_sweep", "dense_sweep_grouped", "bmm_nt", "softmax_gpt2",
+             "softmax_long",
              "trimul_f32_gpt2", "trimul_f32_long"]
 
 

@@ -16,12 +16,13 @@ from ._lib import (CSA_ERR_ALIGN, CSA_ERR_ARCH, CSA_ERR_CUDA, CSA_ERR_LAUNCH, CS
                    CSA_ERR_SHAPE, CSA_ERR_TIMEOUT, CSA_ERR_UNSUPPORTED, CSA_MASK_NAN,
                    CSA_MASK_NEG_INF, CSA_OK, CsaError)
 from .ops import (DENSE_FETCH_AUTO, DENSE_FETCH_LOADERS, batch_matmul_nt, causal_softmax,
-                  causal_softmax_forward, debug_inject, dense, dense_xwt, get_status,
+                  causal_softmax_forward, debug_inject, dense, dense_xwt, dense_xwt_grouped,
+                  get_status,
                   set_dense_fetch, set_wait_limit_ns, trimul, trimul_forward, trimul_forward_f32,
                   version)
 
 __all__ = [
-    "trimul_forward", "trimul_forward_f32", "dense_xwt", "batch_matmul_nt", "causal_softmax_forward",
+    "trimul_forward", "trimul_forward_f32", "dense_xwt", "dense_xwt_grouped", "batch_matmul_nt", "causal_softmax_forward",
     "causal_softmax", "trimul", "dense", "get_status", "set_wait_limit_ns",
     "debug_inject", "set_dense_fetch", "DENSE_FETCH_AUTO", "DENSE_FETCH_LOADERS", "version", "CsaError", "CSA_OK", "CSA_ERR_NULL", "CSA_ERR_SHAPE",
     "CSA_ERR_ALIGN", "CSA_ERR_UNSUPPORTED", "CSA_ERR_ARCH", "CSA_ERR_LAUNCH", "CSA_ERR_TIMEOUT",

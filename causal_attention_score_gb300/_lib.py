@@ -39,6 +39,7 @@ SIGNATURES = {
     "batch_matmul_nt": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "causal_softmax_forward": (_i, [_vp, _vp, _i, _i, _i, _i, _vp]),
     "dense_xwt_ex": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp]),
+    "dense_xwt_grouped": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp]),
     "csa_get_status": (_i, [_vp]),
     "csa_status_string": (ctypes.c_char_p, [_i]),
     "csa_last_error": (ctypes.c_char_p, []),

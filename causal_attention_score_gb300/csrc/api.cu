@@ -373,6 +373,34 @@ csa_status dense_xwt(float* Y, const void* X, const void* W, int M, int I, int H
   return dense_xwt_ex(Y, X, W, M, I, H, nullptr);
 }
 
+csa_status dense_xwt_grouped(float* const* Y, const void* const* X, const void* W, const int* M,
+                             int n, int I, int H, void* stream) {
+  t_last_error.clear();
+  if (!Y || !X || !W || !M) return set_error(CSA_ERR_NULL, "dense_xwt_grouped: null pointer");
+  if (n <= 0 || I <= 0 || H <= 0)
+    return set_error(CSA_ERR_SHAPE, "dense_xwt_grouped: n, I, H must be >= 1");
+  if (reinterpret_cast<uintptr_t>(W) % 2)
+    return set_error(CSA_ERR_ALIGN, "dense_xwt_grouped: W needs 2-byte alignment");
+  for (int g = 0; g < n; ++g) {
+    if (!Y[g] || !X[g])
+      return set_error(CSA_ERR_NULL, "dense_xwt_grouped: null pointer in problem " +
+                                         std::to_string(g));
+    if (M[g] <= 0)
+      return set_error(CSA_ERR_SHAPE, "dense_xwt_grouped: M[" + std::to_string(g) +
+                                          "] must be >= 1");
+    if (reinterpret_cast<uintptr_t>(X[g]) % 2 || reinterpret_cast<uintptr_t>(Y[g]) % 4)
+      return set_error(CSA_ERR_ALIGN, "dense_xwt_grouped: X[" + std::to_string(g) +
+                                          "] needs 2-byte and Y 4-byte alignment");
+  }
+  DeviceInfo dev;
+  std::string err;
+  int rc = current_device(dev, err);
+  if (rc != CSA_OK) return set_error(rc, err);
+  rc = dense_grouped_launch(Y, X, W, M, n, I, H, static_cast<cudaStream_t>(stream), dev, err);
+  if (rc != CSA_OK) return set_error(rc, err);
+  return CSA_OK;
+}
+
 csa_status csa_get_status(void* stream) {
   t_last_error.clear();
   DeviceInfo dev;

@@ -83,4 +83,8 @@ int softmax_launch(float* out, const void* qkv, int B, int T, int C, int NH, cud
 int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
                  cudaStream_t stream, const DeviceInfo& dev, std::string& err);
 
+int dense_grouped_launch(float* const* Y, const void* const* X, const void* W, const int* M, int n,
+                         int I, int H, cudaStream_t stream, const DeviceInfo& dev,
+                         std::string& err);
+
 }  // namespace csa

@@ -75,6 +75,23 @@ struct DenseArgs {
   uint32_t stage_bytes, off_staging, off_bars, off_misc, tmem_cols;
 };
 
+// Grouped launch: up to kMaxGroup problems Y[g] = X[g] W^T that share W, I and
+// H, one persistent launch over all their tiles. The per-problem tensor maps
+// travel in the kernel parameters (nothing to allocate, so a grouped call can be
+// captured in a CUDA graph).
+constexpr int kMaxGroup = 48;
+template <bool kGrouped>
+struct DenseGroup {};  // one problem: everything is in DenseArgs and the three maps
+template <>
+struct DenseGroup<true> {
+  CUtensorMap x[kMaxGroup];     // X[g] as (I, M[g]), 64 x 128 boxes
+  CUtensorMap y[kMaxGroup];     // Y[g] as (H, M[g]), 32 x 32 boxes (TMA store form)
+  float* Y[kMaxGroup];
+  int M[kMaxGroup];
+  int mt_start[kMaxGroup + 1];  // first m-tile of problem g in the launch; [n] = all
+  int n;
+};
+
 template <bool kPair>
 __device__ __forceinline__ uint32_t load_pair(const uint16_t* row, int k, int I) {
   if (kPair) {
@@ -131,10 +148,12 @@ __device__ __forceinline__ void issue_block_async(const uint16_t* src, int nrows
   }
 }
 
+template <bool kGrouped>
 __global__ void __launch_bounds__(kThreads, 1)
     dense_sm103a_kernel(const __grid_constant__ CUtensorMap tmap_x,
                         const __grid_constant__ CUtensorMap tmap_w,
-                        const __grid_constant__ CUtensorMap tmap_y, const DenseArgs a) {
+                        const __grid_constant__ CUtensorMap tmap_y, const DenseArgs a,
+                        const __grid_constant__ DenseGroup<kGrouped> g) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -155,6 +174,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto b_tile = [&](int s) { return base + s * a.stage_bytes + kBM * 128u; };
 
   const Watchdog wd{a.wait_limit_ns, a.status, abort_flag};
+
+  // Tile t of the launch, n-major (CTAs working at the same time share W's n-tile):
+  // problem p, its m-tile mb, the n-tile nb. In a group the m-tiles of all
+  // problems follow one another.
+  auto locate = [&](long long t, int& p, int& mb, int& nb) {
+    if constexpr (kGrouped) {
+      const int total = g.mt_start[g.n];
+      const int mt = static_cast<int>(t % total);
+      nb = static_cast<int>(t / total);
+      int lo = 0, hi = g.n - 1;  // the last problem whose first m-tile is <= mt
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (g.mt_start[mid] <= mt) lo = mid;
+        else hi = mid - 1;
+      }
+      p = lo;
+      mb = mt - g.mt_start[lo];
+    } else {
+      p = 0;
+      mb = static_cast<int>(t % a.m_tiles);
+      nb = static_cast<int>(t / a.m_tiles);
+    }
+  };
+  auto map_x = [&](int p) -> const CUtensorMap* {
+    if constexpr (kGrouped) return &g.x[p];
+    else return &tmap_x;
+  };
+  auto map_y = [&](int p) -> const CUtensorMap* {
+    if constexpr (kGrouped) return &g.y[p];
+    else return &tmap_y;
+  };
+  auto rows_of = [&](int p) -> int {
+    if constexpr (kGrouped) return g.M[p];
+    else return a.M;
+  };
+  auto y_of = [&](int p) -> float* {
+    if constexpr (kGrouped) return g.Y[p];
+    else return a.Y;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
@@ -186,7 +244,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ Fetch --
     if (a.tma_load) {
       if (warp == 0 && lane == 0) {
-        tma_prefetch_map(&tmap_x);
+        if constexpr (kGrouped) {
+          for (int i = 0; i < g.n; ++i) tma_prefetch_map(&g.x[i]);
+        } else {
+          tma_prefetch_map(&tmap_x);
+        }
         tma_prefetch_map(&tmap_w);
         int stage = 0;
         uint32_t phase = 0;
@@ -194,8 +256,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tx = static_cast<uint32_t>(kBM + a.BN) * 128u;
         for (long long tile = blockIdx.x; tile < a.num_tiles && !*abort_flag;
              tile += gridDim.x) {
-          const int mb = static_cast<int>(tile % a.m_tiles);
-          const int nb = static_cast<int>(tile / a.m_tiles);
+          int p, mb, nb;
+          locate(tile, p, mb, nb);
+          const CUtensorMap* mx = map_x(p);
           bool ok = true;
           for (int kb = 0; kb < a.kblocks; ++kb) {
             if (!mbar_wait(empty_bar(stage), phase ^ 1u, wd, kSiteProducerEmpty)) {
@@ -206,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (a.inject && tile == blockIdx.x && kb == 0) {
               issued &= ~(1u << stage);  // withheld: the MMA warp's wait must run out
             } else {
-              tma_load_2d(a_tile(stage), &tmap_x, full_bar(stage), kb * kBK, mb * kBM);
+              tma_load_2d(a_tile(stage), mx, full_bar(stage), kb * kBK, mb * kBM);
               tma_load_2d(b_tile(stage), &tmap_w, full_bar(stage), kb * kBK, nb * a.BN);
               issued |= 1u << stage;
               issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -228,6 +291,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+    } else if (kGrouped) {
+      // (a group is always fetched by TMA)
     } else if (a.vec2) {
       // Asynchronous copies, kept up to `depth` stages ahead: a stage is handed to
       // the MMA warp (proxy fence + arrive) once this warp's copies into it have
@@ -356,8 +421,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t buf = 0;
     const int chunks = a.BN / 32;
     for (long long tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
-      const int mb = static_cast<int>(tile % a.m_tiles);
-      const int nb = static_cast<int>(tile / a.m_tiles);
+      int p, mb, nb;
+      locate(tile, p, mb, nb);
+      const int M = rows_of(p);
       if (!mbar_wait_warp(tfull_bar(acc), acc_phase, wd, kSiteEpilogueFull)) break;
       tc_fence_after_sync();
       const uint32_t tcol = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
@@ -372,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(tempty_bar(acc));
         }
         const int col0 = nb * a.BN + c * 32;
-        if (row0 >= a.M || col0 >= a.H) continue;
+        if (row0 >= M || col0 >= a.H) continue;
         if (lane == 0) bulk_wait_read<kStoreBufs - 1>();
         __syncwarp();
         const uint32_t box = staging + buf * kBoxBytes;
@@ -382,16 +448,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmap_y, box, col0, row0);
+            tma_store_2d(map_y(p), box, col0, row0);
             bulk_commit();
           }
         } else {
           __syncwarp();
           const int col = col0 + static_cast<int>(lane);
-          float* ycol = a.Y + static_cast<size_t>(row0) * a.H + col;
+          float* ycol = y_of(p) + static_cast<size_t>(row0) * a.H + col;
           for (int rr = 0; rr < 32; ++rr) {
             const uint32_t val = staged_elem_sw128(box, static_cast<uint32_t>(rr), lane);
-            if (row0 + rr < a.M && col < a.H)
+            if (row0 + rr < M && col < a.H)
               ycol[static_cast<size_t>(rr) * a.H] = __uint_as_float(val);
           }
         }
@@ -502,13 +568,13 @@ int scratch_pool(int device, cudaMemPool_t* out, std::string& err) {
 }
 
 // Tile width along H: the largest BN whose wave count times tile cost is
-// smallest (tile cost ~ BN plus a fixed per-tile overhead).
-int choose_bn(int M, int H, int sms) {
-  const int m_tiles = (M + kBM - 1) / kBM;
+// smallest (tile cost ~ BN plus a fixed per-tile overhead), for m_tiles rows of
+// 128-row tiles.
+int choose_bn_tiles(long long m_tiles, int H, int sms) {
   int best = 64;
   long long best_cost = -1;
   for (int bn : {256, 128, 64}) {
-    const long long tiles = static_cast<long long>(m_tiles) * ((H + bn - 1) / bn);
+    const long long tiles = m_tiles * ((H + bn - 1) / bn);
     const long long waves = (tiles + sms - 1) / sms;
     const long long cost = waves * (bn + 32);
     if (best_cost < 0 || cost < best_cost) {
@@ -517,6 +583,26 @@ int choose_bn(int M, int H, int sms) {
     }
   }
   return best;
+}
+
+int choose_bn(int M, int H, int sms) { return choose_bn_tiles((M + kBM - 1) / kBM, H, sms); }
+
+// Shared-memory plan for BN: ring stages, then staging, barriers and misc.
+int plan_smem(DenseArgs& a, const DeviceInfo& dev, std::string& err, size_t& smem) {
+  a.stage_bytes = static_cast<uint32_t>(kBM + a.BN) * 128u;
+  const int fixed = kStagingBytes + 1024 + 1024;
+  a.stages = std::min(CSA_DENSE_MAX_STAGES,
+                      (dev.max_smem_optin - fixed) / static_cast<int>(a.stage_bytes));
+  a.load_depth = std::min(a.stages, 4);
+  if (a.stages < 2) {
+    err = "dense_xwt: not enough shared memory";
+    return CSA_ERR_UNSUPPORTED;
+  }
+  a.off_staging = static_cast<uint32_t>(a.stages) * a.stage_bytes;
+  a.off_bars = a.off_staging + kStagingBytes;
+  a.off_misc = a.off_bars + 8u * static_cast<uint32_t>(2 * a.stages + 5);
+  smem = a.off_misc + 16 + 1024;
+  return CSA_OK;
 }
 
 }  // namespace
@@ -579,19 +665,11 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
   a.inject = take_inject() ? 1 : 0;
   a.tmem_cols = static_cast<uint32_t>(2 * a.BN);
 
-  a.stage_bytes = static_cast<uint32_t>(kBM + a.BN) * 128u;
-  const int fixed = kStagingBytes + 1024 + 1024;
-  a.stages = std::min(CSA_DENSE_MAX_STAGES,
-                      (dev.max_smem_optin - fixed) / static_cast<int>(a.stage_bytes));
-  a.load_depth = std::min(a.stages, 4);
-  if (a.stages < 2) {
-    err = "dense_xwt: not enough shared memory";
-    return release(CSA_ERR_UNSUPPORTED);
+  size_t smem = 0;
+  {
+    const int rc = plan_smem(a, dev, err, smem);
+    if (rc != CSA_OK) return release(rc);
   }
-  a.off_staging = static_cast<uint32_t>(a.stages) * a.stage_bytes;
-  a.off_bars = a.off_staging + kStagingBytes;
-  a.off_misc = a.off_bars + 8u * static_cast<uint32_t>(2 * a.stages + 5);
-  const size_t smem = a.off_misc + 16 + 1024;
 
   CUtensorMap map_x, map_w, map_y;
   std::memset(&map_x, 0, sizeof map_x);
@@ -620,7 +698,7 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
   }
 
   {
-    int rc = set_max_dynamic_smem(reinterpret_cast<const void*>(dense_sm103a_kernel),
+    int rc = set_max_dynamic_smem(reinterpret_cast<const void*>(dense_sm103a_kernel<false>),
                                   static_cast<int>(smem), dev.device, err);
     if (rc != CSA_OK) {
       err = "dense_xwt: " + err;
@@ -645,14 +723,122 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
     }
   }
   const long long grid = std::min<long long>(a.num_tiles, dev.sm_count);
-  e = launch_programmatic(dense_sm103a_kernel, static_cast<unsigned>(grid), kThreads, smem, stream,
-                          map_x, map_w, map_y, a);
+  e = launch_programmatic(dense_sm103a_kernel<false>, static_cast<unsigned>(grid), kThreads, smem,
+                          stream, map_x, map_w, map_y, a, DenseGroup<false>{});
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     err = std::string("dense_xwt: launch: ") + cudaGetErrorString(e);
     return release(CSA_ERR_LAUNCH);
   }
   return release(CSA_OK);
+}
+
+}  // namespace csa
+
+namespace csa {
+
+// Y[g] = X[g] W^T for g < n: launches of up to kMaxGroup problems each when the
+// rows of every X[g] and of W can be described by tensor maps (I * 2 % 16 == 0,
+// 16-byte aligned), else one dense_launch per problem.
+int dense_grouped_launch(float* const* Y, const void* const* X, const void* W, const int* M, int n,
+                         int I, int H, cudaStream_t stream, const DeviceInfo& dev,
+                         std::string& err) {
+  bool tma_rows = (static_cast<long long>(I) * 2) % 16 == 0 &&
+                  reinterpret_cast<uintptr_t>(W) % 16 == 0;
+  bool tma_store = (static_cast<long long>(H) * 4) % 16 == 0;
+  for (int i = 0; i < n; ++i) {
+    tma_rows = tma_rows && reinterpret_cast<uintptr_t>(X[i]) % 16 == 0;
+    tma_store = tma_store && reinterpret_cast<uintptr_t>(Y[i]) % 16 == 0;
+  }
+  if (!tma_rows) {
+    for (int i = 0; i < n; ++i) {
+      const int rc = dense_launch(Y[i], X[i], W, M[i], I, H, stream, dev, err);
+      if (rc != CSA_OK) return rc;
+    }
+    return CSA_OK;
+  }
+  CUtensorMap map_w;  // W's box depends on BN, chosen per launch below
+  static thread_local DenseGroup<true> grp;  // 13 KB: kept off the stack
+  for (int first = 0; first < n; first += kMaxGroup) {
+    const int cnt = std::min(kMaxGroup, n - first);
+    std::memset(&grp, 0, sizeof grp);
+    grp.n = cnt;
+    long long total = 0;
+    for (int i = 0; i < cnt; ++i) {
+      grp.mt_start[i] = static_cast<int>(total);
+      grp.M[i] = M[first + i];
+      grp.Y[i] = Y[first + i];
+      total += (M[first + i] + kBM - 1) / kBM;
+    }
+    if (total >= (1LL << 30)) {
+      err = "dense_xwt_grouped: too many row tiles in one group";
+      return CSA_ERR_SHAPE;
+    }
+    grp.mt_start[cnt] = static_cast<int>(total);
+
+    DenseArgs a{};
+    a.M = 0;  // per problem: grp.M
+    a.I = I;
+    a.H = H;
+    a.BN = choose_bn_tiles(total, H, dev.sm_count);
+    a.m_tiles = static_cast<int>(total);
+    a.n_tiles = (H + a.BN - 1) / a.BN;
+    a.kblocks = (I + kBK - 1) / kBK;
+    a.num_tiles = total * a.n_tiles;
+    a.tma_load = 1u;
+    a.tma_store = tma_store ? 1u : 0u;
+    a.vec2 = 0u;
+    a.idesc = idesc_bf16_f32(kBM, a.BN);
+    a.X = nullptr;
+    a.W = static_cast<const uint16_t*>(W);
+    a.Y = nullptr;
+    a.status = dev.status_word;
+    a.wait_limit_ns = wait_limit_ns();
+    a.inject = take_inject() ? 1 : 0;
+    a.tmem_cols = static_cast<uint32_t>(2 * a.BN);
+    size_t smem = 0;
+    int rc = plan_smem(a, dev, err, smem);
+    if (rc != CSA_OK) return rc;
+
+    const uint64_t st_in[1] = {static_cast<uint64_t>(I) * 2};
+    const uint32_t bx[2] = {kBK, kBM};
+    const uint32_t bw[2] = {kBK, static_cast<uint32_t>(a.BN)};
+    const uint64_t dw[2] = {static_cast<uint64_t>(I), static_cast<uint64_t>(H)};
+    rc = encode_tiled(&map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, dw, st_in, bw,
+                      CU_TENSOR_MAP_SWIZZLE_128B, err);
+    if (rc != CSA_OK) return rc;
+    for (int i = 0; i < cnt; ++i) {
+      const uint64_t dx[2] = {static_cast<uint64_t>(I), static_cast<uint64_t>(grp.M[i])};
+      rc = encode_tiled(&grp.x[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X[first + i], dx, st_in,
+                        bx, CU_TENSOR_MAP_SWIZZLE_128B, err);
+      if (rc != CSA_OK) return rc;
+      if (a.tma_store) {
+        const uint64_t dy[2] = {static_cast<uint64_t>(H), static_cast<uint64_t>(grp.M[i])};
+        const uint64_t sy[1] = {static_cast<uint64_t>(H) * 4};
+        const uint32_t by[2] = {32, 32};
+        rc = encode_tiled(&grp.y[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, grp.Y[i], dy, sy, by,
+                          CU_TENSOR_MAP_SWIZZLE_128B, err);
+        if (rc != CSA_OK) return rc;
+      }
+    }
+    rc = set_max_dynamic_smem(reinterpret_cast<const void*>(dense_sm103a_kernel<true>),
+                              static_cast<int>(smem), dev.device, err);
+    if (rc != CSA_OK) {
+      err = "dense_xwt_grouped: " + err;
+      return rc;
+    }
+    CUtensorMap unused;
+    std::memset(&unused, 0, sizeof unused);
+    const long long grid = std::min<long long>(a.num_tiles, dev.sm_count);
+    cudaError_t e = launch_programmatic(dense_sm103a_kernel<true>, static_cast<unsigned>(grid),
+                                        kThreads, smem, stream, unused, map_w, unused, a, grp);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) {
+      err = std::string("dense_xwt_grouped: launch: ") + cudaGetErrorString(e);
+      return CSA_ERR_LAUNCH;
+    }
+  }
+  return CSA_OK;
 }
 
 }  // namespace csa

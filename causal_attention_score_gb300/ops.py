@@ -74,6 +74,31 @@ def dense_xwt(Y: torch.Tensor, X: torch.Tensor, W: torch.Tensor, M: int, I: int,
     _lib.check(rc, "dense_xwt")
 
 
+def dense_xwt_grouped(Ys, Xs, W: torch.Tensor, I: int, H: int, stream=None) -> None:
+    """Y[g] = X[g] W^T for every g, one launch per 48 problems: fp32 Y[g] [M_g, H] from
+    bf16 X[g] [M_g, I] and the shared W [H, I]; see dense_xwt_grouped in include/csa.h."""
+    import ctypes
+    if len(Ys) != len(Xs) or not Xs:
+        raise ValueError("Ys and Xs must be non-empty lists of the same length")
+    _need(W, "W", torch.bfloat16, H * I)
+    Ms = []
+    for g, (Y, X) in enumerate(zip(Ys, Xs)):
+        if X.dim() != 2 or X.shape[1] != I:
+            raise ValueError(f"X[{g}] must be [M, {I}]")
+        M = int(X.shape[0])
+        _need(X, f"X[{g}]", torch.bfloat16, M * I)
+        _need(Y, f"Y[{g}]", torch.float32, M * H)
+        Ms.append(M)
+    n = len(Xs)
+    y_arr = (ctypes.c_void_p * n)(*[Y.data_ptr() for Y in Ys])
+    x_arr = (ctypes.c_void_p * n)(*[X.data_ptr() for X in Xs])
+    m_arr = (ctypes.c_int * n)(*Ms)
+    rc = _lib.load().dense_xwt_grouped(ctypes.addressof(y_arr), ctypes.addressof(x_arr),
+                                       W.data_ptr(), ctypes.addressof(m_arr), n, I, H,
+                                       _stream_ptr(stream))
+    _lib.check(rc, "dense_xwt_grouped")
+
+
 def batch_matmul_nt(Y: torch.Tensor, X: torch.Tensor, W: torch.Tensor, batch: int, T1: int,
                     T2: int, D: int, stream=None) -> None:
     """Y[i, j, k] = sum_l X[i, j, l] W[i, k, l]: bf16 X [batch, T1, D], W [batch, T2, D]

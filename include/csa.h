@@ -178,6 +178,25 @@ csa_status dense_xwt_ex(float* Y, const void* X, const void* W, int M, int I, in
                         void* stream);
 
 /*
+ * dense_xwt_grouped -- Y[g] = X[g] W^T for g = 0 .. n-1, asynchronous on `stream`:
+ * n dense layers that share W (device, bf16, [H, I]), I and H, computed by one
+ * persistent launch over all their tiles (one launch per 48 problems), so that
+ * a batch of dynamic-shape calls costs one launch instead of n.
+ *   Y  host array of n device pointers: Y[g] fp32 [M[g], H] row-major, fully
+ *      overwritten.
+ *   X  host array of n device pointers: X[g] bf16 [M[g], I] row-major.
+ *   M  host array of n row counts, each >= 1.
+ * The host arrays are read during the call only. Results are bit-identical to n
+ * dense_xwt calls. When I * 2 is not a multiple of 16, or W or some X[g] is not
+ * 16-byte aligned, the call makes n dense_xwt launches instead. Alignment: X[g]
+ * and W 2-byte, Y[g] 4-byte (Y written by TMA when H * 4 % 16 == 0 and every Y[g]
+ * is 16-byte aligned). CSA_ERR_NULL / CSA_ERR_SHAPE / CSA_ERR_ALIGN name the first
+ * offending problem; nothing is launched then.
+ */
+csa_status dense_xwt_grouped(float* const* Y, const void* const* X, const void* W, const int* M,
+                             int n, int I, int H, void* stream);
+
+/*
  * csa_set_dense_fetch -- process-wide fetch mode of dense_xwt for rows that no
  * tensor map can describe (I*2 not a multiple of 16, or X / W not 16-byte
  * aligned):

@@ -146,3 +146,42 @@ def test_no_device_for_the_other_entry_points(lib):
     assert lib.trimul_forward_f32(1024, 1024, 1, 64, 128, 2, 0, 0, None) == _lib.CSA_ERR_CUDA
     assert lib.causal_softmax_forward(1024, 1024, 1, 64, 128, 2, None) == _lib.CSA_ERR_CUDA
     assert lib.batch_matmul_nt(1024, 1024, 1024, 2, 8, 8, 64, None) == _lib.CSA_ERR_CUDA
+
+
+def _grouped_args(ys, xs, ms):
+    n = len(ms)
+    y = (ctypes.c_void_p * n)(*ys)
+    x = (ctypes.c_void_p * n)(*xs)
+    m = (ctypes.c_int * n)(*ms)
+    return y, x, m
+
+
+@pytest.mark.parametrize("ys,xs,ms,n,code", [
+    ([1024, 2048], [1024, 2048], [4, 4], 0, _lib.CSA_ERR_SHAPE),        # n = 0
+    ([1024, None], [1024, 2048], [4, 4], 2, _lib.CSA_ERR_NULL),         # Y[1] null
+    ([1024, 2048], [None, 2048], [4, 4], 2, _lib.CSA_ERR_NULL),         # X[0] null
+    ([1024, 2048], [1024, 2048], [4, 0], 2, _lib.CSA_ERR_SHAPE),        # M[1] = 0
+    ([1024, 2050], [1024, 2048], [4, 4], 2, _lib.CSA_ERR_ALIGN),        # Y[1] 2-byte aligned
+    ([1024, 2048], [1024, 2049], [4, 4], 2, _lib.CSA_ERR_ALIGN),        # X[1] odd address
+])
+def test_dense_grouped_argument_errors(lib, ys, xs, ms, n, code):
+    y, x, m = _grouped_args(ys, xs, ms)
+    rc = lib.dense_xwt_grouped(ctypes.addressof(y), ctypes.addressof(x), 4096,
+                               ctypes.addressof(m), n, 8, 8, None)
+    assert rc == code
+    assert lib.csa_last_error()
+
+
+def test_dense_grouped_null_arrays_and_no_device(lib):
+    y, x, m = _grouped_args([1024], [2048], [4])
+    assert lib.dense_xwt_grouped(None, ctypes.addressof(x), 4096, ctypes.addressof(m), 1, 8, 8,
+                                 None) == _lib.CSA_ERR_NULL
+    assert lib.dense_xwt_grouped(ctypes.addressof(y), ctypes.addressof(x), 4096, None, 1, 8, 8,
+                                 None) == _lib.CSA_ERR_NULL
+    assert lib.dense_xwt_grouped(ctypes.addressof(y), ctypes.addressof(x), 4097,
+                                 ctypes.addressof(m), 1, 8, 8, None) == _lib.CSA_ERR_ALIGN
+    import torch
+    if torch.cuda.is_available():
+        return
+    assert lib.dense_xwt_grouped(ctypes.addressof(y), ctypes.addressof(x), 4096,
+                                 ctypes.addressof(m), 1, 8, 8, None) == _lib.CSA_ERR_CUDA

@@ -195,3 +195,84 @@ def test_dense_misaligned_views(oracle_lib, fetch_mode, offset):
     torch.cuda.synchronize()
     assert csa.get_status() == 0
     assert_close(Y.cpu().numpy(), ref, f"misaligned by {2 * offset} bytes")
+
+
+def _grouped_vs_single(Xs, W, I, H, what):
+    """dense_xwt_grouped against one dense_xwt per problem: equal bit for bit (same
+    k-order per element whatever the tile width)."""
+    Wd = W.cuda()
+    Xd = [X.cuda() for X in Xs]
+    Yg = [poisoned((X.shape[0], H)) for X in Xs]
+    csa.dense_xwt_grouped(Yg, Xd, Wd, I, H)
+    Ys = [poisoned((X.shape[0], H)) for X in Xs]
+    for Y, X in zip(Ys, Xd):
+        csa.dense_xwt(Y, X, Wd, X.shape[0], I, H)
+    torch.cuda.synchronize()
+    assert csa.get_status() == 0
+    for g, (a, b) in enumerate(zip(Yg, Ys)):
+        assert np.array_equal(f32_bits(a), f32_bits(b)), f"{what}: problem {g}"
+    return Yg
+
+
+def test_dense_grouped_sweep(oracle_lib):
+    """The dynamic-shape sweep's 32 problems in one grouped call: equal to 32 separate
+    calls, and sampled rows of each against the oracle."""
+    xs, W = synth.dense_sweep_inputs(seed=0)
+    H, I = W.shape
+    Yg = _grouped_vs_single(xs, W, I, H, "sweep")
+    wbits = synth.bf16_bits(W).reshape(-1)
+    rng = np.random.default_rng(11)
+    for g in (0, 5, 17, 31):
+        X = xs[g]
+        M = X.shape[0]
+        rows = np.unique(np.concatenate([[0, M - 1], rng.integers(0, M, size=4)]))
+        ref = oracle_lib.dense_rows(synth.bf16_bits(X).reshape(-1), wbits, M, I, H, rows)
+        assert_close(Yg[g][torch.from_numpy(rows).cuda()].cpu().numpy(), ref, f"grouped {g}")
+
+
+@pytest.mark.parametrize("I,H", [(768, 200), (64, 130), (128, 3072), (770, 96)])
+def test_dense_grouped_mixed_rows(oracle_lib, I, H):
+    """Row counts on both sides of the 128-row tile, one row, and a multi-wave problem;
+    H = 130 writes Y with plain stores; I = 770 rows are not TMA-describable, so the
+    group runs as separate calls."""
+    Ms = [1, 127, 128, 129, 300, 2049]
+    Xs = [synth.dense_input(synth.DenseShape(M=M, I=I, H=H), seed=M)[0] for M in Ms]
+    W = synth.dense_input(synth.DenseShape(M=1, I=I, H=H), seed=99)[1]
+    Yg = _grouped_vs_single(Xs, W, I, H, f"mixed I={I} H={H}")
+    wbits = synth.bf16_bits(W).reshape(-1)
+    for g in (0, 3, 5):
+        ref = oracle_lib.dense(synth.bf16_bits(Xs[g]).reshape(-1), wbits, Ms[g], I, H)
+        assert_close(Yg[g].cpu().numpy(), ref, f"grouped M={Ms[g]}")
+
+
+def test_dense_grouped_more_than_one_launch():
+    """100 problems: more than one launch's worth (48 each)."""
+    rng = np.random.default_rng(5)
+    I, H = 256, 192
+    Ms = rng.integers(1, 400, size=100).tolist()
+    Xs = [synth.dense_input(synth.DenseShape(M=M, I=I, H=H), seed=i)[0] for i, M in enumerate(Ms)]
+    W = synth.dense_input(synth.DenseShape(M=1, I=I, H=H), seed=7)[1]
+    _grouped_vs_single(Xs, W, I, H, "100 problems")
+
+
+def test_dense_grouped_graph_replay():
+    xs, W = synth.dense_sweep_inputs(seed=0)
+    H, I = W.shape
+    Wd = W.cuda()
+    Xd = [X.cuda() for X in xs[:8]]
+    ref = [poisoned((X.shape[0], H)) for X in Xd]
+    csa.dense_xwt_grouped(ref, Xd, Wd, I, H)
+    Yg = [poisoned((X.shape[0], H)) for X in Xd]
+    side = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        csa.dense_xwt_grouped(Yg, Xd, Wd, I, H, stream=side)
+    for _ in range(3):
+        for Y in Yg:
+            Y.fill_(float("nan"))
+        g.replay()
+    torch.cuda.synchronize()
+    assert csa.get_status() == 0
+    for a, b in zip(Yg, ref):
+        assert np.array_equal(f32_bits(a), f32_bits(b))

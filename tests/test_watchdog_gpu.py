@@ -104,3 +104,24 @@ def test_withheld_hand_off_dense(oracle_lib, M, I, H, mode):
         _timeout_then_recover(lambda: csa.dense_xwt(Y, Xd, Wd, M, I, H), check)
     finally:
         csa.set_dense_fetch(csa.DENSE_FETCH_AUTO)
+
+
+def test_withheld_hand_off_dense_grouped(oracle_lib):
+    """The grouped launch's TMA producer withholds its first load: the MMA warp's wait
+    runs out, the status reports it, and the next call is correct."""
+    I, H = 768, 512
+    Ms = [200, 64, 333]
+    Xs = [synth.dense_input(synth.DenseShape(M=M, I=I, H=H), seed=M)[0] for M in Ms]
+    W = synth.dense_input(synth.DenseShape(M=1, I=I, H=H), seed=3)[1]
+    Xd = [X.cuda() for X in Xs]
+    Wd = W.cuda()
+    Ys = [torch.empty((M, H), dtype=torch.float32, device="cuda") for M in Ms]
+
+    def check():
+        from gpu_util import assert_close
+        wbits = synth.bf16_bits(W).reshape(-1)
+        for X, Y, M in zip(Xs, Ys, Ms):
+            ref = oracle_lib.dense(synth.bf16_bits(X).reshape(-1), wbits, M, I, H)
+            assert_close(Y.cpu().numpy(), ref, f"grouped M={M} after timeout")
+
+    _timeout_then_recover(lambda: csa.dense_xwt_grouped(Ys, Xd, Wd, I, H), check)
