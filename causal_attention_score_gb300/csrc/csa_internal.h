@@ -53,6 +53,28 @@ cudaError_t launch_programmatic(void (*kernel)(KArgs...), unsigned grid, unsigne
 }
 
 // Bound (ns of %globaltimer) on every mbarrier/flag wait in the kernels.
+// launch_programmatic with clusters of cluster_x CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_programmatic_cluster(void (*kernel)(KArgs...), unsigned grid, unsigned block,
+                                        size_t smem, cudaStream_t stream, unsigned cluster_x,
+                                        Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster_x;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 uint64_t wait_limit_ns();
 // True once after csa_debug_inject armed it: the next launch withholds one arrival.
 bool take_inject();

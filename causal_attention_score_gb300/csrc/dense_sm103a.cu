@@ -50,10 +50,14 @@ constexpr int kLoaderWarps = 4;
 constexpr int kMmaWarp = 4;
 constexpr int kFirstEpiWarp = 5;
 #ifndef CSA_DENSE_MAX_STAGES
-#define CSA_DENSE_MAX_STAGES 6
+#define CSA_DENSE_MAX_STAGES 8
+#endif
+// Groups: clusters of two CTAs sharing W tiles by multicast (1) or not (0).
+#ifndef CSA_DENSE_PAIR
+#define CSA_DENSE_PAIR 1
 #endif
 #ifndef CSA_DENSE_STORE_BUFS
-#define CSA_DENSE_STORE_BUFS 4
+#define CSA_DENSE_STORE_BUFS 2
 #endif
 constexpr int kStoreBufs = CSA_DENSE_STORE_BUFS;  // staging boxes per epilogue warp
 constexpr int kBoxBytes = 32 * 32 * 4;
@@ -148,7 +152,14 @@ __device__ __forceinline__ void issue_block_async(const uint16_t* src, int nrows
   }
 }
 
-template <bool kGrouped>
+// kPair (groups only): clusters of two CTAs compute 256-row tiles as a CTA pair
+// (tcgen05 cta_group::2): each CTA loads its own 128 rows of X and half of the W
+// tile's rows, and the pair's first CTA issues M = 256 MMAs that read both CTAs'
+// shared memory, each CTA's TMEM receiving its own rows. Per k-block each SM then
+// receives (128 + BN/2) x 128 bytes instead of (128 + BN) x 128. Both CTAs' loads
+// complete on the first CTA's full barrier; its commits go to both CTAs' barriers;
+// the second CTA's epilogue releases accumulators on the first CTA's barrier.
+template <bool kGrouped, bool kPair = false>
 __global__ void __launch_bounds__(kThreads, 1)
     dense_sm103a_kernel(const __grid_constant__ CUtensorMap tmap_x,
                         const __grid_constant__ CUtensorMap tmap_w,
@@ -175,14 +186,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const Watchdog wd{a.wait_limit_ns, a.status, abort_flag};
 
-  // Tile t of the launch, n-major (CTAs working at the same time share W's n-tile):
-  // problem p, its m-tile mb, the n-tile nb. In a group the m-tiles of all
-  // problems follow one another.
+  // With kPair, this CTA's half of each tile pair (0 or 1) and the pair walk.
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const long long t_first = kPair ? blockIdx.x / 2 : blockIdx.x;
+  const long long t_step = kPair ? gridDim.x / 2 : gridDim.x;
+
+  // Tile t of the launch: problem p, its m-tile mb, the n-tile nb. A group is
+  // m-major (the n-tiles of one m-tile follow one another, so CTAs working at the
+  // same time share X's m-tile and spread their reads over all of W; n-major, every
+  // CTA read the same W tile at once: measured 8 % slower on the grouped sweep),
+  // the m-tiles of all problems following one another. One problem is n-major
+  // (measured 2 % faster than m-major over the sweep's separate calls).
   auto locate = [&](long long t, int& p, int& mb, int& nb) {
     if constexpr (kGrouped) {
-      const int total = g.mt_start[g.n];
-      const int mt = static_cast<int>(t % total);
-      nb = static_cast<int>(t / total);
+      // (pairs: t numbers tile pairs; a pair past the last m-tile has a phantom
+      // half, whose rows are past its problem's M: zero-filled and not stored)
+      const int mt = kPair ? static_cast<int>(2 * (t / a.n_tiles) + rank)
+                           : static_cast<int>(t / a.n_tiles);
+      nb = static_cast<int>(t % a.n_tiles);
       int lo = 0, hi = g.n - 1;  // the last problem whose first m-tile is <= mt
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -221,20 +242,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(tfull_bar(s), 1);
-      mbar_init(tempty_bar(s), 4);
+      mbar_init(tempty_bar(s), kPair ? 8u : 4u);  // with kPair, both CTAs' epilogues
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
-    tmem_alloc(tmem_slot, a.tmem_cols);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(tmem_slot, a.tmem_cols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, a.tmem_cols);
+      tmem_relinquish();
+    }
     tc_fence_before_sync();
   }
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = ld_shared_b32(tmem_slot);
+  // The peer's barriers are initialised before any of its loads, commits or
+  // arrivals reach them.
+  if constexpr (kPair) cluster_sync();
 
   // Nothing global has been touched yet: the kernel ahead in the stream may still
   // be running (programmatic launch), so wait for it here.
@@ -253,9 +282,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         int stage = 0;
         uint32_t phase = 0;
         uint32_t issued = 0, issued_parity = 0;
-        const uint32_t tx = static_cast<uint32_t>(kBM + a.BN) * 128u;
-        for (long long tile = blockIdx.x; tile < a.num_tiles && !*abort_flag;
-             tile += gridDim.x) {
+        // Bytes one CTA loads per stage; with kPair both CTAs' loads complete on
+        // the first CTA's full barrier, which expects both.
+        const int b_rows = kPair ? a.BN / 2 : a.BN;
+        const uint32_t tx = static_cast<uint32_t>(kBM + b_rows) * 128u;
+        for (long long tile = t_first; tile < a.num_tiles && !*abort_flag; tile += t_step) {
           int p, mb, nb;
           locate(tile, p, mb, nb);
           const CUtensorMap* mx = map_x(p);
@@ -265,14 +296,27 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(full_bar(stage), tx);
-            if (a.inject && tile == blockIdx.x && kb == 0) {
+            if (!kPair || rank == 0) mbar_arrive_expect_tx(full_bar(stage), kPair ? 2u * tx : tx);
+            if (a.inject && tile == t_first && kb == 0) {
               issued &= ~(1u << stage);  // withheld: the MMA warp's wait must run out
             } else {
-              tma_load_2d(a_tile(stage), mx, full_bar(stage), kb * kBK, mb * kBM);
-              tma_load_2d(b_tile(stage), &tmap_w, full_bar(stage), kb * kBK, nb * a.BN);
-              issued |= 1u << stage;
-              issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+              if constexpr (kPair) {
+                // This CTA's 128 rows of X and its half of the W tile's rows, both
+                // completing on the first CTA's barrier.
+                const uint32_t bar0 = mapa_shared(full_bar(stage), 0);
+                tma_load_2d_pair(a_tile(stage), mx, bar0, kb * kBK, mb * kBM);
+                tma_load_2d_pair(b_tile(stage), &tmap_w, bar0, kb * kBK,
+                                 nb * a.BN + static_cast<int>(rank) * b_rows);
+              } else {
+                tma_load_2d(a_tile(stage), mx, full_bar(stage), kb * kBK, mb * kBM);
+                tma_load_2d(b_tile(stage), &tmap_w, full_bar(stage), kb * kBK, nb * a.BN);
+              }
+              // (kPair: only the first CTA can see its loads land; the second CTA's
+              // in-flight loads are covered by the teardown's grace period)
+              if (!kPair || rank == 0) {
+                issued |= 1u << stage;
+                issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+              }
             }
             if (++stage == a.stages) {
               stage = 0;
@@ -301,9 +345,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0, oldest = 0, pending = 0, arrivals = 0;
       uint32_t phase = 0;
       bool aborted = false;
-      for (long long tile = blockIdx.x; tile < a.num_tiles && !aborted; tile += gridDim.x) {
-        const int mb = static_cast<int>(tile % a.m_tiles);
-        const int nb = static_cast<int>(tile / a.m_tiles);
+      for (long long tile = t_first; tile < a.num_tiles && !aborted; tile += t_step) {
+        int p, mb, nb;
+        locate(tile, p, mb, nb);
         for (int kb = 0; kb < a.kblocks; ++kb) {
           if (!mbar_wait_warp(empty_bar(stage), phase ^ 1u, wd, kSiteLoaderEmpty)) {
             aborted = true;
@@ -344,9 +388,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       int stage = 0;
       uint32_t phase = 0;
-      for (long long tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
-        const int mb = static_cast<int>(tile % a.m_tiles);
-        const int nb = static_cast<int>(tile / a.m_tiles);
+      for (long long tile = t_first; tile < a.num_tiles; tile += t_step) {
+        int p, mb, nb;
+        locate(tile, p, mb, nb);
         bool ok = true;
         for (int kb = 0; kb < a.kblocks; ++kb) {
           if (!mbar_wait_warp(empty_bar(stage), phase ^ 1u, wd, kSiteLoaderEmpty)) {
@@ -375,7 +419,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (long long tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
+      // With kPair only the pair's first CTA issues MMAs; the second waits for
+      // their completion (the first CTA's drain commit reaches both).
+      const bool issuer = !kPair || rank == 0;
+      for (long long tile = t_first; issuer && tile < a.num_tiles; tile += t_step) {
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, wd, kSiteMmaTmemEmpty)) break;
         tc_fence_after_sync();
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * a.BN);
@@ -389,24 +436,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             const uint32_t off = static_cast<uint32_t>(k) * 32u;
-            umma_bf16(d, umma_desc_k_sw128(a_tile(stage) + off),
-                      umma_desc_k_sw128(b_tile(stage) + off), a.idesc,
-                      (kb > 0 || k > 0) ? 1u : 0u);
+            if constexpr (kPair)
+              umma_bf16_pair(d, umma_desc_k_sw128(a_tile(stage) + off),
+                             umma_desc_k_sw128(b_tile(stage) + off), a.idesc,
+                             (kb > 0 || k > 0) ? 1u : 0u);
+            else
+              umma_bf16(d, umma_desc_k_sw128(a_tile(stage) + off),
+                        umma_desc_k_sw128(b_tile(stage) + off), a.idesc,
+                        (kb > 0 || k > 0) ? 1u : 0u);
           }
-          umma_commit(empty_bar(stage));
+          if constexpr (kPair) umma_commit_pair_multicast(empty_bar(stage), 0x3);  // both CTAs
+          else umma_commit(empty_bar(stage));
           if (++stage == a.stages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(tfull_bar(acc));
+        if constexpr (kPair) umma_commit_pair_multicast(tfull_bar(acc), 0x3);
+        else umma_commit(tfull_bar(acc));
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
-      umma_commit(drain_bar);
+      if (issuer) {
+        if constexpr (kPair) umma_commit_pair_multicast(drain_bar, 0x3);
+        else umma_commit(drain_bar);
+      }
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_test(drain_bar, 0) && globaltimer_ns() - t0 < a.wait_limit_ns) {
       }
@@ -420,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     uint32_t buf = 0;
     const int chunks = a.BN / 32;
-    for (long long tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x) {
+    for (long long tile = t_first; tile < a.num_tiles; tile += t_step) {
       int p, mb, nb;
       locate(tile, p, mb, nb);
       const int M = rows_of(p);
@@ -435,7 +492,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (c == chunks - 1) {
           tc_fence_before_sync();
           __syncwarp();
-          if (lane == 0) mbar_arrive(tempty_bar(acc));
+          if (lane == 0) {
+            // (kPair: the accumulator is released on the pair's first CTA)
+            if constexpr (kPair) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+            else mbar_arrive(tempty_bar(acc));
+          }
         }
         const int col0 = nb * a.BN + c * 32;
         if (row0 >= M || col0 >= a.H) continue;
@@ -472,9 +533,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   __syncthreads();
+  if constexpr (kPair) {
+    // After a watchdog abort the second CTA cannot see its own loads land (they
+    // complete on the first CTA's barrier): give any still in flight time to.
+    if (*abort_flag && threadIdx.x == 0) {
+      const uint64_t t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 100000ull) {
+      }
+    }
+    __syncthreads();
+    // The peer's loads, commits and arrivals on this CTA are done.
+    cluster_sync();
+  }
   if (warp == kMmaWarp) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, a.tmem_cols);
+    if constexpr (kPair) tmem_dealloc_pair(tmem_base, a.tmem_cols);
+    else tmem_dealloc(tmem_base, a.tmem_cols);
   }
 }
 
@@ -587,9 +661,11 @@ int choose_bn_tiles(long long m_tiles, int H, int sms) {
 
 int choose_bn(int M, int H, int sms) { return choose_bn_tiles((M + kBM - 1) / kBM, H, sms); }
 
-// Shared-memory plan for BN: ring stages, then staging, barriers and misc.
-int plan_smem(DenseArgs& a, const DeviceInfo& dev, std::string& err, size_t& smem) {
-  a.stage_bytes = static_cast<uint32_t>(kBM + a.BN) * 128u;
+// Shared-memory plan: ring stages of 128 rows of X and b_rows rows of W (BN, or
+// BN / 2 for a CTA pair), then staging, barriers and misc.
+int plan_smem(DenseArgs& a, const DeviceInfo& dev, std::string& err, size_t& smem,
+              int b_rows) {
+  a.stage_bytes = static_cast<uint32_t>(kBM + b_rows) * 128u;
   const int fixed = kStagingBytes + 1024 + 1024;
   a.stages = std::min(CSA_DENSE_MAX_STAGES,
                       (dev.max_smem_optin - fixed) / static_cast<int>(a.stage_bytes));
@@ -667,7 +743,7 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
 
   size_t smem = 0;
   {
-    const int rc = plan_smem(a, dev, err, smem);
+    const int rc = plan_smem(a, dev, err, smem, a.BN);
     if (rc != CSA_OK) return release(rc);
   }
 
@@ -784,11 +860,13 @@ int dense_grouped_launch(float* const* Y, const void* const* X, const void* W, c
     a.m_tiles = static_cast<int>(total);
     a.n_tiles = (H + a.BN - 1) / a.BN;
     a.kblocks = (I + kBK - 1) / kBK;
-    a.num_tiles = total * a.n_tiles;
+    // Pairs of CTAs (clusters of two) walk tile pairs: adjacent m-tiles, one n-tile.
+    bool pair = CSA_DENSE_PAIR != 0;
+    a.num_tiles = pair ? (total + 1) / 2 * a.n_tiles : total * a.n_tiles;
     a.tma_load = 1u;
     a.tma_store = tma_store ? 1u : 0u;
     a.vec2 = 0u;
-    a.idesc = idesc_bf16_f32(kBM, a.BN);
+    a.idesc = pair ? idesc_bf16_f32(2 * kBM, a.BN) : idesc_bf16_f32(kBM, a.BN);
     a.X = nullptr;
     a.W = static_cast<const uint16_t*>(W);
     a.Y = nullptr;
@@ -797,12 +875,55 @@ int dense_grouped_launch(float* const* Y, const void* const* X, const void* W, c
     a.inject = take_inject() ? 1 : 0;
     a.tmem_cols = static_cast<uint32_t>(2 * a.BN);
     size_t smem = 0;
-    int rc = plan_smem(a, dev, err, smem);
+    int rc = plan_smem(a, dev, err, smem, pair ? a.BN / 2 : a.BN);
     if (rc != CSA_OK) return rc;
+
+    // Clusters that can be resident at once with this much shared memory; none
+    // (or an error) means no pairing.
+    auto* kernel_pair = dense_sm103a_kernel<true, true>;
+    int clusters = 0;
+    if (pair) {
+      rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kernel_pair), static_cast<int>(smem),
+                                dev.device, err);
+      if (rc != CSA_OK) return rc;
+      static std::mutex mu;
+      static int cached_smem[64] = {}, cached_clusters[64] = {};
+      std::lock_guard<std::mutex> lock(mu);
+      const int d = dev.device >= 0 && dev.device < 64 ? dev.device : 0;
+      if (cached_smem[d] != static_cast<int>(smem)) {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(2);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = 2;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        int n_clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&n_clusters, kernel_pair, &cfg) != cudaSuccess) {
+          (void)cudaGetLastError();
+          n_clusters = 0;
+        }
+        cached_smem[d] = static_cast<int>(smem);
+        cached_clusters[d] = n_clusters;
+      }
+      clusters = cached_clusters[d];
+      if (clusters < 1) {
+        pair = false;
+        a.num_tiles = total * a.n_tiles;
+        a.idesc = idesc_bf16_f32(kBM, a.BN);
+        rc = plan_smem(a, dev, err, smem, a.BN);
+        if (rc != CSA_OK) return rc;
+      }
+    }
 
     const uint64_t st_in[1] = {static_cast<uint64_t>(I) * 2};
     const uint32_t bx[2] = {kBK, kBM};
-    const uint32_t bw[2] = {kBK, static_cast<uint32_t>(a.BN)};
+    // With pairs, each CTA loads (and multicasts) half of the W tile's rows.
+    const uint32_t bw[2] = {kBK, static_cast<uint32_t>(pair ? a.BN / 2 : a.BN)};
     const uint64_t dw[2] = {static_cast<uint64_t>(I), static_cast<uint64_t>(H)};
     rc = encode_tiled(&map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, dw, st_in, bw,
                       CU_TENSOR_MAP_SWIZZLE_128B, err);
@@ -829,9 +950,16 @@ int dense_grouped_launch(float* const* Y, const void* const* X, const void* W, c
     }
     CUtensorMap unused;
     std::memset(&unused, 0, sizeof unused);
-    const long long grid = std::min<long long>(a.num_tiles, dev.sm_count);
-    cudaError_t e = launch_programmatic(dense_sm103a_kernel<true>, static_cast<unsigned>(grid),
-                                        kThreads, smem, stream, unused, map_w, unused, a, grp);
+    cudaError_t e;
+    if (pair) {
+      const long long grid = 2 * std::min<long long>(a.num_tiles, clusters);
+      e = launch_programmatic_cluster(kernel_pair, static_cast<unsigned>(grid), kThreads, smem,
+                                      stream, 2u, unused, map_w, unused, a, grp);
+    } else {
+      const long long grid = std::min<long long>(a.num_tiles, dev.sm_count);
+      e = launch_programmatic(dense_sm103a_kernel<true>, static_cast<unsigned>(grid), kThreads,
+                              smem, stream, unused, map_w, unused, a, grp);
+    }
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
       err = std::string("dense_xwt_grouped: launch: ") + cudaGetErrorString(e);
