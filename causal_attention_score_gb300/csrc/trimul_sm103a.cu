@@ -87,6 +87,10 @@ constexpr int kChunkBytes = kTile * 128;  // one 128-row x 64-element operand ch
 #ifndef CSA_TRIMUL_LO_SLOTS
 #define CSA_TRIMUL_LO_SLOTS 3
 #endif
+// fp32 form with Q in TMEM: one staging box per epilogue warp (1) or a pair (0).
+#ifndef CSA_TRIMUL_F32_SINGLE_BOX
+#define CSA_TRIMUL_F32_SINGLE_BOX 1
+#endif
 // fp32 form with Q in TMEM: Q buffers when two fit (1 or 2).
 #ifndef CSA_TRIMUL_Q_BUFS
 #define CSA_TRIMUL_Q_BUFS 2
@@ -125,7 +129,8 @@ struct TrimulArgs {
   int* status;
   unsigned long long wait_limit_ns;
   int inject;
-  uint32_t store_groups;  // staging box pairs per epilogue warp (1 or 2)
+  uint32_t store_groups;  // staging box pairs per epilogue warp (1 or 2; 0: a single box)
+  uint32_t staging_stride;  // staging bytes per epilogue warp
   uint32_t stage_bytes, off_staging, off_mask, off_bars, off_misc;
   // Operand chunks (128-byte rows) per stage, and stages per tile: bf16 keeps a
   // whole tile's chunks in one stage; the fp32 form streams one chunk per stage.
@@ -205,7 +210,11 @@ __device__ __forceinline__ void decode_fill(int r, int& ti, int& tj) {
   tj = i;                         // column tile
 }
 
-template <bool kF32>
+// kSingleBox (fp32 with Q in TMEM, full mode): one staging box per epilogue warp
+// instead of a pair, so the operand rings get 32 KB more shared memory. A
+// separate instance: the lower-only fp32 form measured 16 % slower with this
+// path merely compiled into its kernel.
+template <bool kF32, bool kSingleBox = false>
 __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
     trimul_sm103a_kernel(const __grid_constant__ CUtensorMap tmap_a,
                          const __grid_constant__ CUtensorMap tmap_b,
@@ -740,7 +749,7 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
     const uint32_t ew = warp - 2u;
     const int q = static_cast<int>(warp & 3u);
     const int slab = static_cast<int>(ew >> 2);
-    const uint32_t staging = base + a.off_staging + ew * a.store_groups * 2u * kBoxBytes;
+    const uint32_t staging = base + a.off_staging + ew * a.staging_stride;
     const int T = a.T, T2 = a.T2;  // output rows and columns of one (b, h)
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -813,6 +822,39 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
         }
       }
       if (mode[0] == 0 && mode[1] == 0) continue;
+
+      if constexpr (kSingleBox) {
+        {
+          // One staging box per warp (more room for the operand rings): the two
+          // 32-column boxes go out one after the other.
+          for (int c = 0; c < 2; ++c) {
+            if (mode[c] == 0) continue;
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+            stage_row_sw128(staging, lane, v + 32 * c);
+            if (mode[c] == 1) {
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_3d(&tmap_out, staging, colw + c * 32, row0, bh);
+                bulk_commit();
+              }
+              continue;
+            }
+            __syncwarp();
+            const int col = colw + c * 32 + static_cast<int>(lane);
+            float* ocol = a.out + (static_cast<size_t>(bh) * T + row0) * T2 + col;
+            for (int rr = 0; rr < 32; ++rr) {
+              const int row = row0 + rr;
+              const bool ok = row < T && col < T2 && (mode[c] == 2 || col <= row);
+              const uint32_t val = staged_elem_sw128(staging, static_cast<uint32_t>(rr), lane);
+              if (ok) ocol[static_cast<size_t>(rr) * T2] = __uint_as_float(val);
+            }
+            __syncwarp();
+          }
+          continue;
+        }
+      }
 
       if (lane == 0) {
         if (a.store_groups == 2) bulk_wait_read<1>();
@@ -949,6 +991,16 @@ int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& 
                                         static_cast<int>(a.stage_bytes));
     if (a.stages >= 2) break;
   }
+  const bool single_box = q_tmem && CSA_TRIMUL_F32_SINGLE_BOX && a.n_fill > 0;
+  if (single_box) {
+    // fp32 with Q in TMEM: one staging box per epilogue warp (store_groups 0); its
+    // epilogue mostly waits on the MMAs, and the operand rings take the space.
+    staging_bytes = kEpiWarps * kBoxBytes;
+    a.store_groups = 0u;
+    a.stages = std::min(max_stages, (dev.max_smem_optin - fixed - staging_bytes) /
+                                        static_cast<int>(a.stage_bytes));
+  }
+  a.staging_stride = static_cast<uint32_t>(staging_bytes / kEpiWarps);
   if (a.stages < 1) {
     err = name + ": not enough shared memory for one operand stage";
     return CSA_ERR_UNSUPPORTED;
@@ -1002,7 +1054,9 @@ int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& 
     }
     a.sched = sched_base[dev.device] + kSchedWords * (launch_seq.fetch_add(1) % kSchedSlots);
   }
-  auto* kernel = f32 ? trimul_sm103a_kernel<true> : trimul_sm103a_kernel<false>;
+  auto* kernel = !f32         ? trimul_sm103a_kernel<false, false>
+                 : single_box ? trimul_sm103a_kernel<true, true>
+                              : trimul_sm103a_kernel<true, false>;
   {
     int rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kernel), static_cast<int>(smem),
                                   dev.device, err);
