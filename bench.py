@@ -348,7 +348,7 @@ def make_workload(name, dev):
             X = X_h.to(dev)
             M = X_h.shape[0]
             Y = torch.empty((M, H), dtype=torch.float32, device=dev)
-            parts.append((f"call{i}", (lambda X, Y, M: lambda st: csa.dense_xwt(
+            parts.append((f"call{i}_M{M}", (lambda X, Y, M: lambda st: csa.dense_xwt(
                 Y, X, W, M, I, H, stream=st))(X, Y, M)))
             h2d.append((X, X_h))
             outs.append(Y)
@@ -559,7 +559,7 @@ def run_ours(args, rank, world, local):
         "clocks": sampler.summary(),
         "wall_s_timed_region": round(wall, 4),
     }
-    if part_ms is not None and P <= 4:
+    if part_ms is not None and P <= 40:
         result["parts"] = {f"{label}_us": round(ms * 1e3, 2)
                            for (label, _), ms in zip(wl.parts, part_ms)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "step":
