@@ -810,7 +810,9 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
       }
       if (row0 >= T || colw >= T2) continue;  // slab wholly past the end (tail tile)
 
-      // Per 32-column box: 0 skip, 1 TMA store, 2 plain stores, 3 plain stores t2 <= t only.
+      // Per 32-column box: 0 skip, 1 TMA store, 2 plain stores, 3 plain stores t2 <= t
+      // only, 4 (16-byte-aligned rows) each lane stores its row's t2 <= t part from
+      // registers with vector stores.
       int mode[2];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -818,7 +820,7 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
         mode[c] = col0 >= T2 ? 0 : (a.tma_store ? 1 : 2);
         if (mode[c] != 0 && a.lower_only && diag) {
           if (col0 > row0 + 31) mode[c] = 0;
-          else if (col0 + 31 > row0) mode[c] = 3;
+          else if (col0 + 31 > row0) mode[c] = a.tma_store ? 4 : 3;
         }
       }
       if (mode[0] == 0 && mode[1] == 0) continue;
@@ -865,7 +867,7 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
       if (++grp == a.store_groups) grp = 0;
 #pragma unroll
       for (int c = 0; c < 2; ++c)
-        if (mode[c] != 0) stage_row_sw128(pair + c * kBoxBytes, lane, v + 32 * c);
+        if (mode[c] != 0 && mode[c] != 4) stage_row_sw128(pair + c * kBoxBytes, lane, v + 32 * c);
       const bool any_tma = mode[0] == 1 || mode[1] == 1;
       if (any_tma) fence_proxy_async_smem();
       __syncwarp();
@@ -874,8 +876,28 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
           if (mode[c] == 1) tma_store_3d(&tmap_out, pair + c * kBoxBytes, colw + c * 32, row0, bh);
         bulk_commit();
       }
+#pragma unroll
       for (int c = 0; c < 2; ++c) {
-        if (mode[c] < 2) continue;
+        if (mode[c] != 4 || r >= T) continue;
+        const int c0 = colw + c * 32;
+        const int lim = r - c0;  // this row's columns c0 + e, e <= lim, are t2 <= t
+        float* orow = a.out + (static_cast<size_t>(bh) * T + r) * T2 + c0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int e0 = 4 * k;
+          if (e0 + 3 <= lim) {
+            *reinterpret_cast<float4*>(orow + e0) =
+                make_float4(__uint_as_float(v[32 * c + e0]), __uint_as_float(v[32 * c + e0 + 1]),
+                            __uint_as_float(v[32 * c + e0 + 2]), __uint_as_float(v[32 * c + e0 + 3]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (e0 + j <= lim) orow[e0 + j] = __uint_as_float(v[32 * c + e0 + j]);
+          }
+        }
+      }
+      for (int c = 0; c < 2; ++c) {
+        if (mode[c] < 2 || mode[c] == 4) continue;
         const int col = colw + c * 32 + static_cast<int>(lane);
         float* ocol = a.out + (static_cast<size_t>(bh) * T + row0) * T2 + col;
         for (int rr = 0; rr < 32; ++rr) {
