@@ -137,7 +137,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tfull_bar = [&](int s) { return bars + 8u * (4 + 2 * S + s); };
   auto tempty_bar = [&](int s) { return bars + 8u * (6 + 2 * S + s); };
   const uint32_t drain_bar = bars + 8u * (8 + 2 * S);
-  const uint32_t stats_bar = bars + 8u * (9 + 2 * S);
+  // Row statistics exchange of the two warps that share TMEM lane quarter p (the
+  // two 64-column halves of the same rows): one barrier per pair.
+  auto stats_bar = [&](uint32_t p) { return bars + 8u * (10 + 2 * S + 2 * kRingDepth + p); };
   auto rfull_bar = [&](int s) { return bars + 8u * (10 + 2 * S + s); };
   auto rempty_bar = [&](int s) { return bars + 8u * (10 + 2 * S + kRingDepth + s); };
   const uint32_t tmem_slot = base + a.off_misc;
@@ -170,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(kempty_bar(s), 1);
     }
     mbar_init(drain_bar, 1);
-    mbar_init(stats_bar, kEpiWarps);
+    for (uint32_t p = 0; p < 4; ++p) mbar_init(stats_bar(p), 2);
     for (int s = 0; s < kRingDepth; ++s) {
       mbar_init(rfull_bar(s), 1);
       mbar_init(rempty_bar(s), 1 + kEpiWarps);
@@ -556,8 +558,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           st_shared_b32(sbase + (ew * 32u + lane) * 8u, __float_as_uint(m));
           st_shared_b32(sbase + (ew * 32u + lane) * 8u + 4u, __float_as_uint(l));
           __syncwarp();
-          if (lane == 0) mbar_arrive(stats_bar);
-          if (!mbar_wait_warp_inline(stats_bar, stats_phase, wd, kSiteEpilogueFull)) return false;
+          if (lane == 0) mbar_arrive(stats_bar(static_cast<uint32_t>(q)));
+          if (!mbar_wait_warp_inline(stats_bar(static_cast<uint32_t>(q)), stats_phase, wd,
+                                     kSiteEpilogueFull))
+            return false;
           stats_phase ^= 1u;
           const uint32_t other = sbase + ((ew ^ 4u) * 32u + lane) * 8u;
           const float m2 = __uint_as_float(ld_shared_b32(other));
@@ -744,7 +748,7 @@ int softmax_launch(float* out, const void* qkv, int B, int T, int C, int NH, cud
   a.off_zero = a.off_staging + static_cast<uint32_t>(staging_bytes);
   a.off_stats = a.off_zero + kZeroBytes;
   a.off_bars = a.off_stats + kStatsBytes;
-  a.off_misc = a.off_bars + 8u * static_cast<uint32_t>(10 + 2 * a.stages + 2 * kRingDepth);
+  a.off_misc = a.off_bars + 8u * static_cast<uint32_t>(10 + 2 * a.stages + 2 * kRingDepth + 4);
   const size_t smem = a.off_misc + 16 + 4 * kRingDepth + 8 + 1024;
 
   CUtensorMap map_qkv, map_out, map_zero;
