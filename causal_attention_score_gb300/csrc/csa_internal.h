@@ -52,7 +52,6 @@ cudaError_t launch_programmatic(void (*kernel)(KArgs...), unsigned grid, unsigne
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
-// Bound (ns of %globaltimer) on every mbarrier/flag wait in the kernels.
 // launch_programmatic with clusters of cluster_x CTAs along x.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_programmatic_cluster(void (*kernel)(KArgs...), unsigned grid, unsigned block,
@@ -75,6 +74,7 @@ cudaError_t launch_programmatic_cluster(void (*kernel)(KArgs...), unsigned grid,
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
+// Bound (ns of %globaltimer) on every mbarrier/flag wait in the kernels.
 uint64_t wait_limit_ns();
 // True once after csa_debug_inject armed it: the next launch withholds one arrival.
 bool take_inject();
