@@ -528,7 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_phase ^= 1u;
       }
     }
-    if (lane == 0) bulk_wait_all();
+    // Only the stores' reads of shared memory must finish before the CTA exits;
+    // their global writes complete before the grid does.
+    if (lane == 0) bulk_wait_read<0>();
     __syncwarp();
   }
 

@@ -426,7 +426,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             blk[static_cast<size_t>(rr) * T + i] = 0.0f;
       }
     }
-    if (lane == 0) bulk_wait_all();
+    // Only the stores' reads of shared memory must finish before the CTA exits;
+    // their global writes complete before the grid does.
+    if (lane == 0) bulk_wait_read<0>();
     __syncwarp();
   } else {
     // ---------------------------------------------------------- epilogue --
@@ -664,7 +666,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       *epi_storing = 0;
       *epi_done = 1;
     }
-    if (lane == 0) bulk_wait_all();
+    // Only the stores' reads of shared memory must finish before the CTA exits;
+    // their global writes complete before the grid does.
+    if (lane == 0) bulk_wait_read<0>();
     __syncwarp();
   }
 

@@ -693,7 +693,8 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
     // ------------------------------------------------------- fill writer --
     const int T = a.T, T2 = a.T2;
     const uint64_t once = l2_policy_evict_first();
-    bool ok = true;
+    // (no fill pool: the pool counter is left untouched)
+    bool ok = a.n_fill > 0;
     while (ok) {
       int f = 0;
       if (lane == 0) {
@@ -739,7 +740,9 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
             blk[static_cast<size_t>(rr) * T2 + i] = m;
       }
     }
-    if (lane == 0) bulk_wait_all();
+    // Only the stores' reads of shared memory must finish before the CTA exits;
+    // their global writes complete before the grid does.
+    if (lane == 0) bulk_wait_read<0>();
     __syncwarp();
   } else {
     // ---------------------------------------------------------- epilogue --
@@ -910,7 +913,9 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
       }
     }
     if (ew == 0 && lane == 0) *epi_idle = 1;
-    if (lane == 0) bulk_wait_all();
+    // Only the stores' reads of shared memory must finish before the CTA exits;
+    // their global writes complete before the grid does.
+    if (lane == 0) bulk_wait_read<0>();
     __syncwarp();
   }
 
@@ -919,8 +924,10 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, static_cast<uint32_t>(a.tmem_cols));
   }
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && (a.dynamic || a.n_fill > 0)) {
     // Every fetch of this CTA is done; the last CTA to get here resets the pair.
+    // (A static deal without fill tiles never touches the counters: no reset, and
+    // no fence and atomics on every CTA's way out.)
     __threadfence();
     if (atomicAdd(a.sched + 1, 1u) == gridDim.x - 1) {
       atomicExch(a.sched, 0u);

@@ -155,3 +155,41 @@ def test_trimul_many_launches_reuse_schedule_slots(oracle_lib):
     assert csa.get_status() == 0
     ref = oracle_lib.trimul(synth.bf16_bits(qkv).reshape(-1), 2, 384, shape.C, 2, 0)
     check_trimul_full(f32_bits(out), out.cpu().numpy(), ref, NAN_BITS, "after 300 launches")
+
+
+def test_trimul_full_after_static_launches_in_every_slot(oracle_lib):
+    """Launches with a static deal and no fill tiles (lower-only, batched NT) leave
+    their counter slot untouched and skip the reset; every full-mode launch that
+    follows one of them in the same slot must still store every fill tile. The
+    pattern [lower-only, full, batched NT] has period 3, coprime to the 256-slot
+    ring, so over 3 x 256 launches every slot serves a full launch right after a
+    static one; each full launch is compared bit for bit with the first."""
+    shape, qkv = trimul_case(2, 384, 2, 64, seed=12)
+    q = qkv.cuda()
+    ref = oracle_lib.trimul(synth.bf16_bits(qkv).reshape(-1), 2, 384, shape.C, 2, 0)
+    out = torch.empty(shape.out_shape, dtype=torch.float32, device="cuda")
+    out.view(torch.int32).fill_(-1)
+    csa.trimul_forward(out, q, 2, 384, shape.C, 2)
+    torch.cuda.synchronize()
+    check_trimul_full(f32_bits(out), out.cpu().numpy(), ref, NAN_BITS, "first full launch")
+    want = out.view(torch.int32).clone()
+    X = torch.ones((6, 120, 64), dtype=torch.bfloat16, device="cuda")
+    Y = torch.empty((6, 120, 120), dtype=torch.float32, device="cuda")
+    bad = torch.zeros((), dtype=torch.int64, device="cuda")
+    fulls = 0
+    for i in range(3 * 256 + 3):
+        kind = i % 3
+        if kind == 0:
+            csa.trimul_forward(out, q, 2, 384, shape.C, 2, lower_only=True)
+        elif kind == 1:
+            out.view(torch.int32).fill_(-1)
+            csa.trimul_forward(out, q, 2, 384, shape.C, 2)
+            bad += (out.view(torch.int32) != want).sum()
+            fulls += 1
+        else:
+            csa.batch_matmul_nt(Y, X, X, 6, 120, 120, 64)
+    torch.cuda.synchronize()
+    assert csa.get_status() == 0
+    assert fulls == 257
+    assert int(bad) == 0, f"{int(bad)} words differ across the full-mode launches"
+    assert torch.all(Y == 64.0)
