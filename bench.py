@@ -605,10 +605,26 @@ def cpu_baseline(seconds: float):
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
-    return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": o.num_threads(),
+    cores = o.num_threads()
+    # The same samples on one thread, for about a quarter of the time.
+    o.set_num_threads(1)
+    try:
+        flops1, j = 0, 0
+        t1 = time.perf_counter()
+        while True:
+            flops1 += oracle_sample_step(o, ts, ds, qkv, xb, wb, j)
+            j += 1
+            if time.perf_counter() - t1 >= seconds / 4:
+                break
+        dt1 = time.perf_counter() - t1
+    finally:
+        o.set_num_threads(cores)
+    return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": cores,
             "kind": "oracle",
             "sample": f"{i} samples of one (b,h) head of trimul GPT-2 (1024 rows) + 64 rows of "
-                      f"dense ragged, fp64, {dt:.1f} s"}
+                      f"dense ragged, fp64, {dt:.1f} s",
+            "value_1thread": round(flops1 / dt1 / 1e12, 6),
+            "sample_1thread": f"{j} of the same samples on 1 thread, {dt1:.1f} s"}
 
 
 def run_reference(args, rank, world):
