@@ -182,11 +182,17 @@ KERNEL_SOURCES = [os.path.join(ROOT, "causal_attention_score_gb300", "csrc", f)
 
 
 def kernel_source_hash() -> str:
+    """Hash of the score kernel's code with comments and blank space removed, so that
+    an edit of its comments keeps a traffic record taken on the same code."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)  # block comments
+        src = re.sub(r"//[^\n]*", " ", src)                # line comments
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -10,6 +10,10 @@
 // Design (one persistent launch, one CTA per SM, 9 warps):
 //  - tiles of 128 x BN outputs (BN = 64, 128 or 256, chosen per shape),
 //    K in blocks of 64; tiles are dealt round-robin to CTAs.
+//  - dense_xwt_grouped: up to 48 problems sharing W in one launch (their tensor
+//    maps in the kernel parameters, m-tiles of all problems in one list); when
+//    the occupancy allows it, clusters of two CTAs compute 256 x BN tiles as a
+//    CTA pair (tcgen05 cta_group::2), each CTA holding 128 rows.
 //  - Fetch, two forms:
 //      * TMA (I*2 % 16 == 0, 16-byte aligned X and W): warp 0 issues 2-D tiled
 //        loads; rows >= M / H and columns >= I are zero-filled by the TMA unit.
@@ -52,7 +56,8 @@ constexpr int kFirstEpiWarp = 5;
 #ifndef CSA_DENSE_MAX_STAGES
 #define CSA_DENSE_MAX_STAGES 8
 #endif
-// Groups: clusters of two CTAs sharing W tiles by multicast (1) or not (0).
+// Groups: clusters of two CTAs computing 256-row tiles as a CTA pair (1), or one
+// CTA per 128-row tile (0).
 #ifndef CSA_DENSE_PAIR
 #define CSA_DENSE_PAIR 1
 #endif

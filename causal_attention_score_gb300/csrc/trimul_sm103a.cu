@@ -14,7 +14,9 @@
 //    "fill" tiles that only receive the mask pattern (not written at all in
 //    lower-only mode). The lower tiles form the work list that the producer,
 //    MMA and epilogue warps walk; the fill tiles form a separate launch-wide
-//    pool (warp 10).
+//    pool (warp 10). With fill tiles, CTAs take work-list positions from a
+//    per-launch counter; otherwise (lower-only, the batched NT product) they
+//    are dealt statically and the counters are never touched.
 //  - warp 0 (one lane): TMA producer. A 4-D tensor map (HS, 3*NH, T, B) over
 //    the packed QKV addresses the query of head h at index h and its key at
 //    NH + h; rows past T and columns past HS arrive zero-filled. Q and K tiles
@@ -27,7 +29,9 @@
 //    diagonal on diagonal tiles, stage through swizzled shared memory and
 //    issue 32 x 32 TMA stores (clipped at T). When T % 4 != 0 the output rows
 //    are not 16-byte aligned, so the same staged data is written with
-//    coalesced plain stores.
+//    coalesced plain stores. In lower-only mode the 32 x 32 boxes that straddle
+//    the diagonal are written by each lane from registers, its row's t2 <= t
+//    part only.
 //  - fp32 inputs ("kind::tf32" form, trimul_forward_f32): the referee's own
 //    input type, computed to fp32 accuracy with three tf32 products: each
 //    input x splits exactly into hi = x with its low 13 mantissa bits cleared
@@ -39,11 +43,15 @@
 //    row block lives in TMEM as the MMA's A operand: its hi and lo parts take
 //    2 * HS of the 512 columns beside the two accumulators, written once per
 //    row block by warps 11-14 (one per lane quarter, tcgen05.st) from Q
-//    chunks that pass through the ring, so the ring carries only K, one
-//    32-element chunk per stage with its lo part beside it (written by the
-//    same warps), and each CTA walks one contiguous run of the work list so
-//    that consecutive tiles share their Q. With 128 < HS <= 256 a stage holds
-//    one 32-element chunk of both Q and K and their lo parts.
+//    chunks that pass through the ring (two such Q buffers when HS <= 64, so
+//    the next row block's Q is written while the current one is in use). The
+//    ring then carries only K, one raw 32-element chunk per stage; the same
+//    warps split each into a three-slot ring of lo parts, and each CTA walks
+//    one contiguous run of the work list so that consecutive tiles share their
+//    Q. In full mode that path is its own instance with one staging box per
+//    epilogue warp, which leaves room for more ring stages. With
+//    128 < HS <= 256 a stage holds one 32-element chunk of both Q and K and
+//    their lo parts.
 //  - warp 10: fill writer. It takes fill tiles from the launch-wide pool while
 //    the epilogue has nothing to store (start-up, a wait on the MMA, after the
 //    last lower tile) and writes each as 128 x 16 TMA stores of a resident
