@@ -9,7 +9,7 @@
 // row softmax of the "Smallem" article 5 (row maximum and sum of exponentials,
 // then normalisation). The scores never reach global memory.
 //
-// Design (one persistent launch, one CTA per SM, 10 warps):
+// Design (one persistent launch, one CTA per SM, 11 warps):
 //  - work unit = one (b, h) row block of 128 query rows; units are taken from
 //    a per-launch counter, longest row blocks first.
 //  - warp 0: TMA producer. Per unit it loads the Q tile once (two buffers, so
@@ -28,8 +28,11 @@
 //    pool of 128 x 128 zero tiles, as 128 x 16 TMA stores of a zeroed shared
 //    buffer (plain stores when T % 4 != 0). It takes a tile only while its own
 //    epilogue is not storing (start-up, pass 1, after the last unit), two tiles
-//    in flight at most, so the SM's write stream has no gaps and the pool
-//    evens out the end of the launch across SMs.
+//    in flight at most, and no more than its share of the pool: (Tt - 1) /
+//    (Tt + 1) zero tiles per pass-1 tile its epilogue has started (Tt = tiles
+//    per row), plus a slack of two, until the epilogue has no more units. So
+//    the SM's write stream has no gaps, and the pool lasts into the second half
+//    of the launch and evens out its end across SMs.
 //  - Writes saturate HBM and queue ahead of reads, so the producer prefetches
 //    the next unit's Q and first K tiles into L2 a whole unit early; K is kept
 //    in L2 (every row block of its (b, h) reads it, twice), the output is not.

@@ -42,3 +42,19 @@ def test_algorithmic_bytes():
     assert bench.trimul_algorithmic_bytes(8, 1024, 768, 12) == 8 * 12 * 1024 * 1024 * 4 + 2 * 8 * 1024 * 768 * 2
     assert bench.trimul_algorithmic_bytes(1, 4, 8, 1, lower_only=True) == 10 * 4 + 2 * 4 * 8 * 2
     assert bench.dense_algorithmic_bytes(960, 770, 768) == (960 + 768) * 770 * 2 + 960 * 768 * 4
+
+
+def test_traffic_record_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
+    """roofline.traffic is taken from a committed ncu record only while the score
+    kernel's code is the one it was captured on: a comment edit keeps it, a code
+    edit drops it."""
+    src = tmp_path / "k.cu"
+    src.write_text("// a kernel\n__global__ void k(int* p) { p[0] = 1; }  /* tail */\n")
+    monkeypatch.setattr(bench, "KERNEL_SOURCES", [str(src)])
+    h0 = bench.kernel_source_hash()
+    src.write_text("// a kernel, described at length\n/* block\n comment */\n"
+                   "__global__ void k(int* p) {\n  p[0] = 1;  // store\n}\n")
+    assert bench.kernel_source_hash() == h0
+    src.write_text("// a kernel\n__global__ void k(int* p) { p[0] = 2; }\n")
+    assert bench.kernel_source_hash() != h0
+
