@@ -371,7 +371,8 @@ def make_workload(name, dev):
         Xs = [X_h.to(dev) for X_h in xs_h]
         Ys = [torch.empty((X.shape[0], H), dtype=torch.float32, device=dev) for X in Xs]
         flops = sum(dense_flops(X.shape[0], I, H) for X in Xs)
-        fn = lambda st: csa.dense_xwt_grouped(Ys, Xs, W, I, H, stream=st)
+        plan = csa.DenseGroupedPlan(Ys, Xs, W, I, H)  # tensors checked once
+        fn = lambda st: plan(stream=st)
         return finish("dense dynamic-shape sweep, grouped: the same 32 problems (M = 16*T, "
                       "T ~ U{1..128}, seed 0, I=768, H=3072) in one dense_xwt_grouped launch",
                       {"dense_sweep": {"calls": len(xs_h), "I": I, "H": H, "grouped": True}},

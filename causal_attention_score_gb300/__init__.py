@@ -5,7 +5,8 @@ Public API (all compute runs in libcsa_gb300.so; see include/csa.h):
 * ``trimul_forward(out, qkv, B, T, C, NH, mask="nan", lower_only=False)``
 * ``trimul_forward_f32(out, qkv_f32, B, T, C, NH, mask="nan", lower_only=False)``
 * ``dense_xwt(Y, X, W, M, I, H)`` and ``dense_xwt_grouped(Ys, Xs, W, I, H)`` (many
-  ragged X against one shared W in one launch per 48 problems)
+  ragged X against one shared W in one launch per 48 problems; ``DenseGroupedPlan``
+  checks the tensors once for repeated calls)
 * ``batch_matmul_nt(Y, X, W, batch, T1, T2, D)``
 * ``causal_softmax_forward(att, qkv, B, T, C, NH)``
 * allocating helpers ``trimul(qkv)``, ``causal_softmax(qkv)`` and ``dense(X, W)``
@@ -17,14 +18,14 @@ The library is loaded on first use; importing this package needs no GPU.
 from ._lib import (CSA_ERR_ALIGN, CSA_ERR_ARCH, CSA_ERR_CUDA, CSA_ERR_LAUNCH, CSA_ERR_NULL,
                    CSA_ERR_SHAPE, CSA_ERR_TIMEOUT, CSA_ERR_UNSUPPORTED, CSA_MASK_NAN,
                    CSA_MASK_NEG_INF, CSA_OK, CsaError)
-from .ops import (DENSE_FETCH_AUTO, DENSE_FETCH_LOADERS, batch_matmul_nt, causal_softmax,
-                  causal_softmax_forward, debug_inject, dense, dense_xwt, dense_xwt_grouped,
-                  get_status, set_dense_fetch, set_wait_limit_ns, trimul, trimul_forward,
-                  trimul_forward_f32, version)
+from .ops import (DENSE_FETCH_AUTO, DENSE_FETCH_LOADERS, DenseGroupedPlan, batch_matmul_nt,
+                  causal_softmax, causal_softmax_forward, debug_inject, dense, dense_xwt,
+                  dense_xwt_grouped, get_status, set_dense_fetch, set_wait_limit_ns, trimul,
+                  trimul_forward, trimul_forward_f32, version)
 
 __all__ = [
-    "trimul_forward", "trimul_forward_f32", "dense_xwt", "dense_xwt_grouped", "batch_matmul_nt",
-    "causal_softmax_forward", "causal_softmax", "trimul", "dense", "get_status",
+    "trimul_forward", "trimul_forward_f32", "dense_xwt", "dense_xwt_grouped", "DenseGroupedPlan",
+    "batch_matmul_nt", "causal_softmax_forward", "causal_softmax", "trimul", "dense", "get_status",
     "set_wait_limit_ns", "debug_inject", "set_dense_fetch", "DENSE_FETCH_AUTO",
     "DENSE_FETCH_LOADERS", "version", "CsaError", "CSA_OK", "CSA_ERR_NULL", "CSA_ERR_SHAPE",
     "CSA_ERR_ALIGN", "CSA_ERR_UNSUPPORTED", "CSA_ERR_ARCH", "CSA_ERR_LAUNCH", "CSA_ERR_TIMEOUT",

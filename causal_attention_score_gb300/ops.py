@@ -74,29 +74,50 @@ def dense_xwt(Y: torch.Tensor, X: torch.Tensor, W: torch.Tensor, M: int, I: int,
     _lib.check(rc, "dense_xwt")
 
 
+class DenseGroupedPlan:
+    """dense_xwt_grouped with its arguments checked and marshalled once.
+
+    Calling the plan launches Y[g] = X[g] W^T for every g on ``stream``; a call costs
+    one C call plus a check that every tensor still has the storage it was planned
+    with, instead of the full per-tensor checks (which take longer than the launch
+    itself for a few dozen problems). The plan keeps references to its tensors.
+    """
+
+    def __init__(self, Ys, Xs, W: torch.Tensor, I: int, H: int):
+        import ctypes
+        if len(Ys) != len(Xs) or not Xs:
+            raise ValueError("Ys and Xs must be non-empty lists of the same length")
+        _need(W, "W", torch.bfloat16, H * I)
+        Ms = []
+        for g, (Y, X) in enumerate(zip(Ys, Xs)):
+            if X.dim() != 2 or X.shape[1] != I:
+                raise ValueError(f"X[{g}] must be [M, {I}]")
+            M = int(X.shape[0])
+            _need(X, f"X[{g}]", torch.bfloat16, M * I)
+            _need(Y, f"Y[{g}]", torch.float32, M * H)
+            Ms.append(M)
+        n = len(Xs)
+        self._tensors = [W] + list(Ys) + list(Xs)
+        self._ptrs = [t.data_ptr() for t in self._tensors]
+        self._y = (ctypes.c_void_p * n)(*[Y.data_ptr() for Y in Ys])
+        self._x = (ctypes.c_void_p * n)(*[X.data_ptr() for X in Xs])
+        self._m = (ctypes.c_int * n)(*Ms)
+        self._args = (ctypes.addressof(self._y), ctypes.addressof(self._x), W.data_ptr(),
+                      ctypes.addressof(self._m), n, I, H)
+
+    def __call__(self, stream=None) -> None:
+        if [t.data_ptr() for t in self._tensors] != self._ptrs:
+            raise ValueError("a tensor of this DenseGroupedPlan no longer has the storage it "
+                             "was planned with; make a new plan")
+        rc = _lib.load().dense_xwt_grouped(*self._args, _stream_ptr(stream))
+        _lib.check(rc, "dense_xwt_grouped")
+
+
 def dense_xwt_grouped(Ys, Xs, W: torch.Tensor, I: int, H: int, stream=None) -> None:
     """Y[g] = X[g] W^T for every g, one launch per 48 problems: fp32 Y[g] [M_g, H] from
-    bf16 X[g] [M_g, I] and the shared W [H, I]; see dense_xwt_grouped in include/csa.h."""
-    import ctypes
-    if len(Ys) != len(Xs) or not Xs:
-        raise ValueError("Ys and Xs must be non-empty lists of the same length")
-    _need(W, "W", torch.bfloat16, H * I)
-    Ms = []
-    for g, (Y, X) in enumerate(zip(Ys, Xs)):
-        if X.dim() != 2 or X.shape[1] != I:
-            raise ValueError(f"X[{g}] must be [M, {I}]")
-        M = int(X.shape[0])
-        _need(X, f"X[{g}]", torch.bfloat16, M * I)
-        _need(Y, f"Y[{g}]", torch.float32, M * H)
-        Ms.append(M)
-    n = len(Xs)
-    y_arr = (ctypes.c_void_p * n)(*[Y.data_ptr() for Y in Ys])
-    x_arr = (ctypes.c_void_p * n)(*[X.data_ptr() for X in Xs])
-    m_arr = (ctypes.c_int * n)(*Ms)
-    rc = _lib.load().dense_xwt_grouped(ctypes.addressof(y_arr), ctypes.addressof(x_arr),
-                                       W.data_ptr(), ctypes.addressof(m_arr), n, I, H,
-                                       _stream_ptr(stream))
-    _lib.check(rc, "dense_xwt_grouped")
+    bf16 X[g] [M_g, I] and the shared W [H, I]; see dense_xwt_grouped in include/csa.h.
+    For repeated calls on the same tensors, DenseGroupedPlan checks them once."""
+    DenseGroupedPlan(Ys, Xs, W, I, H)(stream)
 
 
 def batch_matmul_nt(Y: torch.Tensor, X: torch.Tensor, W: torch.Tensor, batch: int, T1: int,

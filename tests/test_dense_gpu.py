@@ -276,3 +276,27 @@ def test_dense_grouped_graph_replay():
     assert csa.get_status() == 0
     for a, b in zip(Yg, ref):
         assert np.array_equal(f32_bits(a), f32_bits(b))
+
+
+def test_dense_grouped_plan_repeats_and_notices_new_storage():
+    """A DenseGroupedPlan launches the same products as dense_xwt_grouped, call after
+    call, and refuses to run once one of its tensors has new storage."""
+    xs, W = synth.dense_sweep_inputs(seed=0)
+    H, I = W.shape
+    Wd = W.cuda()
+    Xd = [X.cuda() for X in xs[:6]]
+    ref = [poisoned((X.shape[0], H)) for X in Xd]
+    csa.dense_xwt_grouped(ref, Xd, Wd, I, H)
+    Yp = [poisoned((X.shape[0], H)) for X in Xd]
+    plan = csa.DenseGroupedPlan(Yp, Xd, Wd, I, H)
+    for _ in range(3):
+        for Y in Yp:
+            Y.fill_(float("nan"))
+        plan()
+    torch.cuda.synchronize()
+    assert csa.get_status() == 0
+    for a, b in zip(Yp, ref):
+        assert np.array_equal(f32_bits(a), f32_bits(b))
+    Yp[2].set_(torch.empty_like(Yp[2]))  # the tensor now points at other memory
+    with pytest.raises(ValueError):
+        plan()
