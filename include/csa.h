@@ -2,7 +2,13 @@
  * csa.h -- C ABI of the GB300 (sm_103a) causal-attention-score library,
  * libcsa_gb300.so.
  *
- * Two products, each one persistent tcgen05/TMA kernel launch per call:
+ * Two products, each a persistent tcgen05/TMA kernel (plus, for dense rows no
+ * tensor map can describe, one realigning copy launched before it), and the
+ * calls built on them: the batched NT product (batch_matmul_nt), the fused
+ * causal softmax of the scores (causal_softmax_forward), the score product
+ * over fp32 inputs (trimul_forward_f32), many dense layers sharing W in one
+ * launch (dense_xwt_grouped), and an allocation-free score entry point
+ * (trimul_forward_noalloc). Each is documented at its declaration below.
  *
  *  trimul_forward  the causal triangular score product of
  *                  "llm.c dev/cuda/trimat_forward.cu" (the CPU referee
@@ -133,7 +139,8 @@ csa_status trimul_forward_f32(float* out, const float* qkv, int B, int T, int C,
  * synchronisation cudaFree brings, or in plug-in hosts that only hand out
  * buffers. trimul_forward_ex itself never calls cudaMalloc either, but keeps
  * per-launch scheduling counters in a ring of slots; this variant instead
- * keeps its scratch -- the kernel's two work-list counters -- in one fixed
+ * keeps its scratch -- the kernel's work-list counters (next position,
+ * finished CTAs, next fill tile) -- in one fixed
  * 256-byte device array that every GPU loading the library holds until exit,
  * and calls no cudaMalloc, cudaFree or allocating library routine.
  *
