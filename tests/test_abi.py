@@ -88,6 +88,26 @@ def test_binding_refuses_cpu_tensors(lib):
         csa.trimul_forward(out, qkv, 1, 4, 8, 1)
 
 
+def test_grouped_plan_checks_its_arguments_on_the_host(lib):
+    """DenseGroupedPlan refuses bad arguments before anything reaches the library:
+    unequal or empty lists, a wrong row length, CPU tensors."""
+    import torch
+    import causal_attention_score_gb300 as csa
+    W = torch.zeros((8, 16), dtype=torch.bfloat16)
+    X = torch.zeros((3, 16), dtype=torch.bfloat16)
+    Y = torch.zeros((3, 8))
+    with pytest.raises(ValueError):
+        csa.DenseGroupedPlan([Y, Y], [X], W, 16, 8)
+    with pytest.raises(ValueError):
+        csa.DenseGroupedPlan([], [], W, 16, 8)
+    with pytest.raises(ValueError):
+        csa.DenseGroupedPlan([Y], [torch.zeros((3, 15), dtype=torch.bfloat16)], W, 16, 8)
+    with pytest.raises(ValueError):  # W (and X, Y) on the CPU
+        csa.DenseGroupedPlan([Y], [X], W, 16, 8)
+    with pytest.raises(ValueError):
+        csa.dense_xwt_grouped([Y], [X], W, 16, 8)
+
+
 @pytest.mark.parametrize("args,code", [
     ((None, 16, 1, 1, 8, 1, 0, 0, None), _lib.CSA_ERR_NULL),
     ((16, 16, 1, 1, 10, 3, 0, 0, None), _lib.CSA_ERR_SHAPE),
