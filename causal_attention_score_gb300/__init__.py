@@ -15,9 +15,9 @@ Public API (all compute runs in libcsa_gb300.so; see include/csa.h):
 
 The library is loaded on first use; importing this package needs no GPU.
 """
-from ._lib import (CSA_ERR_ALIGN, CSA_ERR_ARCH, CSA_ERR_CUDA, CSA_ERR_LAUNCH, CSA_ERR_NULL,
-                   CSA_ERR_SHAPE, CSA_ERR_TIMEOUT, CSA_ERR_UNSUPPORTED, CSA_MASK_NAN,
-                   CSA_MASK_NEG_INF, CSA_OK, CsaError)
+from ._lib import (CSA_ERR_ALIGN, CSA_ERR_ARCH, CSA_ERR_CHECK, CSA_ERR_CUDA, CSA_ERR_LAUNCH,
+                   CSA_ERR_NULL, CSA_ERR_SHAPE, CSA_ERR_TIMEOUT, CSA_ERR_UNSUPPORTED,
+                   CSA_MASK_NAN, CSA_MASK_NEG_INF, CSA_OK, CsaError)
 from .ops import (DENSE_FETCH_AUTO, DENSE_FETCH_LOADERS, DenseGroupedPlan, batch_matmul_nt,
                   causal_softmax, causal_softmax_forward, debug_inject, dense, dense_xwt,
                   dense_xwt_grouped, get_status, set_dense_fetch, set_wait_limit_ns, trimul,
@@ -29,5 +29,5 @@ __all__ = [
     "set_wait_limit_ns", "debug_inject", "set_dense_fetch", "DENSE_FETCH_AUTO",
     "DENSE_FETCH_LOADERS", "version", "CsaError", "CSA_OK", "CSA_ERR_NULL", "CSA_ERR_SHAPE",
     "CSA_ERR_ALIGN", "CSA_ERR_UNSUPPORTED", "CSA_ERR_ARCH", "CSA_ERR_LAUNCH", "CSA_ERR_TIMEOUT",
-    "CSA_ERR_CUDA", "CSA_MASK_NAN", "CSA_MASK_NEG_INF",
+    "CSA_ERR_CUDA", "CSA_ERR_CHECK", "CSA_MASK_NAN", "CSA_MASK_NEG_INF",
 ]

@@ -20,6 +20,7 @@ CSA_ERR_ARCH = -5
 CSA_ERR_LAUNCH = -6
 CSA_ERR_TIMEOUT = -7
 CSA_ERR_CUDA = -8
+CSA_ERR_CHECK = -9
 
 CSA_MASK_NAN = 0x7FC00000
 CSA_MASK_NEG_INF = 0xFF800000

@@ -3,6 +3,9 @@
 Each ``csrc/*.cu`` is compiled to an object in parallel, then linked into a
 shared library with the CUDA runtime linked statically (so loading the
 library needs no GPU and no libcuda; the driver is reached at first use).
+``build(debug=True)`` makes libcsa_gb300_debug.so from the same sources with
+-DCSA_DEBUG: the kernels then check tile indices, ring indices and TMEM column
+ranges on the device and report a failed check as CSA_ERR_CHECK.
 """
 from __future__ import annotations
 
@@ -20,6 +23,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIBNAME = "libcsa_gb300.so"
 LIBPATH = os.path.join(PKG, LIBNAME)
+DEBUG_LIBPATH = os.path.join(PKG, "libcsa_gb300_debug.so")
+DEBUG_BUILD = os.path.join(PKG, "_build_debug")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -44,16 +49,17 @@ def _deps():
             + glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)])
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIBPATH):
+def up_to_date(path: str = LIBPATH) -> bool:
+    if not os.path.exists(path):
         return False
-    t = os.path.getmtime(LIBPATH)
+    t = os.path.getmtime(path)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def _compile(src: str, verbose_ptxas: bool) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
-    extra = ["-Xptxas", "-v"] if verbose_ptxas else []
+def _compile(src: str, verbose_ptxas: bool, debug: bool = False) -> str:
+    obj = os.path.join(DEBUG_BUILD if debug else BUILD,
+                       os.path.basename(src).replace(".cu", ".o"))
+    extra = (["-Xptxas", "-v"] if verbose_ptxas else []) + (["-DCSA_DEBUG"] if debug else [])
     cmd = [nvcc(), *_flags(extra), "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -63,22 +69,25 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Compile and link the library if any source changed; returns its path."""
-    if not force and up_to_date():
-        return LIBPATH
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, debug: bool = False) -> str:
+    """Compile and link the library (or, with debug=True, its checking variant) if any
+    source changed; returns its path."""
+    path = DEBUG_LIBPATH if debug else LIBPATH
+    if not force and up_to_date(path):
+        return path
+    os.makedirs(DEBUG_BUILD if debug else BUILD, exist_ok=True)
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), srcs))
-    tmp = LIBPATH + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas, debug), srcs))
+    tmp = path + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIBPATH)
-    return LIBPATH
+    os.replace(tmp, path)
+    return path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv,
+                debug="--debug" in sys.argv))

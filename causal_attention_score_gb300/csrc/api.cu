@@ -433,6 +433,7 @@ const char* csa_status_string(csa_status s) {
     case CSA_ERR_LAUNCH: return "kernel launch failed";
     case CSA_ERR_TIMEOUT: return "device-side wait ran out";
     case CSA_ERR_CUDA: return "CUDA call failed";
+    case CSA_ERR_CHECK: return "device-side index check failed (debug build)";
     default: return "unknown status";
   }
 }

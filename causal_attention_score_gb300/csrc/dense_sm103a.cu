@@ -223,6 +223,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       nb = static_cast<int>(t / a.m_tiles);
     }
   };
+#ifdef CSA_DEBUG
+  // A located tile lies inside the launch's problems and n-tiles (with kPair the
+  // phantom half past the last m-tile is allowed).
+  auto tile_ok = [&](int p, int mb, int nb) {
+    int n = 1;
+    if constexpr (kGrouped) n = g.n;
+    return p >= 0 && p < n && mb >= 0 && nb >= 0 && nb < a.n_tiles &&
+           (kGrouped || mb < a.m_tiles);
+  };
+#endif
   auto map_x = [&](int p) -> const CUtensorMap* {
     if constexpr (kGrouped) return &g.x[p];
     else return &tmap_x;
@@ -294,6 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (long long tile = t_first; tile < a.num_tiles && !*abort_flag; tile += t_step) {
           int p, mb, nb;
           locate(tile, p, mb, nb);
+          if (!CSA_CHECK(tile_ok(p, mb, nb), wd, kCheckTile)) break;
           const CUtensorMap* mx = map_x(p);
           bool ok = true;
           for (int kb = 0; kb < a.kblocks; ++kb) {
@@ -430,6 +441,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (long long tile = t_first; issuer && tile < a.num_tiles; tile += t_step) {
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, wd, kSiteMmaTmemEmpty)) break;
         tc_fence_after_sync();
+        if (!CSA_CHECK(acc >= 0 && (acc + 1) * a.BN <= static_cast<int>(a.tmem_cols), wd,
+                       kCheckTmem))
+          break;
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * a.BN);
         bool ok = true;
         for (int kb = 0; kb < a.kblocks; ++kb) {
@@ -485,6 +499,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (long long tile = t_first; tile < a.num_tiles; tile += t_step) {
       int p, mb, nb;
       locate(tile, p, mb, nb);
+      if (!CSA_CHECK(tile_ok(p, mb, nb) &&
+                         (acc + 1) * a.BN <= static_cast<int>(a.tmem_cols),
+                     wd, kCheckTile))
+        break;
       const int M = rows_of(p);
       if (!mbar_wait_warp(tfull_bar(acc), acc_phase, wd, kSiteEpilogueFull)) break;
       tc_fence_after_sync();

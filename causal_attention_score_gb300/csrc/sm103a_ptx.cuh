@@ -46,6 +46,32 @@ struct Watchdog {
   volatile int* abort_flag;  // shared memory, per CTA
 };
 
+// Debug builds (-DCSA_DEBUG) check tile indices, ring indices and TMEM column
+// ranges on the device before they are used. A failed check records
+// CSA_ERR_CHECK and its site in the status word and sets the CTA's abort flag:
+// the role skips the access the check guards and the CTA unwinds as after a
+// timeout. In release builds CSA_CHECK is the constant true and no check code
+// exists.
+enum CheckSite : int {
+  kCheckTile = 101,   // a work position decoded outside its problem's tiles
+  kCheckTmem = 102,   // a TMEM column range outside the allocation
+  kCheckRing = 103,   // a ring stage or accumulator index outside its ring
+};
+
+__device__ __forceinline__ bool debug_check(bool ok, const Watchdog& wd, int site) {
+  if (!ok) {
+    *wd.abort_flag = 1;
+    if (atomicCAS(wd.status, 0, CSA_ERR_CHECK) == 0) atomicExch(wd.status + 1, site);
+  }
+  return ok;
+}
+
+#ifdef CSA_DEBUG
+#define CSA_CHECK(cond, wd, site) ::csa::debug_check((cond), (wd), (site))
+#else
+#define CSA_CHECK(cond, wd, site) true
+#endif
+
 // ------------------------------------------------- programmatic launches --
 // With a programmatic launch the kernel may start while the one before it in
 // the stream is still running; it must not touch global memory before the wait

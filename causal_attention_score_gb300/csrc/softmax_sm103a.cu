@@ -246,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (done) break;
         int bh, ti;
         decode_unit(cur, a, bh, ti);
+        if (!CSA_CHECK(bh >= 0 && bh < a.BH && ti >= 0 && ti < a.Tt, wd, kCheckTile)) break;
         const int b = bh / a.NH, h = bh - b * a.NH;
         if (!mbar_wait(qempty_bar(qb), qphase ^ 1u, wd, kSiteProducerEmpty)) break;
         mbar_arrive_expect_tx(qfull_bar(qb), qtx);
@@ -323,6 +324,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after_sync();
+            if (!CSA_CHECK(acc >= 0 && (acc + 1) * kTile <= kTmemCols, wd, kCheckTmem)) {
+              ok = false;
+              break;
+            }
             const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kTile);
             for (int k = 0; k < a.ksteps; ++k) {
               const uint32_t off = static_cast<uint32_t>(k & 3) * 32u;
@@ -403,6 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int w = z / a.BH;
       const int bh = z - w * a.BH;
       const int pr = w / Tt, o = w - pr * Tt;
+      if (!CSA_CHECK(bh >= 0 && bh < a.BH && pr >= 0 && pr < Tt, wd, kCheckTile)) break;
       int ti, tj;
       if (o < Tt - 1 - pr) {
         ti = pr;
@@ -467,6 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int bh, ti;
       decode_unit(cur, a, bh, ti);
+      if (!CSA_CHECK(bh >= 0 && bh < a.BH && ti >= 0 && ti < a.Tt, wd, kCheckTile)) break;
       if (ew == 0 && lane == 0) *p1_started = *p1_started + ti + 1;
       const int row0 = ti * kTile + q * 32;
       const int r = row0 + static_cast<int>(lane);

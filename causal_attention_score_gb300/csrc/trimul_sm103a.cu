@@ -373,6 +373,10 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
         int bh, r, ti, tj;
         decode_position(static_cast<int>(cur), a.per_lower, bh, r);
         decode_computed(r, a.causal, a.Tt2, ti, tj);
+        if (!CSA_CHECK(bh >= 0 && bh < a.BH && ti >= 0 && ti < a.Tt && tj >= 0 && tj < a.Tt2 &&
+                           stage >= 0 && stage < a.stages,
+                       wd, kCheckTile))
+          break;
         const int outer = bh / a.nh_div, inner = bh - outer * a.nh_div;
         // Q in TMEM: a new row block first sends its Q chunks through the ring.
         const bool new_q = kF32 && a.q_tmem && (bh != q_bh || ti != q_ti);
@@ -491,6 +495,10 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
         }
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, wd, kSiteMmaTmemEmpty)) break;
         tc_fence_after_sync();
+        if (!CSA_CHECK(acc >= 0 && (acc + 1) * kTile <= static_cast<int>(a.tmem_cols) &&
+                           (!a.q_tmem || qlo_col(qbuf) + q_cols <= a.tmem_cols),
+                       wd, kCheckTmem))
+          break;
         const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kTile);
         bool ok = true;
         for (int ts = 0; ts < a.tile_stages; ++ts) {
@@ -729,6 +737,7 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
       const int bh = f / a.per_fill;
       int ti, tj;
       decode_fill(f - bh * a.per_fill, ti, tj);
+      if (!CSA_CHECK(bh < a.BH && ti >= 0 && ti < tj && tj < a.Tt, wd, kCheckTile)) break;
       const int r0 = ti * kTile, c0 = tj * kTile;  // rows r0.. are all < T (ti < tj)
       if (a.tma_store) {
         if (lane == 0) {
@@ -787,6 +796,10 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
       int bh, rank, ti, tj;
       decode_position(static_cast<int>(cur), a.per_lower, bh, rank);
       decode_computed(rank, a.causal, a.Tt2, ti, tj);
+      if (!CSA_CHECK(bh >= 0 && bh < a.BH && ti >= 0 && ti < a.Tt && tj >= 0 && tj < a.Tt2 &&
+                         acc * kTile + (slab + 1) * kSlabCols <= static_cast<int>(a.tmem_cols),
+                     wd, kCheckTile))
+        break;
       const int row0 = ti * kTile + q * 32;
       const int colw = tj * kTile + slab * kSlabCols;
 

@@ -63,6 +63,8 @@ typedef int csa_status;
 #define CSA_ERR_LAUNCH        -6  /* the kernel launch failed (see csa_last_error) */
 #define CSA_ERR_TIMEOUT       -7  /* a device-side bounded wait ran out (csa_get_status) */
 #define CSA_ERR_CUDA          -8  /* a CUDA runtime/driver call failed (no device, ...) */
+#define CSA_ERR_CHECK         -9  /* a device-side index check of a debug build (built with
+                                     -DCSA_DEBUG) failed (reported by csa_get_status) */
 
 /* Causal mask bit patterns for the upper triangle (t2 > t). The page writes
  * NAN (the float quiet NaN, 0x7FC00000) and notes -inf would also do. */

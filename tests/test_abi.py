@@ -33,9 +33,21 @@ def test_every_declared_symbol_is_exported(lib):
         assert n in _lib.SIGNATURES, f"{n} has no ctypes signature in the binding"
 
 
+def test_checking_build_compiles_and_exports_every_symbol():
+    """The -DCSA_DEBUG variant (device-side index checks) builds from the same
+    sources and exports the same C ABI."""
+    path = build_lib.build(debug=True)
+    dbg = ctypes.CDLL(path)
+    for n in _declared_functions():
+        assert hasattr(dbg, n), f"{n} missing from the checking build"
+    dbg.csa_status_string.restype = ctypes.c_char_p
+    assert b"check" in dbg.csa_status_string(_lib.CSA_ERR_CHECK)
+
+
 def test_status_strings(lib):
-    for code in range(-8, 1):
+    for code in range(-9, 1):
         assert lib.csa_status_string(code)
+        assert lib.csa_status_string(code) != b"unknown status"
     assert lib.csa_version().decode().endswith("sm_103a")
 
 
