@@ -216,6 +216,15 @@ def recorded_traffic():
         return None
 
 
+def _percentile(xs, q):
+    """q-th percentile (linear interpolation) of a non-empty list."""
+    v = sorted(xs)
+    pos = (len(v) - 1) * q / 100.0
+    lo = int(math.floor(pos))
+    hi = min(lo + 1, len(v) - 1)
+    return v[lo] + (v[hi] - v[lo]) * (pos - lo)
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -588,6 +597,8 @@ def run_ours(args, rank, world, local):
                 "pipeline": "two lanes (stream + buffers each) take alternate steps; each step "
                             "copies its inputs in and its results out"},
         "gpu_launches": wl.kernels_per_step * K,
+        "flops_per_step": wl.flops,
+        "ms_step_percentiles": {f"p{q}": round(_percentile(step_ms, q), 5) for q in (10, 50, 90)},
         "clocks": sampler.summary(),
         "wall_s_timed_region": round(wall, 4),
     }

@@ -58,3 +58,12 @@ def test_traffic_record_hash_ignores_comments_but_not_code(tmp_path, monkeypatch
     src.write_text("// a kernel\n__global__ void k(int* p) { p[0] = 2; }\n")
     assert bench.kernel_source_hash() != h0
 
+
+
+def test_step_time_percentiles_match_numpy():
+    import numpy as np
+    rng = np.random.default_rng(1)
+    for n in (1, 2, 7, 200):
+        xs = rng.uniform(0.05, 0.09, size=n).tolist()
+        for q in (10, 50, 90):
+            assert abs(bench._percentile(xs, q) - float(np.percentile(xs, q))) < 1e-12
