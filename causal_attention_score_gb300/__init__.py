@@ -10,7 +10,8 @@ Public API (all compute runs in libcsa_gb300.so; see include/csa.h):
 * ``batch_matmul_nt(Y, X, W, batch, T1, T2, D)``
 * ``causal_softmax_forward(att, qkv, B, T, C, NH)``
 * allocating helpers ``trimul(qkv)``, ``causal_softmax(qkv)`` and ``dense(X, W)``
-* ``get_status()`` for the device watchdog word, ``set_wait_limit_ns`` for its bound,
+* ``get_status()`` for the device watchdog word, ``set_wait_limit_ns`` /
+  ``get_wait_limit_ns`` for its bound (default 2 s, or ``CSA_WAIT_LIMIT_NS``),
   ``set_dense_fetch`` for the dense layer's operand fetch mode.
 
 The library is loaded on first use; importing this package needs no GPU.
@@ -20,14 +21,15 @@ from ._lib import (CSA_ERR_ALIGN, CSA_ERR_ARCH, CSA_ERR_CHECK, CSA_ERR_CUDA, CSA
                    CSA_MASK_NAN, CSA_MASK_NEG_INF, CSA_OK, CsaError)
 from .ops import (DENSE_FETCH_AUTO, DENSE_FETCH_LOADERS, DenseGroupedPlan, batch_matmul_nt,
                   causal_softmax, causal_softmax_forward, debug_inject, dense, dense_xwt,
-                  dense_xwt_grouped, get_status, set_dense_fetch, set_wait_limit_ns, trimul,
-                  trimul_forward, trimul_forward_f32, version)
+                  dense_xwt_grouped, get_status, get_wait_limit_ns, set_dense_fetch,
+                  set_wait_limit_ns, trimul, trimul_forward, trimul_forward_f32, version)
 
 __all__ = [
     "trimul_forward", "trimul_forward_f32", "dense_xwt", "dense_xwt_grouped", "DenseGroupedPlan",
     "batch_matmul_nt", "causal_softmax_forward", "causal_softmax", "trimul", "dense", "get_status",
-    "set_wait_limit_ns", "debug_inject", "set_dense_fetch", "DENSE_FETCH_AUTO",
-    "DENSE_FETCH_LOADERS", "version", "CsaError", "CSA_OK", "CSA_ERR_NULL", "CSA_ERR_SHAPE",
+    "set_wait_limit_ns", "get_wait_limit_ns", "debug_inject", "set_dense_fetch",
+    "DENSE_FETCH_AUTO", "DENSE_FETCH_LOADERS", "version", "CsaError", "CSA_OK", "CSA_ERR_NULL",
+    "CSA_ERR_SHAPE",
     "CSA_ERR_ALIGN", "CSA_ERR_UNSUPPORTED", "CSA_ERR_ARCH", "CSA_ERR_LAUNCH", "CSA_ERR_TIMEOUT",
     "CSA_ERR_CUDA", "CSA_ERR_CHECK", "CSA_MASK_NAN", "CSA_MASK_NEG_INF",
 ]

@@ -46,6 +46,7 @@ SIGNATURES = {
     "csa_last_error": (ctypes.c_char_p, []),
     "csa_version": (ctypes.c_char_p, []),
     "csa_set_wait_limit_ns": (None, [ctypes.c_uint64]),
+    "csa_get_wait_limit_ns": (ctypes.c_uint64, []),
     "csa_debug_inject": (None, [_i]),
     "csa_set_dense_fetch": (_i, [_i]),
 }

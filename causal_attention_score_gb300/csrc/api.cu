@@ -8,6 +8,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -213,9 +214,24 @@ int encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, con
   return CSA_OK;
 }
 
+// The default bound: CSA_WAIT_LIMIT_NS from the environment when it holds a
+// positive integer (read once), else 2 s.
+uint64_t default_wait_limit_ns() {
+  static const uint64_t v = [] {
+    const char* e = std::getenv("CSA_WAIT_LIMIT_NS");
+    if (e && *e) {
+      char* end = nullptr;
+      const unsigned long long x = std::strtoull(e, &end, 10);
+      if (end && *end == '\0' && x > 0) return static_cast<uint64_t>(x);
+    }
+    return kDefaultWaitLimitNs;
+  }();
+  return v;
+}
+
 uint64_t wait_limit_ns() {
   const uint64_t v = g_wait_limit_ns.load();
-  return v ? v : kDefaultWaitLimitNs;
+  return v ? v : default_wait_limit_ns();
 }
 
 bool take_inject() { return g_inject.exchange(0) != 0; }
@@ -443,6 +459,8 @@ const char* csa_last_error(void) { return t_last_error.c_str(); }
 const char* csa_version(void) { return "0.1.0 sm_103a"; }
 
 void csa_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns); }
+
+uint64_t csa_get_wait_limit_ns(void) { return csa::wait_limit_ns(); }
 
 void csa_debug_inject(int enable) { g_inject.store(enable ? 1 : 0); }
 

@@ -180,7 +180,14 @@ def get_status(stream=None) -> int:
 
 
 def set_wait_limit_ns(ns: int) -> None:
+    """Bound on every device-side wait (0 restores the default: 2 s, or the
+    environment variable CSA_WAIT_LIMIT_NS)."""
     _lib.load().csa_set_wait_limit_ns(int(ns))
+
+
+def get_wait_limit_ns() -> int:
+    """The bound the next launch will use, in nanoseconds."""
+    return int(_lib.load().csa_get_wait_limit_ns())
 
 
 def debug_inject(enable: bool = True) -> None:

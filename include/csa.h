@@ -271,7 +271,10 @@ const char* csa_version(void);
  * Watchdog controls, for tests of the failure path (no GPU fault involved).
  *
  * csa_set_wait_limit_ns -- upper bound, in nanoseconds of %globaltimer, on
- *   every spin-wait inside the kernels (default 2e9 = 2 s; 0 restores it).
+ *   every spin-wait inside the kernels (0 restores the default: 2e9 = 2 s, or
+ *   the environment variable CSA_WAIT_LIMIT_NS when it holds a positive integer,
+ *   read once at the first launch or query).
+ * csa_get_wait_limit_ns -- the bound the next launch will use.
  * csa_debug_inject -- when nonzero, the next kernel launch (any entry point)
  *   withholds one hand-off in every CTA: the first operand load (score
  *   products, the softmax's first Q tile, the dense layer's TMA form) or the
@@ -280,6 +283,7 @@ const char* csa_version(void);
  *   output incomplete. Consumed by that launch.
  */
 void csa_set_wait_limit_ns(uint64_t ns);
+uint64_t csa_get_wait_limit_ns(void);
 void csa_debug_inject(int enable);
 
 #ifdef __cplusplus

@@ -217,3 +217,19 @@ def test_dense_grouped_null_arrays_and_no_device(lib):
         return
     assert lib.dense_xwt_grouped(ctypes.addressof(y), ctypes.addressof(x), 4096,
                                  ctypes.addressof(m), 1, 8, 8, None) == _lib.CSA_ERR_CUDA
+
+
+def test_wait_limit_default_setter_and_environment(lib):
+    """The watchdog bound: 2 s by default, set and restored through the API, and taken
+    from CSA_WAIT_LIMIT_NS when that holds a positive integer (a fresh process)."""
+    import subprocess
+    import sys
+    assert lib.csa_get_wait_limit_ns() == 2_000_000_000 or os.environ.get("CSA_WAIT_LIMIT_NS")
+    lib.csa_set_wait_limit_ns(12345)
+    assert lib.csa_get_wait_limit_ns() == 12345
+    lib.csa_set_wait_limit_ns(0)
+    code = ("import causal_attention_score_gb300 as c; print(c.get_wait_limit_ns())")
+    for env, want in (("50000000", 50_000_000), ("junk", 2_000_000_000), ("0", 2_000_000_000)):
+        out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True,
+                             text=True, env={**os.environ, "CSA_WAIT_LIMIT_NS": env}, check=True)
+        assert int(out.stdout.strip()) == want, (env, out.stdout, out.stderr)
