@@ -1,23 +1,30 @@
-"""Benchmark of the hot path: one step = one causal score product on the GPT-2-small
-shape plus one ragged dense layer, the two products of this library.
+"""Benchmark of the hot path. One step is one pass over every stage of the path on the
+largest configurations the pages give:
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--graph]
 
-Workload (seeded synthetic data, resident in HBM before timing):
-  trimul_forward  QKV bf16 (B=8, T=1024, 3, NH=12, HS=64) N(0,1) seed 0 -> fp32 (8, 12, 1024, 1024)
-                  (the shape of the "llm.c dev/cuda/trimat_forward.cu" main);
-  dense_xwt       X [960, 770], W [768, 770] bf16 uniform[-1,1] seed 0 -> fp32 Y [960, 768]
-                  (B*T = 16*60 and I = 770 of "DietCode ... test_local_padding").
+Default step (workload "step"; seeded synthetic data, resident in HBM before timing):
+  trimul_forward     the causal scores of QKV bf16 (B=2, T=4096, 3, NH=16, HS=128), N(0,1)
+                     seed 0 -> fp32 (2, 16, 4096, 4096), NaN above the diagonal (the long
+                     context; the score product of "llm.c dev/cuda/trimat_forward.cu");
+  dense_xwt_grouped  the dynamic-shape sweep: 32 problems X_i [16*T_i, 768], T_i ~ U{1..128}
+                     (seed 0), X_i uniform[-1,1] (seed 1000+i), sharing W [3072, 768]
+                     (uniform[-1,1], seed 1), in one launch;
+  dense_xwt          the ragged layer X [960, 770], W [768, 770], uniform[-1,1] seed 0
+                     (B*T = 16*60 and I = 770 of "DietCode ... test_local_padding").
 Metric: useful TFLOP/s = (lower-triangle flops 2*HS*B*NH*T(T+1)/2 + dense flops 2*M*I*H)
-per step / step time. L2 is flushed (256 MiB write) between timed steps, outside the
-timed events; the timed region has one event before and one after each step. For a step
-of several parts, the per-part times (`parts`) and the roofline kernel's launch duration
-come from a second pass of the same K steps with an event after each part. Rank 0 prints
-one JSON line.
+per step / step time. L2 is flushed (256 MiB write) between timed steps, outside the timed
+events; the timed region has one event before and one after each step. Before it, the step
+runs back to back for a clock soak (--soak-ms) so that the timed steps see steady clocks;
+NVML clock samples are taken through the soak and the timed region. Per-part times (and
+each kernel's launch duration, the `rooflines` entries) come from a second pass of the same
+K steps with an event after each part; the sweep's 32 problems are also timed as 32
+separate dense_xwt calls in a third pass (`sweep_calls`). Rank 0 prints one JSON line.
 
 --impl reference times the fp64 CPU oracle (the only other implementation of the
-method; the pages ship no runnable GPU code) on the host cores, on a bounded
-sample of the same workload per step, and prints the same line.
+method; the pages ship no runnable GPU code) on the host cores, each step a bounded
+sample (1/32) of the same workload, and prints the same line.
 """
 from __future__ import annotations
 
@@ -179,18 +186,26 @@ def nvml_index(local_rank: int) -> int:
     return local_rank
 
 
+CSRC = os.path.join(ROOT, "causal_attention_score_gb300", "csrc")
+KERNEL_SOURCES = [os.path.join(CSRC, f) for f in ("trimul_sm103a.cu", "sm103a_ptx.cuh")]
+DENSE_SOURCES = [os.path.join(CSRC, f) for f in ("dense_sm103a.cu", "sm103a_ptx.cuh")]
+# Committed ncu records of DRAM bytes per launch: record name -> (file, kernel sources).
+TRAFFIC_RECORDS = {
+    "trimul_long": ("trimul_long_dram_traffic.txt", "KERNEL_SOURCES"),
+    "trimul_gpt2": ("trimul_gpt2_dram_traffic.txt", "KERNEL_SOURCES"),
+    "dense_sweep_grouped": ("dense_sweep_grouped_dram_traffic.txt", "DENSE_SOURCES"),
+    "dense_ragged": ("dense_ragged_dram_traffic.txt", "DENSE_SOURCES"),
+}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "trimul_gpt2_dram_traffic.txt")
-KERNEL_SOURCES = [os.path.join(ROOT, "causal_attention_score_gb300", "csrc", f)
-                  for f in ("trimul_sm103a.cu", "sm103a_ptx.cuh")]
 
 
-def kernel_source_hash() -> str:
-    """Hash of the score kernel's code with comments and blank space removed, so that
-    an edit of its comments keeps a traffic record taken on the same code."""
+def kernel_source_hash(sources=None) -> str:
+    """Hash of a kernel's code with comments and blank space removed, so that an edit
+    of its comments keeps a traffic record taken on the same code."""
     import hashlib
     import re
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in (KERNEL_SOURCES if sources is None else sources):
         with open(f, encoding="utf-8") as fh:
             src = fh.read()
         src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)  # block comments
@@ -199,17 +214,19 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """DRAM bytes (read + write) per trimul launch from the committed ncu summary,
-    or None when there is none or the kernel source changed since it was taken."""
+def recorded_traffic(record: str = "trimul_gpt2"):
+    """DRAM bytes (read + write) per launch from a committed ncu summary, or None when
+    there is none or the kernel's code changed since it was taken."""
+    fname, sources = TRAFFIC_RECORDS[record]
+    path = TRAFFIC_FILE if record == "trimul_gpt2" else os.path.join(ROOT, "profiles", fname)
     try:
         kv = {}
-        with open(TRAFFIC_FILE) as f:
+        with open(path) as f:
             for line in f:
                 if ":" in line and not line.startswith("#"):
                     k, v = line.split(":", 1)
                     kv[k.strip()] = v.strip()
-        if kv.get("kernel_source_sha256_16") != kernel_source_hash():
+        if kv.get("kernel_source_sha256_16") != kernel_source_hash(globals()[sources]):
             return None
         return float(kv["dram_bytes_per_launch_full_size"])
     except (OSError, KeyError, ValueError):
@@ -237,24 +254,41 @@ def measured_peaks():
 
 # ------------------------------------------------------------ our arm --
 
-class Workload:
-    """What one step runs: launch functions timed back to back with CUDA events,
-    the useful flops of a step, the dominant kernel's roofline terms, and the
-    host<->device copies of the end-to-end variant."""
+class Part:
+    """One launch (or call) of a step: a label, fn(stream), the number of this
+    library's kernels it launches, and its roofline terms: kernel name, bound
+    ("hbm" or "tensor"), algorithmic bytes or flops per launch, and the name of
+    the committed DRAM traffic record, if any."""
 
-    def __init__(self, name, config, parts, flops, roof, h2d, d2h, dtype="bf16",
-                 data="synthetic (seeded N(0,1) / uniform[-1,1], rounded to bf16)"):
+    def __init__(self, label, fn, kernels=1, kernel=None, bound=None, per_launch=None,
+                 traffic=None):
+        self.label = label
+        self.fn = fn
+        self.kernels = kernels
+        self.kernel = kernel
+        self.bound = bound
+        self.per_launch = per_launch
+        self.traffic = traffic
+
+
+class Workload:
+    """What one step runs: parts timed back to back with CUDA events, the useful flops
+    of a step, the host<->device copies of the end-to-end variant, optional separate
+    calls timed one by one (`calls`: [(label, M, flops, fn)]) and the oracle sample
+    that stands for a bounded part of the step on the CPU."""
+
+    def __init__(self, name, config, parts, flops, h2d, d2h, dtype="bf16",
+                 data="synthetic (seeded N(0,1) / uniform[-1,1], rounded to bf16)", calls=None):
         self.name = name          # human-readable workload string (config.workload)
         self.dtype = dtype        # arithmetic type of the path
         self.data = data
         self.config = config      # extra config keys
-        self.parts = parts        # [(label, fn(stream))]
+        self.parts = parts        # [Part]
         self.flops = flops        # useful flops per step
-        self.roof = roof          # dict: part, kernel, bound, per_launch (bytes or flops)
         self.h2d = h2d            # [(device tensor, host tensor)]
         self.d2h = d2h            # [(host tensor, device tensor)]
-        # kernels of this library launched per step (a part's fn.kernels, else 1)
-        self.kernels_per_step = sum(getattr(fn, "kernels", 1) for _, fn in parts)
+        self.calls = calls or []
+        self.kernels_per_step = sum(p.kernels for p in parts)
 
 
 def make_workload(name, dev):
@@ -263,120 +297,29 @@ def make_workload(name, dev):
     import causal_attention_score_gb300 as csa
     from causal_attention_score_gb300 import synth
 
-    def trimul_part(shape, lower_only=False, seed=0):
+    def trimul_part(shape, lower_only=False, seed=0, traffic=None):
         qkv_h = synth.trimul_input(shape, seed=seed, dist="normal")
         qkv = qkv_h.to(dev)
         out = torch.empty(shape.out_shape, dtype=torch.float32, device=dev)
         fn = lambda st: csa.trimul_forward(out, qkv, shape.B, shape.T, shape.C, shape.NH,
                                            lower_only=lower_only, stream=st)
-        return fn, [(qkv, qkv_h)], [out]
+        part = Part("trimul", fn, kernel="trimul_sm103a_kernel", bound="hbm",
+                    per_launch=trimul_algorithmic_bytes(shape.B, shape.T, shape.C, shape.NH,
+                                                        lower_only),
+                    traffic=traffic)
+        return part, [(qkv, qkv_h)], [out]
 
-    def dense_part(shape, seed=0):
+    def dense_part(shape, seed=0, label="dense_ragged"):
         X_h, W_h = synth.dense_input(shape, seed=seed)
         X, W = X_h.to(dev), W_h.to(dev)
         Y = torch.empty((shape.M, shape.H), dtype=torch.float32, device=dev)
         fn = lambda st: csa.dense_xwt(Y, X, W, shape.M, shape.I, shape.H, stream=st)
-        # Rows that no tensor map can describe are first copied to 16-byte-aligned
-        # rows by a second kernel (torch allocations are 16-byte aligned).
-        fn.kernels = 1 if (shape.I * 2) % 16 == 0 else 2
-        return fn, [(X, X_h), (W, W_h)], [Y]
+        part = Part(label, fn, kernels=csa.dense_xwt_kernels(shape.M, shape.I, shape.H, X, W),
+                    kernel="dense_sm103a_kernel", bound="tensor",
+                    per_launch=dense_flops(shape.M, shape.I, shape.H), traffic="dense_ragged")
+        return part, [(X, X_h), (W, W_h)], [Y]
 
-    def pinned_like(t):
-        return torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-
-    def finish(wl_name, config, parts, flops, roof, h2d, outs, **kw):
-        h2d = [(d, h.pin_memory()) for d, h in h2d]
-        d2h = [(pinned_like(o), o) for o in outs]
-        return Workload(wl_name, config, parts, flops, roof, h2d, d2h, **kw)
-
-    ts, ds = synth.TRIMUL_GPT2, synth.DENSE_RAGGED
-    if name == "step":
-        tf, th, to = trimul_part(ts)
-        df, dh, do = dense_part(ds)
-        return finish(
-            "trimul GPT-2-small (B=8,T=1024,C=768,NH=12,HS=64) + dense ragged "
-            "(M=960,I=770,H=768), one call each per step",
-            {"trimul": {"B": ts.B, "T": ts.T, "C": ts.C, "NH": ts.NH, "mask": "NaN"},
-             "dense": {"M": ds.M, "I": ds.I, "H": ds.H}},
-            [("trimul", tf), ("dense", df)],
-            trimul_flops(ts.B, ts.T, ts.C, ts.NH) + dense_flops(ds.M, ds.I, ds.H),
-            {"part": 0, "kernel": "trimul_sm103a_kernel", "bound": "hbm",
-             "per_launch": trimul_algorithmic_bytes(ts.B, ts.T, ts.C, ts.NH)},
-            th + dh, to + do)
-    if name in ("trimul_gpt2", "trimul_long", "trimul_gpt2_lower", "trimul_long_lower"):
-        shape = synth.TRIMUL_GPT2 if "gpt2" in name else synth.TRIMUL_LONG
-        lower = name.endswith("_lower")
-        tf, th, to = trimul_part(shape, lower_only=lower)
-        return finish(
-            f"trimul {'GPT-2-small' if 'gpt2' in name else 'long context'} (B={shape.B},"
-            f"T={shape.T},C={shape.C},NH={shape.NH},HS={shape.HS})"
-            + (", lower triangle only" if lower else ""),
-            {"trimul": {"B": shape.B, "T": shape.T, "C": shape.C, "NH": shape.NH,
-                        "mask": "untouched" if lower else "NaN"}},
-            [("trimul", tf)], trimul_flops(shape.B, shape.T, shape.C, shape.NH),
-            {"part": 0, "kernel": "trimul_sm103a_kernel", "bound": "hbm",
-             "per_launch": trimul_algorithmic_bytes(shape.B, shape.T, shape.C, shape.NH, lower)},
-            th, to)
-    if name in ("trimul_f32_gpt2", "trimul_f32_long"):
-        shape = synth.TRIMUL_GPT2 if "gpt2" in name else synth.TRIMUL_LONG
-        qkv_h = synth.trimul_input_f32(shape, seed=0, dist="uniform")
-        qkv = qkv_h.to(dev)
-        out = torch.empty(shape.out_shape, dtype=torch.float32, device=dev)
-        fn = lambda st: csa.trimul_forward_f32(out, qkv, shape.B, shape.T, shape.C, shape.NH,
-                                               stream=st)
-        return finish(
-            f"trimul over fp32 inputs (3 x tf32), {'GPT-2-small' if 'gpt2' in name else 'long context'}"
-            f" (B={shape.B},T={shape.T},C={shape.C},NH={shape.NH},HS={shape.HS})",
-            {"trimul_f32": {"B": shape.B, "T": shape.T, "C": shape.C, "NH": shape.NH,
-                            "mask": "NaN"}},
-            [("trimul_f32", fn)], trimul_flops(shape.B, shape.T, shape.C, shape.NH),
-            {"part": 0, "kernel": "trimul_sm103a_kernel<fp32>", "bound": "hbm",
-             "per_launch": trimul_algorithmic_bytes(shape.B, shape.T, shape.C, shape.NH,
-                                                    in_bytes=4)},
-            [(qkv, qkv_h)], [out], dtype="tf32x3",
-            data="synthetic (seeded uniform[-1,1] fp32, not rounded)")
-    if name in ("softmax_gpt2", "softmax_long"):
-        shape = synth.TRIMUL_GPT2 if name == "softmax_gpt2" else synth.TRIMUL_LONG
-        qkv_h = synth.trimul_input(shape, seed=0, dist="normal")
-        qkv = qkv_h.to(dev)
-        att = torch.empty(shape.out_shape, dtype=torch.float32, device=dev)
-        fn = lambda st: csa.causal_softmax_forward(att, qkv, shape.B, shape.T, shape.C, shape.NH,
-                                                   stream=st)
-        return finish(
-            f"causal softmax of the scores, {'GPT-2-small' if name == 'softmax_gpt2' else 'long context'}"
-            f" (B={shape.B},T={shape.T},C={shape.C},NH={shape.NH},HS={shape.HS})",
-            {"softmax": {"B": shape.B, "T": shape.T, "C": shape.C, "NH": shape.NH}},
-            [("softmax", fn)], trimul_flops(shape.B, shape.T, shape.C, shape.NH),
-            {"part": 0, "kernel": "softmax_sm103a_kernel", "bound": "hbm",
-             "per_launch": trimul_algorithmic_bytes(shape.B, shape.T, shape.C, shape.NH)},
-            [(qkv, qkv_h)], [att])
-    if name == "dense_ragged":
-        df, dh, do = dense_part(ds)
-        return finish("dense ragged (M=960,I=770,H=768)", {"dense": {"M": ds.M, "I": ds.I,
-                                                                     "H": ds.H}},
-                      [("dense", df)], dense_flops(ds.M, ds.I, ds.H),
-                      {"part": 0, "kernel": "dense_sm103a_kernel", "bound": "tensor",
-                       "per_launch": dense_flops(ds.M, ds.I, ds.H)}, dh, do)
-    if name == "dense_sweep":
-        xs_h, W_h = synth.dense_sweep_inputs(seed=0)
-        W = W_h.to(dev)
-        H, I = W_h.shape
-        parts, h2d, outs, flops = [], [(W, W_h)], [], 0
-        for i, X_h in enumerate(xs_h):
-            X = X_h.to(dev)
-            M = X_h.shape[0]
-            Y = torch.empty((M, H), dtype=torch.float32, device=dev)
-            parts.append((f"call{i}_M{M}", (lambda X, Y, M: lambda st: csa.dense_xwt(
-                Y, X, W, M, I, H, stream=st))(X, Y, M)))
-            h2d.append((X, X_h))
-            outs.append(Y)
-            flops += dense_flops(M, I, H)
-        return finish("dense dynamic-shape sweep: 32 calls, M = 16*T, T ~ U{1..128} (seed 0), "
-                      "I=768, H=3072", {"dense_sweep": {"calls": len(xs_h), "I": I, "H": H}},
-                      parts, flops, {"part": None, "kernel": "dense_sm103a_kernel",
-                                     "bound": "tensor", "per_launch": flops}, h2d, outs)
-    if name == "dense_sweep_grouped":
-        # The same 32 problems as dense_sweep, in one dense_xwt_grouped launch per step.
+    def sweep_parts():
         xs_h, W_h = synth.dense_sweep_inputs(seed=0)
         W = W_h.to(dev)
         H, I = W_h.shape
@@ -384,13 +327,112 @@ def make_workload(name, dev):
         Ys = [torch.empty((X.shape[0], H), dtype=torch.float32, device=dev) for X in Xs]
         flops = sum(dense_flops(X.shape[0], I, H) for X in Xs)
         plan = csa.DenseGroupedPlan(Ys, Xs, W, I, H)  # tensors checked once
-        fn = lambda st: plan(stream=st)
+        part = Part("dense_grouped", lambda st: plan(stream=st),
+                    kernel="dense_sm103a_kernel<grouped, CTA pairs>", bound="tensor",
+                    per_launch=flops, traffic="dense_sweep_grouped")
+        calls = [(f"call{i}_M{X.shape[0]}", int(X.shape[0]), dense_flops(X.shape[0], I, H),
+                  (lambda X, Y: lambda st: csa.dense_xwt(Y, X, W, X.shape[0], I, H,
+                                                         stream=st))(X, Y))
+                 for i, (X, Y) in enumerate(zip(Xs, Ys))]
+        return part, [(W, W_h)] + list(zip(Xs, xs_h)), Ys, flops, calls, (I, H, len(Xs))
+
+    def pinned_like(t):
+        return torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+
+    def finish(wl_name, config, parts, flops, h2d, outs, **kw):
+        h2d = [(d, h.pin_memory()) for d, h in h2d]
+        d2h = [(pinned_like(o), o) for o in outs]
+        return Workload(wl_name, config, parts, flops, h2d, d2h, **kw)
+
+    ts, tl, ds = synth.TRIMUL_GPT2, synth.TRIMUL_LONG, synth.DENSE_RAGGED
+    if name == "step":
+        tp, th, to = trimul_part(tl, traffic="trimul_long")
+        gp, gh, go, gflops, calls, (I, H, n) = sweep_parts()
+        dp, dh, do = dense_part(ds)
+        return finish(
+            "trimul long context (B=2,T=4096,C=2048,NH=16,HS=128) + dense dynamic-shape sweep "
+            "(32 problems M=16*T, T~U{1..128} seed 0, I=768, H=3072) in one grouped launch + "
+            "dense ragged (M=960,I=770,H=768), one call each per step",
+            {"trimul": {"B": tl.B, "T": tl.T, "C": tl.C, "NH": tl.NH, "mask": "NaN"},
+             "dense_sweep": {"calls": n, "I": I, "H": H, "grouped": True,
+                             "M": [c[1] for c in calls]},
+             "dense": {"M": ds.M, "I": ds.I, "H": ds.H}},
+            [tp, gp, dp],
+            trimul_flops(tl.B, tl.T, tl.C, tl.NH) + gflops + dense_flops(ds.M, ds.I, ds.H),
+            th + gh + dh, to + go + do, calls=calls)
+    if name == "step_gpt2":
+        tp, th, to = trimul_part(ts, traffic="trimul_gpt2")
+        dp, dh, do = dense_part(ds)
+        return finish(
+            "trimul GPT-2-small (B=8,T=1024,C=768,NH=12,HS=64) + dense ragged "
+            "(M=960,I=770,H=768), one call each per step",
+            {"trimul": {"B": ts.B, "T": ts.T, "C": ts.C, "NH": ts.NH, "mask": "NaN"},
+             "dense": {"M": ds.M, "I": ds.I, "H": ds.H}},
+            [tp, dp],
+            trimul_flops(ts.B, ts.T, ts.C, ts.NH) + dense_flops(ds.M, ds.I, ds.H),
+            th + dh, to + do)
+    if name in ("trimul_gpt2", "trimul_long", "trimul_gpt2_lower", "trimul_long_lower"):
+        shape = ts if "gpt2" in name else tl
+        lower = name.endswith("_lower")
+        tp, th, to = trimul_part(shape, lower_only=lower,
+                                 traffic=None if lower else name)
+        return finish(
+            f"trimul {'GPT-2-small' if 'gpt2' in name else 'long context'} (B={shape.B},"
+            f"T={shape.T},C={shape.C},NH={shape.NH},HS={shape.HS})"
+            + (", lower triangle only" if lower else ""),
+            {"trimul": {"B": shape.B, "T": shape.T, "C": shape.C, "NH": shape.NH,
+                        "mask": "untouched" if lower else "NaN"}},
+            [tp], trimul_flops(shape.B, shape.T, shape.C, shape.NH), th, to)
+    if name in ("trimul_f32_gpt2", "trimul_f32_long"):
+        shape = ts if "gpt2" in name else tl
+        qkv_h = synth.trimul_input_f32(shape, seed=0, dist="uniform")
+        qkv = qkv_h.to(dev)
+        out = torch.empty(shape.out_shape, dtype=torch.float32, device=dev)
+        fn = lambda st: csa.trimul_forward_f32(out, qkv, shape.B, shape.T, shape.C, shape.NH,
+                                               stream=st)
+        part = Part("trimul_f32", fn, kernel="trimul_sm103a_kernel<fp32>", bound="hbm",
+                    per_launch=trimul_algorithmic_bytes(shape.B, shape.T, shape.C, shape.NH,
+                                                        in_bytes=4))
+        return finish(
+            f"trimul over fp32 inputs (3 x tf32), {'GPT-2-small' if 'gpt2' in name else 'long context'}"
+            f" (B={shape.B},T={shape.T},C={shape.C},NH={shape.NH},HS={shape.HS})",
+            {"trimul_f32": {"B": shape.B, "T": shape.T, "C": shape.C, "NH": shape.NH,
+                            "mask": "NaN"}},
+            [part], trimul_flops(shape.B, shape.T, shape.C, shape.NH),
+            [(qkv, qkv_h)], [out], dtype="tf32x3",
+            data="synthetic (seeded uniform[-1,1] fp32, not rounded)")
+    if name in ("softmax_gpt2", "softmax_long"):
+        shape = ts if name == "softmax_gpt2" else tl
+        qkv_h = synth.trimul_input(shape, seed=0, dist="normal")
+        qkv = qkv_h.to(dev)
+        att = torch.empty(shape.out_shape, dtype=torch.float32, device=dev)
+        fn = lambda st: csa.causal_softmax_forward(att, qkv, shape.B, shape.T, shape.C, shape.NH,
+                                                   stream=st)
+        part = Part("softmax", fn, kernel="softmax_sm103a_kernel", bound="hbm",
+                    per_launch=trimul_algorithmic_bytes(shape.B, shape.T, shape.C, shape.NH))
+        return finish(
+            f"causal softmax of the scores, {'GPT-2-small' if name == 'softmax_gpt2' else 'long context'}"
+            f" (B={shape.B},T={shape.T},C={shape.C},NH={shape.NH},HS={shape.HS})",
+            {"softmax": {"B": shape.B, "T": shape.T, "C": shape.C, "NH": shape.NH}},
+            [part], trimul_flops(shape.B, shape.T, shape.C, shape.NH), [(qkv, qkv_h)], [att])
+    if name == "dense_ragged":
+        dp, dh, do = dense_part(ds)
+        return finish("dense ragged (M=960,I=770,H=768)",
+                      {"dense": {"M": ds.M, "I": ds.I, "H": ds.H}},
+                      [dp], dense_flops(ds.M, ds.I, ds.H), dh, do)
+    if name == "dense_sweep":
+        gp, gh, go, flops, calls, (I, H, n) = sweep_parts()
+        parts = [Part(label, fn, kernel="dense_sm103a_kernel", bound="tensor", per_launch=f)
+                 for label, _, f, fn in calls]
+        return finish("dense dynamic-shape sweep: 32 calls, M = 16*T, T ~ U{1..128} (seed 0), "
+                      "I=768, H=3072", {"dense_sweep": {"calls": n, "I": I, "H": H}},
+                      parts, flops, gh, go)
+    if name == "dense_sweep_grouped":
+        gp, gh, go, flops, calls, (I, H, n) = sweep_parts()
         return finish("dense dynamic-shape sweep, grouped: the same 32 problems (M = 16*T, "
                       "T ~ U{1..128}, seed 0, I=768, H=3072) in one dense_xwt_grouped launch",
-                      {"dense_sweep": {"calls": len(xs_h), "I": I, "H": H, "grouped": True}},
-                      [("grouped", fn)], flops,
-                      {"part": 0, "kernel": "dense_sm103a_kernel<true>", "bound": "tensor",
-                       "per_launch": flops}, [(W, W_h)] + list(zip(Xs, xs_h)), Ys)
+                      {"dense_sweep": {"calls": n, "I": I, "H": H, "grouped": True}},
+                      [gp], flops, gh, go, calls=calls)
     if name == "bmm_nt":
         bs = synth.BMM_NT_RAGGED
         X_h, W_h = synth.bmm_input(bs, seed=0)
@@ -399,18 +441,39 @@ def make_workload(name, dev):
         fn = lambda st: csa.batch_matmul_nt(Y, X, W, bs.batch, bs.T1, bs.T2, bs.D, stream=st)
         flops = 2 * bs.batch * bs.T1 * bs.T2 * bs.D
         nbytes = bs.batch * bs.T1 * bs.T2 * 4 + bs.batch * (bs.T1 + bs.T2) * bs.D * 2
+        part = Part("bmm_nt", fn, kernel="trimul_sm103a_kernel", bound="hbm", per_launch=nbytes)
         return finish("batched NT product (B*NH=192, T=120, D=64; DietCode BatchMatmulNT)",
                       {"bmm_nt": {"batch": bs.batch, "T1": bs.T1, "T2": bs.T2, "D": bs.D}},
-                      [("bmm_nt", fn)], flops,
-                      {"part": 0, "kernel": "trimul_sm103a_kernel", "bound": "hbm",
-                       "per_launch": nbytes}, [(X, X_h), (W, W_h)], [Y])
+                      [part], flops, [(X, X_h), (W, W_h)], [Y])
     raise ValueError(f"unknown workload {name}")
 
 
-WORKLOADS = ["step", "trimul_gpt2", "trimul_long", "trimul_gpt2_lower", "trimul_long_lower",
-             "dense_ragged", "dense_sweep", "dense_sweep_grouped", "bmm_nt", "softmax_gpt2",
-             "softmax_long",
-             "trimul_f32_gpt2", "trimul_f32_long"]
+WORKLOADS = ["step", "step_gpt2", "trimul_gpt2", "trimul_long", "trimul_gpt2_lower",
+             "trimul_long_lower", "dense_ragged", "dense_sweep", "dense_sweep_grouped", "bmm_nt",
+             "softmax_gpt2", "softmax_long", "trimul_f32_gpt2", "trimul_f32_long"]
+
+
+def roofline_entry(part, seconds, hbm_peak, bf16_peak, peak_src, timing):
+    """Achieved rate of one kernel launch against its bound's measured peak."""
+    if part.bound == "hbm":
+        achieved = part.per_launch / seconds / 1e9
+        return {"kernel": part.kernel, "part": part.label, "bound": "hbm",
+                "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 4),
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst copy)",
+                "algorithmic_bytes_per_launch": part.per_launch,
+                "launch_us": round(seconds * 1e6, 2),
+                "traffic": recorded_traffic(part.traffic) if part.traffic else None,
+                "timing": timing}
+    achieved = part.per_launch / seconds / 1e12
+    return {"kernel": part.kernel, "part": part.label, "bound": "tensor",
+            "achieved": round(achieved, 2), "peak": bf16_peak, "unit": "TFLOP/s",
+            "frac": round(achieved / bf16_peak, 4),
+            "peak_source": f"{peak_src} (MEASURED_PEAKS.json bf16_tflops, burst cuBLAS)",
+            "algorithmic_flops_per_launch": part.per_launch,
+            "launch_us": round(seconds * 1e6, 2),
+            "traffic": recorded_traffic(part.traffic) if part.traffic else None,
+            "timing": timing}
 
 
 def run_ours(args, rank, world, local):
@@ -426,8 +489,8 @@ def run_ours(args, rank, world, local):
     P = len(wl.parts)
 
     def step():
-        for _, fn in wl.parts:
-            fn(stream)
+        for part in wl.parts:
+            part.fn(stream)
 
     graph = None
     if args.graph:
@@ -438,8 +501,8 @@ def run_ours(args, rank, world, local):
         side.wait_stream(stream)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=side):
-            for _, fn in wl.parts:
-                fn(side)
+            for part in wl.parts:
+                part.fn(side)
         torch.cuda.synchronize(dev)
 
     def run_step():
@@ -448,24 +511,45 @@ def run_ours(args, rank, world, local):
         else:
             step()
 
-    for _ in range(args.warmup):
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(args.warmup):
         flush.zero_()
+        if i == args.warmup - 1:
+            w0.record(stream)
         run_step()
+    w1.record(stream)
     torch.cuda.synchronize(dev)
     if csa.get_status(stream) != 0:
         raise RuntimeError("device status not ok after warm-up")
+    est_ms = max(w0.elapsed_time(w1), 1e-3)
+
+    # Clock soak: the same steps back to back (with their L2 flushes) for about
+    # --soak-ms, so that the timed steps run at the clocks a sustained load settles at.
+    soak_sampler = ClockSampler(nvml_index(local), period_s=0.0005)
+    n_soak = 0
+    if args.soak_ms > 0:
+        n_soak = max(1, min(20000, int(math.ceil(args.soak_ms / (est_ms + 0.05)))))
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        soak_sampler.start()
+        s0 = time.perf_counter()
+        for _ in range(n_soak):
+            flush.zero_()
+            run_step()
+        torch.cuda.synchronize(dev)
+        soak_wall = time.perf_counter() - s0
+        soak_sampler.stop()
 
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-    sampler = ClockSampler(nvml_index(local))
+    sampler = ClockSampler(nvml_index(local), period_s=0.0005)
     barrier(world)
     torch.cuda.synchronize(dev)
     sampler.start()
     wall0 = time.perf_counter()
     # The timed region: whole steps, one event before and one after each. (An event
     # between two parts would sit between their kernels in the stream and keep the
-    # second from starting its launch under the first one's tail: measured 4.4 us
-    # on the default step.)
+    # second from starting its launch under the first one's tail.)
     for i in range(K):
         flush.zero_()  # evict L2 between steps; not inside the timed events
         ev[i][0].record(stream)
@@ -473,11 +557,12 @@ def run_ours(args, rank, world, local):
         ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
+    sampler.stop()
     if csa.get_status(stream) != 0:
         raise RuntimeError("device status not ok after the timed steps")
 
-    # Per-part times (and the roofline kernel's launch duration) for a step of several
-    # parts: a second pass of K steps, launched directly, with an event after each part.
+    # Per-part times (each kernel's launch duration) for a step of several parts: a
+    # second pass of K steps, launched directly, with an event after each part.
     part_ms = None
     if P > 1:
         pev = [[torch.cuda.Event(enable_timing=True) for _ in range(P + 1)] for _ in range(K)]
@@ -485,14 +570,33 @@ def run_ours(args, rank, world, local):
         for i in range(K):
             flush.zero_()
             pev[i][0].record(stream)
-            for p, (_, fn) in enumerate(wl.parts):
-                fn(stream)
+            for p, part in enumerate(wl.parts):
+                part.fn(stream)
                 pev[i][p + 1].record(stream)
         torch.cuda.synchronize(dev)
         if csa.get_status(stream) != 0:
             raise RuntimeError("device status not ok after the per-part steps")
         part_ms = [statistics.mean(e[p].elapsed_time(e[p + 1]) for e in pev) for p in range(P)]
-    sampler.stop()
+
+    # Separate calls (the sweep's problems one dense_xwt call each): a third pass, L2
+    # flushed before each call, an event on either side of it.
+    call_ms = None
+    if wl.calls:
+        reps = max(3, min(K, 20))
+        cev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in wl.calls] for _ in range(reps)]
+        torch.cuda.synchronize(dev)
+        for r in range(reps):
+            for c, (_, _, _, fn) in enumerate(wl.calls):
+                flush.zero_()
+                cev[r][c][0].record(stream)
+                fn(stream)
+                cev[r][c][1].record(stream)
+        torch.cuda.synchronize(dev)
+        if csa.get_status(stream) != 0:
+            raise RuntimeError("device status not ok after the separate calls")
+        call_ms = [statistics.median(cev[r][c][0].elapsed_time(cev[r][c][1]) for r in range(reps))
+                   for c in range(len(wl.calls))]
     barrier(world)
 
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
@@ -514,8 +618,8 @@ def run_ours(args, rank, world, local):
         with torch.cuda.stream(ls):
             for d, h in lw.h2d:
                 d.copy_(h, non_blocking=True)
-            for _, fn in lw.parts:
-                fn(ls)
+            for part in lw.parts:
+                part.fn(ls)
             for h, d in lw.d2h:
                 h.copy_(d, non_blocking=True)
 
@@ -547,34 +651,23 @@ def run_ours(args, rank, world, local):
     e2e_value = world * ke * wl.flops / (e2e_ms * 1e-3) / 1e12
 
     hbm_peak, bf16_peak, peak_src = measured_peaks()
-    roof = wl.roof
-    dom_s = (part_ms[roof["part"]] if (part_ms is not None and roof["part"] is not None)
-             else total_ms / K) * 1e-3
-    # Where the roofline kernel's launch duration comes from.
-    if part_ms is not None and roof["part"] is not None and P > 1:
-        dom_timing = ("CUDA events around its launch, in a second pass of the same K steps "
-                      "(direct launches) with an event after each part")
+    if P > 1:
+        timing = ("CUDA events around its launch, in a second pass of the same K steps "
+                  "(direct launches) with an event after each part")
     else:
-        dom_timing = "CUDA events around each step of the timed region"
-    if roof["bound"] == "hbm":
-        achieved = roof["per_launch"] / dom_s / 1e9
-        roofline = {"kernel": roof["kernel"], "bound": "hbm", "achieved": round(achieved, 1),
-                    "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                    "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst copy)",
-                    "algorithmic_bytes_per_launch": roof["per_launch"],
-                    "traffic": args.traffic if args.workload == "step" else None,
-                    "timing": dom_timing}
-    else:
-        achieved = roof["per_launch"] / dom_s / 1e12
-        roofline = {"kernel": roof["kernel"], "bound": "tensor", "achieved": round(achieved, 2),
-                    "peak": bf16_peak, "unit": "TFLOP/s", "frac": round(achieved / bf16_peak, 4),
-                    "peak_source": f"{peak_src} (MEASURED_PEAKS.json bf16_tflops, burst cuBLAS)",
-                    "algorithmic_flops_per_launch": roof["per_launch"], "traffic": None,
-                    "timing": dom_timing}
+        timing = "CUDA events around each step of the timed region"
+    rooflines = [roofline_entry(part, ms * 1e-3, hbm_peak, bf16_peak, peak_src, timing)
+                 for part, ms in zip(wl.parts, part_ms)]
+    dominant = max(range(P), key=lambda p: part_ms[p])
     config = {"workload": wl.name, **wl.config,
               "l2": "flushed between timed steps (256 MiB write, outside the timed events)",
               "launch": "one CUDA graph per step" if graph is not None else "direct launches",
               "parallelism": f"replicas x{world}"}
+    clocks = sampler.summary()
+    if n_soak:
+        soak = soak_sampler.summary()
+        soak.update({"steps": n_soak, "wall_s": round(soak_wall, 4)})
+        clocks["soak"] = soak
     result = {
         "metric": METRIC,
         "value": round(value, 3),
@@ -590,7 +683,8 @@ def run_ours(args, rank, world, local):
         "data": wl.data,
         "config": config,
         "pct_of_bf16_peak": round(100 * value / world / bf16_peak, 3),
-        "roofline": roofline,
+        "roofline": rooflines[dominant],
+        "rooflines": rooflines,
         "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": ke,
                 "ms_per_step": round(e2e_ms / ke, 4),
@@ -599,66 +693,106 @@ def run_ours(args, rank, world, local):
         "gpu_launches": wl.kernels_per_step * K,
         "flops_per_step": wl.flops,
         "ms_step_percentiles": {f"p{q}": round(_percentile(step_ms, q), 5) for q in (10, 50, 90)},
-        "clocks": sampler.summary(),
+        "clocks": clocks,
         "wall_s_timed_region": round(wall, 4),
     }
-    if part_ms is not None and P <= 40:
-        result["parts"] = {f"{label}_us": round(ms * 1e3, 2)
-                           for (label, _), ms in zip(wl.parts, part_ms)}
+    if P <= 40:
+        result["parts"] = {f"{part.label}_us": round(ms * 1e3, 2)
+                           for part, ms in zip(wl.parts, part_ms)}
         if P > 1:
             result["parts_timing"] = ("a second pass of the K steps, direct launches, with an "
                                       "event after each part")
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "step":
-        result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if call_ms is not None:
+        result["sweep_calls"] = {
+            "timing": "each problem as its own dense_xwt call, L2 flushed before each, median "
+                      "of CUDA events around the call",
+            "total_us": round(sum(call_ms) * 1e3, 2),
+            "calls": [{"M": M, "us": round(ms * 1e3, 2),
+                       "frac_bf16": round(f / (ms * 1e-3) / 1e12 / bf16_peak, 4)}
+                      for (_, M, f, _), ms in zip(wl.calls, call_ms)]}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload in ORACLE_SAMPLES:
+        result["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
     return result
 
 
 # --------------------------------------------------------- oracle timing --
 
-def _oracle_inputs():
-    import numpy as np  # noqa: F401
-    from causal_attention_score_gb300 import synth
-    ts, ds = synth.TRIMUL_GPT2, synth.DENSE_RAGGED
-    qkv = synth.bf16_bits(synth.trimul_input(ts, seed=0, dist="normal")).reshape(-1)
-    X, W = synth.dense_input(ds, seed=0)
-    return ts, ds, qkv, synth.bf16_bits(X).reshape(-1), synth.bf16_bits(W).reshape(-1)
+class OracleSample:
+    """Bounded samples of a step on the oracle. Sample i covers one (b, h) head of the
+    score product (all its rows) and the rows r = i (mod 32) of each dense problem, so
+    that 32 consecutive samples of the default step cover about one whole step."""
+
+    def __init__(self, workload):
+        import numpy as np
+
+        from causal_attention_score_gb300 import synth
+        self.np = np
+        ts = synth.TRIMUL_LONG if workload == "step" else synth.TRIMUL_GPT2
+        self.ts = ts
+        self.qkv = synth.bf16_bits(synth.trimul_input(ts, seed=0, dist="normal")).reshape(-1)
+        X, W = synth.dense_input(synth.DENSE_RAGGED, seed=0)
+        self.dense = [(synth.bf16_bits(X).reshape(-1), synth.bf16_bits(W).reshape(-1),
+                       synth.DENSE_RAGGED.M, synth.DENSE_RAGGED.I, synth.DENSE_RAGGED.H)]
+        self.sweep = workload == "step"
+        if self.sweep:
+            xs, Ws = synth.dense_sweep_inputs(seed=0)
+            wb = synth.bf16_bits(Ws).reshape(-1)
+            H, I = Ws.shape
+            self.dense += [(synth.bf16_bits(Xi).reshape(-1), wb, Xi.shape[0], I, H) for Xi in xs]
+        self.stride = 32
+
+    def describe(self):
+        if self.sweep:
+            return ("one (b,h) head of trimul long context (4096 rows) + rows r = i mod 32 of "
+                    "each of the 33 dense problems (the sweep's 32 and the ragged one): 1/32 of "
+                    "a step")
+        return "one (b,h) head of trimul GPT-2 (1024 rows) + 64 rows of dense ragged"
+
+    def __call__(self, o, i):
+        """Runs sample i on oracle `o`; returns its useful flops."""
+        np = self.np
+        ts = self.ts
+        bh = i % (ts.B * ts.NH)
+        b, h = divmod(bh, ts.NH)
+        bht = np.array([(b, h, t) for t in range(ts.T)], dtype=np.int64)
+        o.trimul_rows(self.qkv, ts.B, ts.T, ts.C, ts.NH, bht)
+        flops = 2 * ts.HS * ts.T * (ts.T + 1) // 2
+        for xb, wb, M, I, H in self.dense:
+            if self.sweep:
+                rows = np.arange(i % self.stride, M, self.stride, dtype=np.int64)
+            else:
+                rows = (np.arange(64, dtype=np.int64) + 64 * i) % M
+            if rows.size:
+                o.dense_rows(xb, wb, M, I, H, rows)
+                flops += 2 * int(rows.size) * I * H
+        return flops
 
 
-def oracle_sample_step(o, ts, ds, qkv, xb, wb, i):
-    """One bounded sample of the workload on the oracle: all T rows of one (b, h)
-    of the score product and 64 rows of the dense layer. Returns its useful flops."""
-    import numpy as np
-    bh = i % (ts.B * ts.NH)
-    b, h = divmod(bh, ts.NH)
-    bht = np.array([(b, h, t) for t in range(ts.T)], dtype=np.int64)
-    o.trimul_rows(qkv, ts.B, ts.T, ts.C, ts.NH, bht)
-    rows = (np.arange(64, dtype=np.int64) + 64 * i) % ds.M
-    o.dense_rows(xb, wb, ds.M, ds.I, ds.H, rows)
-    return (2 * ts.HS * ts.T * (ts.T + 1) // 2) + 2 * 64 * ds.I * ds.H
+ORACLE_SAMPLES = ("step", "step_gpt2")
 
 
-def cpu_baseline(seconds: float):
-    """The oracle as it stands on the host cores: repeated bounded samples for about
-    `seconds` of CPU time; throughput in the metric's unit."""
+def cpu_baseline(workload: str, seconds: float):
+    """The oracle as it stands on the host cores: repeated bounded samples of the step for
+    about `seconds` of CPU time; throughput in the metric's unit."""
     import oracle
     o = oracle.get()
-    ts, ds, qkv, xb, wb = _oracle_inputs()
+    sample = OracleSample(workload)
     flops, i = 0, 0
     t0 = time.perf_counter()
     while True:
-        flops += oracle_sample_step(o, ts, ds, qkv, xb, wb, i)
+        flops += sample(o, i)
         i += 1
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
     cores = o.num_threads()
-    # The same samples on one thread, for about a quarter of the time.
+    # The same samples on one thread, for about a quarter of the time (at least one).
     o.set_num_threads(1)
     try:
         flops1, j = 0, 0
         t1 = time.perf_counter()
         while True:
-            flops1 += oracle_sample_step(o, ts, ds, qkv, xb, wb, j)
+            flops1 += sample(o, j)
             j += 1
             if time.perf_counter() - t1 >= seconds / 4:
                 break
@@ -667,8 +801,7 @@ def cpu_baseline(seconds: float):
         o.set_num_threads(cores)
     return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": cores,
             "kind": "oracle",
-            "sample": f"{i} samples of one (b,h) head of trimul GPT-2 (1024 rows) + 64 rows of "
-                      f"dense ragged, fp64, {dt:.1f} s",
+            "sample": f"{i} samples, each {sample.describe()}; fp64, {dt:.1f} s",
             "value_1thread": round(flops1 / dt1 / 1e12, 6),
             "sample_1thread": f"{j} of the same samples on 1 thread, {dt1:.1f} s"}
 
@@ -678,15 +811,21 @@ def run_reference(args, rank, world):
         return None
     import oracle
     o = oracle.get()
-    ts, ds, qkv, xb, wb = _oracle_inputs()
+    workload = args.workload if args.workload in ORACLE_SAMPLES else "step"
+    sample = OracleSample(workload)
     for i in range(args.warmup):
-        oracle_sample_step(o, ts, ds, qkv, xb, wb, i)
+        sample(o, i)
     flops = 0
     t0 = time.perf_counter()
     for i in range(args.steps):
-        flops += oracle_sample_step(o, ts, ds, qkv, xb, wb, i)
+        flops += sample(o, i)
     dt = time.perf_counter() - t0
     value = flops / dt / 1e12
+    names = {"step": "trimul long context (B=2,T=4096,C=2048,NH=16,HS=128) + dense dynamic-shape "
+                     "sweep (32 problems M=16*T, T~U{1..128} seed 0, I=768, H=3072) + dense "
+                     "ragged (M=960,I=770,H=768)",
+             "step_gpt2": "trimul GPT-2-small (B=8,T=1024,C=768,NH=12,HS=64) + dense ragged "
+                          "(M=960,I=770,H=768)"}
     return {
         "impl": "reference",
         "metric": METRIC,
@@ -701,13 +840,10 @@ def run_reference(args, rank, world):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded, rounded to bf16)",
-        "config": {
-            "workload": "trimul GPT-2-small (B=8,T=1024,C=768,NH=12,HS=64) + dense ragged "
-                        "(M=960,I=770,H=768); each step a bounded sample: one (b,h) head "
-                        "(1024 rows) + 64 dense rows",
-        },
+        "config": {"workload": names[workload] + "; each step a bounded sample: "
+                   + sample.describe()},
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": o.num_threads(),
-                         "kind": "oracle", "sample": "per step: one (b,h) head + 64 dense rows"},
+                         "kind": "oracle", "sample": "per step: " + sample.describe()},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -720,14 +856,14 @@ def main(argv=None):
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--soak-ms", type=float, default=150.0,
+                   help="run the step back to back this long before the timed region")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--workload", choices=WORKLOADS, default="step",
                    help="what a step runs (default: the headline step)")
     p.add_argument("--graph", action="store_true",
                    help="capture each step's launches as one CUDA graph and replay it")
-    p.add_argument("--traffic", type=float, default=None,
-                   help="dram bytes read+written per trimul launch from an ncu capture")
     args = p.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         p.error("--warmup must be >= 3")
@@ -741,8 +877,6 @@ def main(argv=None):
             print(json.dumps(res), flush=True)
         return
     rank, world, local = dist_setup(args.gpus)
-    if args.traffic is None:
-        args.traffic = recorded_traffic()
     res = run_ours(args, rank, world, local)
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)

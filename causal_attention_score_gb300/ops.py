@@ -74,6 +74,14 @@ def dense_xwt(Y: torch.Tensor, X: torch.Tensor, W: torch.Tensor, M: int, I: int,
     _lib.check(rc, "dense_xwt")
 
 
+def dense_xwt_kernels(M: int, I: int, H: int, X: torch.Tensor, W: torch.Tensor) -> int:
+    """How many of this library's kernels one dense_xwt call on these tensors launches:
+    one when tensor maps can describe the rows of X and W (I * 2 a multiple of 16,
+    both 16-byte aligned), else two (a realigning copy, then the product)."""
+    tma = (I * 2) % 16 == 0 and X.data_ptr() % 16 == 0 and W.data_ptr() % 16 == 0
+    return 1 if tma else 2
+
+
 class DenseGroupedPlan:
     """dense_xwt_grouped with its arguments checked and marshalled once.
 
