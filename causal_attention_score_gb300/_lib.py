@@ -21,6 +21,7 @@ CSA_ERR_LAUNCH = -6
 CSA_ERR_TIMEOUT = -7
 CSA_ERR_CUDA = -8
 CSA_ERR_CHECK = -9
+CSA_ERR_WORKSPACE = -10
 
 CSA_MASK_NAN = 0x7FC00000
 CSA_MASK_NEG_INF = 0xFF800000
@@ -40,6 +41,8 @@ SIGNATURES = {
     "batch_matmul_nt": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "causal_softmax_forward": (_i, [_vp, _vp, _i, _i, _i, _i, _vp]),
     "dense_xwt_ex": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp]),
+    "dense_xwt_workspace_size": (_i, [_vp, _vp, _i, _i, _i, ctypes.POINTER(ctypes.c_size_t)]),
+    "dense_xwt_ws": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, ctypes.c_size_t, _vp]),
     "dense_xwt_grouped": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp]),
     "csa_get_status": (_i, [_vp]),
     "csa_status_string": (ctypes.c_char_p, [_i]),

@@ -241,6 +241,18 @@ int dense_fetch_mode() { return g_dense_fetch.load(); }
 
 using namespace csa;
 
+// Checks shared by the dense entry points; CSA_OK or the status to return.
+static int dense_args_ok(const char* who, const void* Y, const void* X, const void* W, int M,
+                         int I, int H) {
+  if (!Y || !X || !W) return set_error(CSA_ERR_NULL, std::string(who) + ": null pointer");
+  if (M <= 0 || I <= 0 || H <= 0)
+    return set_error(CSA_ERR_SHAPE, std::string(who) + ": M, I, H must be >= 1");
+  if (reinterpret_cast<uintptr_t>(X) % 2 || reinterpret_cast<uintptr_t>(W) % 2 ||
+      reinterpret_cast<uintptr_t>(Y) % 4)
+    return set_error(CSA_ERR_ALIGN, std::string(who) + ": X, W need 2-byte and Y 4-byte alignment");
+  return CSA_OK;
+}
+
 extern "C" {
 
 csa_status trimul_forward_ex(float* out, const void* qkv, int B, int T, int C, int NH,
@@ -370,17 +382,48 @@ csa_status batch_matmul_nt(float* Y, const void* X, const void* W, int batch, in
 csa_status dense_xwt_ex(float* Y, const void* X, const void* W, int M, int I, int H,
                         void* stream) {
   t_last_error.clear();
-  if (!Y || !X || !W) return set_error(CSA_ERR_NULL, "dense_xwt: null pointer");
-  if (M <= 0 || I <= 0 || H <= 0)
-    return set_error(CSA_ERR_SHAPE, "dense_xwt: M, I, H must be >= 1");
-  if (reinterpret_cast<uintptr_t>(X) % 2 || reinterpret_cast<uintptr_t>(W) % 2 ||
-      reinterpret_cast<uintptr_t>(Y) % 4)
-    return set_error(CSA_ERR_ALIGN, "dense_xwt: X, W need 2-byte and Y 4-byte alignment");
+  int rc = dense_args_ok("dense_xwt", Y, X, W, M, I, H);
+  if (rc != CSA_OK) return rc;
   DeviceInfo dev;
   std::string err;
-  int rc = current_device(dev, err);
+  rc = current_device(dev, err);
   if (rc != CSA_OK) return set_error(rc, err);
-  rc = dense_launch(Y, X, W, M, I, H, static_cast<cudaStream_t>(stream), dev, err);
+  rc = dense_launch(Y, X, W, M, I, H, nullptr, 0, static_cast<cudaStream_t>(stream), dev, err);
+  if (rc != CSA_OK) return set_error(rc, err);
+  return CSA_OK;
+}
+
+csa_status dense_xwt_workspace_size(const void* X, const void* W, int M, int I, int H,
+                                    size_t* bytes) {
+  t_last_error.clear();
+  if (!bytes) return set_error(CSA_ERR_NULL, "dense_xwt_workspace_size: null pointer");
+  *bytes = 0;
+  if (!X || !W) return set_error(CSA_ERR_NULL, "dense_xwt_workspace_size: null pointer");
+  if (M <= 0 || I <= 0 || H <= 0)
+    return set_error(CSA_ERR_SHAPE, "dense_xwt_workspace_size: M, I, H must be >= 1");
+  *bytes = dense_workspace_bytes(X, W, M, I, H);
+  return CSA_OK;
+}
+
+csa_status dense_xwt_ws(float* Y, const void* X, const void* W, int M, int I, int H,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  t_last_error.clear();
+  int rc = dense_args_ok("dense_xwt_ws", Y, X, W, M, I, H);
+  if (rc != CSA_OK) return rc;
+  const size_t need = dense_workspace_bytes(X, W, M, I, H);
+  if (need > 0 && (!workspace || workspace_bytes < need))
+    return set_error(CSA_ERR_WORKSPACE, "dense_xwt_ws: " + std::to_string(need) +
+                                            " bytes of workspace needed, " +
+                                            std::to_string(workspace ? workspace_bytes : 0) +
+                                            " given");
+  if (workspace && reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
+    return set_error(CSA_ERR_ALIGN, "dense_xwt_ws: workspace must be 16-byte aligned");
+  DeviceInfo dev;
+  std::string err;
+  rc = current_device(dev, err);
+  if (rc != CSA_OK) return set_error(rc, err);
+  rc = dense_launch(Y, X, W, M, I, H, need > 0 ? workspace : nullptr, workspace_bytes,
+                    static_cast<cudaStream_t>(stream), dev, err);
   if (rc != CSA_OK) return set_error(rc, err);
   return CSA_OK;
 }
@@ -450,6 +493,7 @@ const char* csa_status_string(csa_status s) {
     case CSA_ERR_TIMEOUT: return "device-side wait ran out";
     case CSA_ERR_CUDA: return "CUDA call failed";
     case CSA_ERR_CHECK: return "device-side index check failed (debug build)";
+    case CSA_ERR_WORKSPACE: return "workspace missing or too small";
     default: return "unknown status";
   }
 }

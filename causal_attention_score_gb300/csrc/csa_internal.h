@@ -102,8 +102,14 @@ int bmm_nt_launch(float* Y, const void* X, const void* W, int batch, int T1, int
 int softmax_launch(float* out, const void* qkv, int B, int T, int C, int NH, cudaStream_t stream,
                    const DeviceInfo& dev, std::string& err);
 
-int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
-                 cudaStream_t stream, const DeviceInfo& dev, std::string& err);
+// One dense layer. Rows no tensor map can describe are first copied into
+// `workspace` (ws_bytes long, at least dense_workspace_bytes) as 16-byte-aligned
+// rows, or fetched by loader warps when workspace is nullptr.
+int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H, void* workspace,
+                 size_t ws_bytes, cudaStream_t stream, const DeviceInfo& dev, std::string& err);
+
+// Workspace bytes dense_launch needs to realign X and W (0 when their rows need none).
+size_t dense_workspace_bytes(const void* X, const void* W, int M, int I, int H);
 
 int dense_grouped_launch(float* const* Y, const void* const* X, const void* W, const int* M, int n,
                          int I, int H, cudaStream_t stream, const DeviceInfo& dev,

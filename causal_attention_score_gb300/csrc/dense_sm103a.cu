@@ -18,12 +18,12 @@
 //      * TMA (I*2 % 16 == 0, 16-byte aligned X and W): warp 0 issues 2-D tiled
 //        loads; rows >= M / H and columns >= I are zero-filled by the TMA unit.
 //        Rows that no tensor map can describe (e.g. I = 770: 1540-byte rows)
-//        are first copied by realign_rows_kernel into a scratch copy whose
-//        rows start on 16-byte boundaries (pitch I rounded up to 8 elements);
-//        the tiles are then fetched from that copy by TMA, with the same zero
-//        fill at the edges. The copy only moves rows: no padding to tile
-//        multiples is materialised.
-//      * loader warps (rows no tensor map can describe, with no scratch copy):
+//        are first copied by realign_rows_kernel into the caller's workspace
+//        as rows that start on 16-byte boundaries (pitch I rounded up to 8
+//        elements); the tiles are then fetched from that copy by TMA, with the
+//        same zero fill at the edges. The copy only moves rows: no padding to
+//        tile multiples is materialised.
+//      * loader warps (rows no tensor map can describe, with no workspace):
 //        warps 0-3 read 4-byte (or 2-byte) pairs with plain loads, substitute
 //        zeros out of range, and write them into the same 128-byte-swizzled
 //        K-major layout the TMA would produce.
@@ -630,42 +630,6 @@ __global__ void __launch_bounds__(kRealignThreads)
   }
 }
 
-// Library-owned memory pool of the scratch copies, one per device, created on
-// first use and kept for the life of the process. Allocations and frees are
-// stream-ordered on the caller's stream; up to 256 MiB of freed scratch stays
-// reserved in the pool between calls.
-int scratch_pool(int device, cudaMemPool_t* out, std::string& err) {
-  static std::mutex mu;
-  static cudaMemPool_t pools[64] = {};
-  std::lock_guard<std::mutex> lock(mu);
-  if (device < 0 || device >= 64) {
-    err = "dense_xwt: device ordinal out of range";
-    return CSA_ERR_CUDA;
-  }
-  if (!pools[device]) {
-    cudaMemPoolProps props{};
-    props.allocType = cudaMemAllocationTypePinned;
-    props.location.type = cudaMemLocationTypeDevice;
-    props.location.id = device;
-    cudaMemPool_t pool = nullptr;
-    cudaError_t e = cudaMemPoolCreate(&pool, &props);
-    if (e != cudaSuccess) {
-      err = std::string("dense_xwt: cudaMemPoolCreate: ") + cudaGetErrorString(e);
-      return CSA_ERR_CUDA;
-    }
-    uint64_t keep = 256ull << 20;
-    e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
-    if (e != cudaSuccess) {
-      cudaMemPoolDestroy(pool);
-      err = std::string("dense_xwt: cudaMemPoolSetAttribute: ") + cudaGetErrorString(e);
-      return CSA_ERR_CUDA;
-    }
-    pools[device] = pool;
-  }
-  *out = pools[device];
-  return CSA_OK;
-}
-
 // Tile width along H: the largest BN whose wave count times tile cost is
 // smallest (tile cost ~ BN plus a fixed per-tile overhead), for m_tiles rows of
 // 128-row tiles.
@@ -706,10 +670,25 @@ int plan_smem(DenseArgs& a, const DeviceInfo& dev, std::string& err, size_t& sme
   return CSA_OK;
 }
 
+// Rows that tensor maps can describe as they are: I * 2 a multiple of 16 and
+// both operands 16-byte aligned.
+bool rows_describable(const void* X, const void* W, int I) {
+  return (static_cast<long long>(I) * 2) % 16 == 0 && reinterpret_cast<uintptr_t>(X) % 16 == 0 &&
+         reinterpret_cast<uintptr_t>(W) % 16 == 0;
+}
+
+size_t round256(size_t n) { return (n + 255) / 256 * 256; }
+
 }  // namespace
 
-int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
-                 cudaStream_t stream, const DeviceInfo& dev, std::string& err) {
+size_t dense_workspace_bytes(const void* X, const void* W, int M, int I, int H) {
+  if (rows_describable(X, W, I)) return 0;
+  const size_t P = (static_cast<size_t>(I) + 7) / 8 * 8;
+  return 256 + round256(static_cast<size_t>(M) * P * 2) + static_cast<size_t>(H) * P * 2;
+}
+
+int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H, void* workspace,
+                 size_t ws_bytes, cudaStream_t stream, const DeviceInfo& dev, std::string& err) {
   const uintptr_t px = reinterpret_cast<uintptr_t>(X), pw = reinterpret_cast<uintptr_t>(W),
                   py = reinterpret_cast<uintptr_t>(Y);
   if (px % 2 || pw % 2 || py % 4) {
@@ -725,38 +704,33 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
   a.n_tiles = (H + a.BN - 1) / a.BN;
   a.kblocks = (I + kBK - 1) / kBK;
   a.num_tiles = static_cast<long long>(a.m_tiles) * a.n_tiles;
-  a.tma_load = ((static_cast<long long>(I) * 2) % 16 == 0 && px % 16 == 0 && pw % 16 == 0) ? 1u : 0u;
+  a.tma_load = rows_describable(X, W, I) ? 1u : 0u;
   a.tma_store = ((static_cast<long long>(H) * 4) % 16 == 0 && py % 16 == 0) ? 1u : 0u;
   a.vec2 = (I % 2 == 0 && px % 4 == 0 && pw % 4 == 0) ? 1u : 0u;
 
-  // Rows no tensor map can describe: copy them to 16-byte-aligned rows first
-  // (unless the caller asked for the loader-warp fetch, or no scratch is had).
+  // Rows no tensor map can describe: copied first into the caller's workspace as
+  // 16-byte-aligned rows (unless there is none, or the caller asked for the
+  // loader-warp fetch), then fetched by TMA.
   const void* X_tma = X;
   const void* W_tma = W;
   long long pitch = I;
-  void* scratch = nullptr;
-  if (!a.tma_load && dense_fetch_mode() == CSA_DENSE_FETCH_AUTO) {
-    const long long P = (static_cast<long long>(I) + 7) / 8 * 8;
-    const size_t bytes_x = (static_cast<size_t>(M) * P * 2 + 255) / 256 * 256;
-    const size_t bytes = bytes_x + static_cast<size_t>(H) * P * 2;
-    cudaMemPool_t pool = nullptr;
-    int rc = scratch_pool(dev.device, &pool, err);
-    if (rc != CSA_OK) return rc;
-    if (cudaMallocFromPoolAsync(&scratch, bytes, pool, stream) != cudaSuccess) {
-      (void)cudaGetLastError();  // out of memory: fetch with loader warps instead
-      scratch = nullptr;
-    } else {
-      X_tma = scratch;
-      W_tma = static_cast<uint8_t*>(scratch) + bytes_x;
-      pitch = P;
-      a.tma_load = 1u;
+  bool realign = false;
+  if (!a.tma_load && workspace && dense_fetch_mode() == CSA_DENSE_FETCH_AUTO) {
+    const size_t need = dense_workspace_bytes(X, W, M, I, H);
+    if (ws_bytes < need) {
+      err = "dense_xwt_ws: " + std::to_string(need) + " bytes of workspace needed, " +
+            std::to_string(ws_bytes) + " given";
+      return CSA_ERR_WORKSPACE;
     }
+    const long long P = (static_cast<long long>(I) + 7) / 8 * 8;
+    uint8_t* p = static_cast<uint8_t*>(workspace);
+    p += (256 - reinterpret_cast<uintptr_t>(p) % 256) % 256;
+    X_tma = p;
+    W_tma = p + round256(static_cast<size_t>(M) * P * 2);
+    pitch = P;
+    a.tma_load = 1u;
+    realign = true;
   }
-  // Releases the scratch copy in stream order after the product's launch.
-  auto release = [&](int rc) {
-    if (scratch) cudaFreeAsync(scratch, stream);
-    return rc;
-  };
   a.idesc = idesc_bf16_f32(kBM, a.BN);
   a.X = static_cast<const uint16_t*>(X);
   a.W = static_cast<const uint16_t*>(W);
@@ -769,7 +743,7 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
   size_t smem = 0;
   {
     const int rc = plan_smem(a, dev, err, smem, a.BN);
-    if (rc != CSA_OK) return release(rc);
+    if (rc != CSA_OK) return rc;
   }
 
   CUtensorMap map_x, map_w, map_y;
@@ -784,10 +758,10 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
     const uint32_t bw[2] = {kBK, static_cast<uint32_t>(a.BN)};
     int rc = encode_tiled(&map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X_tma, dx, st, bx,
                           CU_TENSOR_MAP_SWIZZLE_128B, err);
-    if (rc != CSA_OK) return release(rc);
+    if (rc != CSA_OK) return rc;
     rc = encode_tiled(&map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W_tma, dw, st, bw,
                       CU_TENSOR_MAP_SWIZZLE_128B, err);
-    if (rc != CSA_OK) return release(rc);
+    if (rc != CSA_OK) return rc;
   }
   if (a.tma_store) {
     const uint64_t dy[2] = {static_cast<uint64_t>(H), static_cast<uint64_t>(M)};
@@ -795,7 +769,7 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
     const uint32_t by[2] = {32, 32};
     int rc = encode_tiled(&map_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, Y, dy, st, by,
                           CU_TENSOR_MAP_SWIZZLE_128B, err);
-    if (rc != CSA_OK) return release(rc);
+    if (rc != CSA_OK) return rc;
   }
 
   {
@@ -803,11 +777,11 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
                                   static_cast<int>(smem), dev.device, err);
     if (rc != CSA_OK) {
       err = "dense_xwt: " + err;
-      return release(rc);
+      return rc;
     }
   }
   cudaError_t e;
-  if (scratch) {
+  if (realign) {
     // The realigned copy, launched last of all so that a call that fails a
     // check launches nothing.
     const long long rows = static_cast<long long>(M) + H;
@@ -820,7 +794,7 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
       err = std::string("dense_xwt: launch: ") + cudaGetErrorString(e);
-      return release(CSA_ERR_LAUNCH);
+      return CSA_ERR_LAUNCH;
     }
   }
   const long long grid = std::min<long long>(a.num_tiles, dev.sm_count);
@@ -829,9 +803,9 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H,
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     err = std::string("dense_xwt: launch: ") + cudaGetErrorString(e);
-    return release(CSA_ERR_LAUNCH);
+    return CSA_ERR_LAUNCH;
   }
-  return release(CSA_OK);
+  return CSA_OK;
 }
 
 }  // namespace csa
@@ -853,7 +827,7 @@ int dense_grouped_launch(float* const* Y, const void* const* X, const void* W, c
   }
   if (!tma_rows) {
     for (int i = 0; i < n; ++i) {
-      const int rc = dense_launch(Y[i], X[i], W, M[i], I, H, stream, dev, err);
+      const int rc = dense_launch(Y[i], X[i], W, M[i], I, H, nullptr, 0, stream, dev, err);
       if (rc != CSA_OK) return rc;
     }
     return CSA_OK;

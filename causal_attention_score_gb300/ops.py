@@ -63,23 +63,66 @@ def trimul_forward_f32(out: torch.Tensor, qkv: torch.Tensor, B: int, T: int, C: 
     _lib.check(rc, "trimul_forward_f32")
 
 
+def dense_workspace_size(X: torch.Tensor, W: torch.Tensor, M: int, I: int, H: int) -> int:
+    """Bytes of workspace ``dense_xwt_ws`` needs for these operands (0 when the rows of
+    X and W can be fetched by TMA as they are); see dense_xwt_workspace_size in
+    include/csa.h."""
+    import ctypes
+    n = ctypes.c_size_t(0)
+    rc = _lib.load().dense_xwt_workspace_size(X.data_ptr(), W.data_ptr(), M, I, H,
+                                               ctypes.byref(n))
+    _lib.check(rc, "dense_xwt_workspace_size")
+    return int(n.value)
+
+
 def dense_xwt(Y: torch.Tensor, X: torch.Tensor, W: torch.Tensor, M: int, I: int, H: int,
               stream=None) -> None:
-    """Y = X W^T into ``Y`` (fp32 [M, H]) from bf16 X [M, I] and W [H, I]."""
+    """Y = X W^T into ``Y`` (fp32 [M, H]) from bf16 X [M, I] and W [H, I].
+
+    Where no tensor map can describe the rows of X and W (I * 2 not a multiple of 16,
+    or misaligned views), the kernel realigns them into a workspace that this binding
+    takes from torch's caching allocator on the call's stream (caller memory: the
+    library itself allocates nothing) and passes to dense_xwt_ws."""
     _need(X, "X", torch.bfloat16, M * I)
     _need(W, "W", torch.bfloat16, H * I)
     _need(Y, "Y", torch.float32, M * H)
-    rc = _lib.load().dense_xwt_ex(Y.data_ptr(), X.data_ptr(), W.data_ptr(), M, I, H,
-                                  _stream_ptr(stream))
-    _lib.check(rc, "dense_xwt")
+    lib = _lib.load()
+    nbytes = dense_workspace_size(X, W, M, I, H)
+    if nbytes == 0:
+        rc = lib.dense_xwt_ex(Y.data_ptr(), X.data_ptr(), W.data_ptr(), M, I, H,
+                              _stream_ptr(stream))
+        _lib.check(rc, "dense_xwt")
+        return
+    # The workspace is in use until the kernel completes on `stream`: allocated with
+    # that stream current, so the caching allocator reuses it only in stream order.
+    if stream is None:
+        st = torch.cuda.current_stream(X.device)
+    elif isinstance(stream, torch.cuda.Stream):
+        st = stream
+    else:
+        st = torch.cuda.ExternalStream(int(stream), device=X.device)
+    with torch.cuda.stream(st):
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=X.device)
+    rc = lib.dense_xwt_ws(Y.data_ptr(), X.data_ptr(), W.data_ptr(), M, I, H, ws.data_ptr(),
+                          nbytes, int(st.cuda_stream))
+    _lib.check(rc, "dense_xwt_ws")
 
 
-def dense_xwt_kernels(M: int, I: int, H: int, X: torch.Tensor, W: torch.Tensor) -> int:
-    """How many of this library's kernels one dense_xwt call on these tensors launches:
-    one when tensor maps can describe the rows of X and W (I * 2 a multiple of 16,
-    both 16-byte aligned), else two (a realigning copy, then the product)."""
-    tma = (I * 2) % 16 == 0 and X.data_ptr() % 16 == 0 and W.data_ptr() % 16 == 0
-    return 1 if tma else 2
+def dense_xwt_ws(Y: torch.Tensor, X: torch.Tensor, W: torch.Tensor, M: int, I: int, H: int,
+                 workspace: torch.Tensor | None, stream=None) -> None:
+    """dense_xwt with a caller-provided workspace (a CUDA tensor of at least
+    ``dense_workspace_size`` bytes, or None when that size is 0)."""
+    _need(X, "X", torch.bfloat16, M * I)
+    _need(W, "W", torch.bfloat16, H * I)
+    _need(Y, "Y", torch.float32, M * H)
+    ptr, nbytes = 0, 0
+    if workspace is not None:
+        if not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        ptr, nbytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    rc = _lib.load().dense_xwt_ws(Y.data_ptr(), X.data_ptr(), W.data_ptr(), M, I, H, ptr or None,
+                                  nbytes, _stream_ptr(stream))
+    _lib.check(rc, "dense_xwt_ws")
 
 
 class DenseGroupedPlan:
@@ -207,9 +250,9 @@ DENSE_FETCH_LOADERS = 1
 
 
 def set_dense_fetch(mode: int) -> None:
-    """Process-wide fetch mode of ``dense_xwt`` for rows no tensor map can describe:
-    ``DENSE_FETCH_AUTO`` (realigned scratch copy + TMA) or ``DENSE_FETCH_LOADERS``
-    (loader warps, no scratch)."""
+    """Process-wide fetch mode of ``dense_xwt`` / ``dense_xwt_ws`` for rows no tensor map
+    can describe: ``DENSE_FETCH_AUTO`` (rows realigned into the workspace, then TMA) or
+    ``DENSE_FETCH_LOADERS`` (loader warps; the workspace unused). Same bits either way."""
     _lib.check(_lib.load().csa_set_dense_fetch(int(mode)), "csa_set_dense_fetch")
 
 

@@ -3,8 +3,9 @@
  * libcsa_gb300.so.
  *
  * Two products, each a persistent tcgen05/TMA kernel (plus, for dense rows no
- * tensor map can describe, one realigning copy launched before it), and the
- * calls built on them: the batched NT product (batch_matmul_nt), the fused
+ * tensor map can describe, one realigning copy into caller workspace launched
+ * before it), and the calls built on them: the batched NT product
+ * (batch_matmul_nt), the fused
  * causal softmax of the scores (causal_softmax_forward), the score product
  * over fp32 inputs (trimul_forward_f32), many dense layers sharing W in one
  * launch (dense_xwt_grouped), and an allocation-free score entry point
@@ -28,8 +29,11 @@
  *
  * Conventions shared by every entry point:
  *  - Pointers named as device pointers must point to memory of the current CUDA
- *    device (cudaMalloc'd or torch-allocated). The caller owns every buffer;
- *    the library never allocates, frees or retains caller memory.
+ *    device (cudaMalloc'd or torch-allocated). The caller owns every buffer,
+ *    scratch space included (dense_xwt_ws); no call allocates device memory.
+ *    The library keeps, per device, only fixed arrays in its own image: the
+ *    status word, the kernels' work-list counters and the scratch of
+ *    trimul_forward_noalloc.
  *  - bf16 inputs are passed as `const void*` to raw 16-bit bfloat16 values.
  *  - Outputs are fp32 and fully overwritten (no read-modify-write).
  *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
@@ -46,6 +50,7 @@
 #ifndef CSA_GB300_H
 #define CSA_GB300_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -65,6 +70,8 @@ typedef int csa_status;
 #define CSA_ERR_CUDA          -8  /* a CUDA runtime/driver call failed (no device, ...) */
 #define CSA_ERR_CHECK         -9  /* a device-side index check of a debug build (built with
                                      -DCSA_DEBUG) failed (reported by csa_get_status) */
+#define CSA_ERR_WORKSPACE    -10  /* dense_xwt_ws: workspace missing or smaller than
+                                     dense_xwt_workspace_size reports */
 
 /* Causal mask bit patterns for the upper triangle (t2 > t). The page writes
  * NAN (the float quiet NaN, 0x7FC00000) and notes -inf would also do. */
@@ -166,25 +173,51 @@ csa_status trimul_forward_noalloc(float* out, const void* qkv, int B, int T, int
  *   X  device, bf16, [M, I] row-major; W device, bf16, [H, I] row-major.
  *   M, I, H >= 1, any values (no tile-multiple requirement).
  *
- * X and W need only 2-byte alignment: when I*2 is a multiple of 16 and both
- * are 16-byte aligned, tiles are fetched by TMA. Otherwise (fetch mode
- * CSA_DENSE_FETCH_AUTO, the default) a first kernel copies the rows of X and W
- * into a scratch copy whose rows start on 16-byte boundaries, and the tiles
- * are fetched from it by TMA; the scratch, (M + H) * ceil8(I) * 2 bytes plus
- * at most 256, comes from a memory pool the library owns (one per device) and
- * is allocated and released in order on the call's stream, so the call may
- * be captured in a CUDA graph. If it cannot be had, or in mode
- * CSA_DENSE_FETCH_LOADERS, loader warps fetch the tiles with plain loads
- * instead (no scratch). Y is written by TMA when H*4 is a multiple of 16 and
- * Y is 16-byte aligned (4-byte alignment required otherwise).
- * Sums are fp32 accumulations of exact bf16 products, in the same order on
- * every fetch path (results are bit-identical).
+ * X and W need only 2-byte alignment. When I*2 is a multiple of 16 and both are
+ * 16-byte aligned, tiles are fetched by TMA straight from X and W. Otherwise
+ * (rows no tensor map can describe, e.g. I = 770) this call, which has no
+ * workspace, fetches them with loader warps; dense_xwt_ws computes the same
+ * layer faster with caller workspace. Y is written by TMA when H*4 is a
+ * multiple of 16 and Y is 16-byte aligned (4-byte alignment required
+ * otherwise). Sums are fp32 accumulations of exact bf16 products, in the same
+ * order on every fetch path (results are bit-identical). Nothing is allocated.
  */
 csa_status dense_xwt(float* Y, const void* X, const void* W, int M, int I, int H);
 
 /* dense_xwt_ex -- as dense_xwt on `stream` (cudaStream_t as void*). */
 csa_status dense_xwt_ex(float* Y, const void* X, const void* W, int M, int I, int H,
                         void* stream);
+
+/*
+ * dense_xwt_workspace_size -- bytes of device workspace dense_xwt_ws needs for
+ * these operands, written to *bytes: 0 when tensor maps describe the rows of X
+ * and W as they are (I*2 % 16 == 0, both 16-byte aligned), else
+ * 256 + ceil256(M*P*2) + H*P*2 with P = I rounded up to a multiple of 8 (a
+ * copy of X and W whose rows start on 16-byte boundaries, and alignment
+ * slack). Depends on the pointers' alignment and the sizes only.
+ * CSA_ERR_NULL / CSA_ERR_SHAPE as dense_xwt (then *bytes = 0).
+ */
+csa_status dense_xwt_workspace_size(const void* X, const void* W, int M, int I, int H,
+                                    size_t* bytes);
+
+/*
+ * dense_xwt_ws -- dense_xwt with caller-owned scratch, on `stream`. Where no
+ * tensor map can describe the rows of X and W, a first kernel copies them into
+ * `workspace` as rows of pitch P (16-byte multiples) and the product kernel
+ * fetches every tile from that copy by TMA, with zero fill past M, H and I --
+ * the local padding of "DietCode tests/codegen/test_1_local_padding.py"
+ * (bounds handled only where data is fetched and written back).
+ *   workspace        device, 16-byte aligned, at least dense_xwt_workspace_size
+ *                    bytes (else CSA_ERR_WORKSPACE / CSA_ERR_ALIGN, nothing
+ *                    launched); may be NULL when that size is 0.
+ *   workspace_bytes  its size.
+ * The workspace needs no clearing, and its content after a call is unspecified.
+ * It is in use until the call's kernels complete on `stream`: calls that may
+ * overlap on the GPU need separate workspaces. Results are bit-identical to
+ * dense_xwt on the same operands. Nothing is allocated.
+ */
+csa_status dense_xwt_ws(float* Y, const void* X, const void* W, int M, int I, int H,
+                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * dense_xwt_grouped -- Y[g] = X[g] W^T for g = 0 .. n-1, asynchronous on `stream`:
@@ -206,13 +239,13 @@ csa_status dense_xwt_grouped(float* const* Y, const void* const* X, const void* 
                              int n, int I, int H, void* stream);
 
 /*
- * csa_set_dense_fetch -- process-wide fetch mode of dense_xwt for rows that no
- * tensor map can describe (I*2 not a multiple of 16, or X / W not 16-byte
+ * csa_set_dense_fetch -- process-wide fetch mode of dense_xwt_ws for rows that
+ * no tensor map can describe (I*2 not a multiple of 16, or X / W not 16-byte
  * aligned):
- *   CSA_DENSE_FETCH_AUTO     copy the rows to 16-byte-aligned scratch, then TMA
- *                            (loader warps if the scratch cannot be had);
- *   CSA_DENSE_FETCH_LOADERS  loader warps inside the product kernel, no scratch.
- * Returns CSA_OK, or CSA_ERR_SHAPE for an unknown mode (the mode is unchanged).
+ *   CSA_DENSE_FETCH_AUTO     copy the rows into the caller's workspace, then TMA;
+ *   CSA_DENSE_FETCH_LOADERS  loader warps, as dense_xwt (the workspace unused).
+ * Both modes give the same bits. Returns CSA_OK, or CSA_ERR_SHAPE for an
+ * unknown mode (the mode is unchanged).
  */
 #define CSA_DENSE_FETCH_AUTO    0
 #define CSA_DENSE_FETCH_LOADERS 1

@@ -45,7 +45,7 @@ def test_checking_build_compiles_and_exports_every_symbol():
 
 
 def test_status_strings(lib):
-    for code in range(-9, 1):
+    for code in range(-10, 1):
         assert lib.csa_status_string(code)
         assert lib.csa_status_string(code) != b"unknown status"
     assert lib.csa_version().decode().endswith("sm_103a")
@@ -233,3 +233,50 @@ def test_wait_limit_default_setter_and_environment(lib):
         out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True,
                              text=True, env={**os.environ, "CSA_WAIT_LIMIT_NS": env}, check=True)
         assert int(out.stdout.strip()) == want, (env, out.stdout, out.stderr)
+
+
+def _ws_bytes(lib, X, W, M, I, H):
+    n = ctypes.c_size_t(123)
+    rc = lib.dense_xwt_workspace_size(X, W, M, I, H, ctypes.byref(n))
+    return rc, n.value
+
+
+def test_dense_workspace_size(lib):
+    """No workspace when tensor maps describe the rows as they are; otherwise the
+    realigned copy (rows padded to 8 elements, X's part 256-byte rounded) and 256
+    bytes of alignment slack."""
+    P = (770 + 7) // 8 * 8
+    r256 = lambda n: (n + 255) // 256 * 256
+    assert _ws_bytes(lib, 4096, 8192, 960, 768, 768) == (0, 0)
+    assert _ws_bytes(lib, 4096, 8192, 960, 770, 768) == (
+        0, 256 + r256(960 * P * 2) + 768 * P * 2)
+    # a misaligned view needs the copy even when I * 2 is a multiple of 16
+    rc, n = _ws_bytes(lib, 4098, 8192, 10, 768, 20)
+    assert rc == 0 and n == 256 + r256(10 * 768 * 2) + 20 * 768 * 2
+    assert _ws_bytes(lib, None, 8192, 1, 1, 1)[0] == _lib.CSA_ERR_NULL
+    assert _ws_bytes(lib, 16, 16, 0, 1, 1) == (_lib.CSA_ERR_SHAPE, 0)
+    assert lib.dense_xwt_workspace_size(16, 16, 1, 1, 1, None) == _lib.CSA_ERR_NULL
+
+
+def test_dense_ws_rejects_missing_small_or_misaligned_workspace(lib):
+    """Checked before any device is touched (this host has none)."""
+    _, need = _ws_bytes(lib, 4096, 8192, 960, 770, 768)
+    args = (1 << 20, 4096, 8192, 960, 770, 768)
+    assert lib.dense_xwt_ws(*args, None, 0, None) == _lib.CSA_ERR_WORKSPACE
+    assert b"needed" in lib.csa_last_error()
+    assert lib.dense_xwt_ws(*args, 1 << 24, need - 1, None) == _lib.CSA_ERR_WORKSPACE
+    assert lib.dense_xwt_ws(*args, (1 << 24) + 8, need, None) == _lib.CSA_ERR_ALIGN
+    assert lib.dense_xwt_ws(None, 4096, 8192, 960, 770, 768, 1 << 24, need,
+                            None) == _lib.CSA_ERR_NULL
+
+
+def test_library_sources_call_no_device_allocator():
+    """Every device buffer belongs to the caller: no source of the library calls a
+    device allocator or a memory pool (its only device memory is fixed arrays)."""
+    csrc = os.path.join(ROOT, "causal_attention_score_gb300", "csrc")
+    pat = re.compile(r"cuda(Malloc|Free|MemPool|MallocAsync|FreeAsync|MallocFromPoolAsync)"
+                     r"|cuMem(Alloc|Create|Free)")
+    for f in sorted(os.listdir(csrc)):
+        text = open(os.path.join(csrc, f), encoding="utf-8").read()
+        code = re.sub(r"//[^\n]*", "", re.sub(r"/\*.*?\*/", "", text, flags=re.S))
+        assert not pat.search(code), f"{f} calls a device allocator"

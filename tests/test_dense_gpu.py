@@ -105,8 +105,8 @@ def test_dense_sweep(oracle_lib):
 
 @pytest.fixture(params=["auto", "loaders"])
 def fetch_mode(request):
-    """Both fetch paths for rows no tensor map can describe: the realigned scratch
-    copy + TMA (default) and the loader warps (no scratch)."""
+    """Both fetch paths for rows no tensor map can describe: the rows realigned into
+    the workspace + TMA (default) and the loader warps (workspace unused)."""
     mode = csa.DENSE_FETCH_AUTO if request.param == "auto" else csa.DENSE_FETCH_LOADERS
     csa.set_dense_fetch(mode)
     yield request.param
@@ -147,8 +147,8 @@ def test_dense_fetch_mode_rejects_unknown():
 
 
 def test_dense_realigned_on_streams_and_graph(oracle_lib):
-    """The scratch copy is stream-ordered: calls on two streams at once, and the
-    call captured in a CUDA graph and replayed, give the oracle's result."""
+    """The binding's workspace is stream-ordered: calls on two streams at once, and
+    the call captured in a CUDA graph and replayed, give the oracle's result."""
     M, I, H = 300, 770, 512
     X, W = synth.dense_input(synth.DenseShape(M=M, I=I, H=H), seed=21)
     ref = oracle_lib.dense(synth.bf16_bits(X).reshape(-1), synth.bf16_bits(W).reshape(-1), M, I, H)
@@ -195,6 +195,112 @@ def test_dense_misaligned_views(oracle_lib, fetch_mode, offset):
     torch.cuda.synchronize()
     assert csa.get_status() == 0
     assert_close(Y.cpu().numpy(), ref, f"misaligned by {2 * offset} bytes")
+
+
+def _ws_call(Y, X, W, ws, stream=None):
+    M, I = X.shape
+    H = W.shape[0]
+    csa.dense_xwt_ws(Y, X, W, M, I, H, ws, stream=stream)
+
+
+def test_dense_ws_ragged_case_against_oracle(oracle_lib):
+    """dense_xwt_ws with a caller workspace on the ragged case X [960, 770], W [768, 770]
+    (seed 0): the rows realigned into the workspace, then the TMA product."""
+    s = synth.DENSE_RAGGED
+    X, W = synth.dense_input(s, seed=0)
+    ref = oracle_lib.dense(synth.bf16_bits(X).reshape(-1), synth.bf16_bits(W).reshape(-1),
+                           s.M, s.I, s.H)
+    Xd, Wd = X.cuda(), W.cuda()
+    n = csa.dense_workspace_size(Xd, Wd, s.M, s.I, s.H)
+    assert n > 0
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    Y = poisoned((s.M, s.H))
+    _ws_call(Y, Xd, Wd, ws)
+    torch.cuda.synchronize()
+    assert csa.get_status() == 0
+    assert_close(Y.cpu().numpy(), ref, "dense_xwt_ws ragged")
+
+
+@pytest.mark.parametrize("M,I,H", [(960, 770, 768), (1024, 770, 1024), (4000, 770, 768),
+                                   (300, 1002, 770), (129, 65, 129)])
+def test_dense_ws_garbage_and_reused_workspace(oracle_lib, M, I, H):
+    """The workspace needs no clearing: filled with garbage, or holding a previous
+    call's copy (of this shape or another), every call gives the oracle's result,
+    and repeated calls the same bits. Shapes with more tiles than SMs make a CTA
+    compute several tiles in turn."""
+    X, W = synth.dense_input(synth.DenseShape(M=M, I=I, H=H), seed=M + 7 * I)
+    ref = oracle_lib.dense(synth.bf16_bits(X).reshape(-1), synth.bf16_bits(W).reshape(-1), M, I, H)
+    Xd, Wd = X.cuda(), W.cuda()
+    n = csa.dense_workspace_size(Xd, Wd, M, I, H)
+    ws = torch.empty(n + 4096, dtype=torch.uint8, device="cuda")
+    ws.random_(0, 256, generator=torch.Generator(device="cuda").manual_seed(M))
+    first = None
+    for k in range(3):
+        if k == 2:
+            # a different shape through the same workspace, then this one again
+            X2, W2 = synth.dense_input(synth.DenseShape(M=33, I=I, H=65), seed=1)
+            Y2 = poisoned((33, 65))
+            _ws_call(Y2, X2.cuda(), W2.cuda(), ws)
+        Y = poisoned((M, H))
+        _ws_call(Y, Xd, Wd, ws)
+        torch.cuda.synchronize()
+        assert csa.get_status() == 0
+        assert_close(Y.cpu().numpy(), ref, f"dense_xwt_ws{(M, I, H)} call {k}")
+        if first is None:
+            first = f32_bits(Y)
+        else:
+            assert np.array_equal(f32_bits(Y), first), "repeated calls differ in bits"
+
+
+def test_dense_ws_matches_workspace_free_call_bits():
+    """dense_xwt_ex without workspace (loader warps) and dense_xwt_ws (realigned copy
+    + TMA) on the same operands: the same tiles summed in the same order, the same
+    bits."""
+    M, I, H = 960, 770, 768
+    X, W = synth.dense_input(synth.DenseShape(M=M, I=I, H=H), seed=4)
+    Xd, Wd = X.cuda(), W.cuda()
+    Ya, Yb = poisoned((M, H)), poisoned((M, H))
+    from causal_attention_score_gb300 import _lib
+    rc = _lib.load().dense_xwt_ex(Ya.data_ptr(), Xd.data_ptr(), Wd.data_ptr(), M, I, H,
+                                  torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    ws = torch.empty(csa.dense_workspace_size(Xd, Wd, M, I, H), dtype=torch.uint8,
+                     device="cuda")
+    _ws_call(Yb, Xd, Wd, ws)
+    torch.cuda.synchronize()
+    assert csa.get_status() == 0
+    assert np.array_equal(f32_bits(Ya), f32_bits(Yb))
+
+
+def test_dense_calls_leave_device_memory_unchanged():
+    """No call allocates: after a first call of each form (which loads the kernels),
+    further calls leave the device's free memory exactly where it was."""
+    M, I, H = 960, 770, 768
+    X, W = synth.dense_input(synth.DenseShape(M=M, I=I, H=H), seed=2)
+    Xd, Wd = X.cuda(), W.cuda()
+    Xs, Ws = synth.dense_input(synth.DenseShape(M=200, I=768, H=512), seed=3)
+    Xs, Ws = Xs.cuda(), Ws.cuda()
+    ws = torch.empty(csa.dense_workspace_size(Xd, Wd, M, I, H), dtype=torch.uint8,
+                     device="cuda")
+    Y, Ys = torch.empty((M, H), device="cuda"), torch.empty((200, 512), device="cuda")
+    from causal_attention_score_gb300 import _lib
+    lib = _lib.load()
+    st = torch.cuda.current_stream().cuda_stream
+
+    def calls():
+        assert lib.dense_xwt_ex(Y.data_ptr(), Xd.data_ptr(), Wd.data_ptr(), M, I, H, st) == 0
+        _ws_call(Y, Xd, Wd, ws)
+        assert lib.dense_xwt_ex(Ys.data_ptr(), Xs.data_ptr(), Ws.data_ptr(), 200, 768, 512,
+                                st) == 0
+
+    calls()
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(20):
+        calls()
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert csa.get_status() == 0
 
 
 def _grouped_vs_single(Xs, W, I, H, what):

@@ -73,8 +73,8 @@ def test_batch_matmul_nt_graph_replays():
 
 
 def test_step_graph_replays():
-    """The benchmark's step (score product, then the ragged dense layer with its
-    realigning copy) as one graph."""
+    """A step of the score product, then the ragged dense layer (its rows realigned
+    into a workspace inside its one launch), as one graph."""
     ts, ds = synth.TrimulShape(B=1, T=384, C=128, NH=2), synth.DenseShape(M=300, I=770, H=136)
     q = synth.trimul_input(ts, seed=5).cuda()
     X, W = synth.dense_input(ds, seed=6)

@@ -86,7 +86,7 @@ def test_withheld_load_softmax(oracle_lib):
     (960, 770, 768, csa.DENSE_FETCH_LOADERS),  # loader warps, 4-byte cp.async
     (300, 768, 512, csa.DENSE_FETCH_AUTO),     # TMA fetch
     (130, 771, 200, csa.DENSE_FETCH_LOADERS),  # loader warps, 2-byte loads
-    (960, 770, 768, csa.DENSE_FETCH_AUTO),     # realigned scratch copy, then TMA
+    (960, 770, 768, csa.DENSE_FETCH_AUTO),     # rows realigned into the workspace, then TMA
 ])
 def test_withheld_hand_off_dense(oracle_lib, M, I, H, mode):
     X, W = synth.dense_input(synth.DenseShape(M=M, I=I, H=H), seed=6)
