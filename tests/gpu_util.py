@@ -58,3 +58,56 @@ def trimul_case(B, T, NH, HS, seed=0, dist="normal"):
     shape = synth.TrimulShape(B=B, T=T, C=NH * HS, NH=NH)
     qkv = synth.trimul_input(shape, seed=seed, dist=dist)
     return shape, qkv
+
+
+# ----------------------------------------------------------- softmax bound --
+#
+# Per-probability bound of the fused causal softmax, from its arithmetic. With
+# a(t, u) = sum_d |q_{t,d} k_{u,d}| / sqrt(HS) (the oracle's score of |Q| and |K|)
+# and A(t) = max_{u <= t} a(t, u):
+#  - each score carries at most (HS + 4) * 2^-24 * a(t, u) of absolute error (fp32
+#    accumulation of HS exact bf16 products, the scale's and the log2(e) factor's
+#    roundings); log p = s_u - logsumexp(s) moves by at most the error of s_u plus
+#    the largest error in the row, so p moves by that much relatively;
+#  - the fp32 sum of the t + 1 exponentials: (t + 1) * 2^-24;
+#  - the exponent argument (x - m) - log2 l, of magnitude < 160 where p is not
+#    flushed: 160 * 2^-24;
+#  - the running-maximum rescales of l, one per 32 columns at most: 2^-22 each;
+#  - the approximate exp2 / log2 instructions (a few units of 2^-22 each): 2^-20.
+# Below 2^-125 the exp2 result may be flushed to zero: an absolute floor.
+SOFTMAX_FLOOR = 2.0 ** -125
+
+
+def softmax_rel_bound(abs_rows: np.ndarray, t: np.ndarray, HS: int) -> np.ndarray:
+    """Relative bound per probability for rows of a(t, u) (NaN above the diagonal);
+    `t` gives each row's query index (broadcast against abs_rows[..., 0])."""
+    a = np.where(np.isnan(abs_rows), 0.0, abs_rows)
+    A = a.max(axis=-1, keepdims=True)
+    t = np.asarray(t, dtype=np.float64)[..., None]
+    u = 2.0 ** -24
+    return ((HS + 4) * u * (a + A) + (t + 1 + 160) * u + np.ceil((t + 1) / 32) * 2.0 ** -22
+            + 2.0 ** -20)
+
+
+def assert_softmax_close(got: np.ndarray, ref: np.ndarray, rel: np.ndarray, what: str) -> None:
+    """|got - ref| <= ref * rel + 2^-125 on every entry at or below the diagonal (where
+    rel is finite); the caller checks the zeros above it bit-exactly."""
+    got = got.astype(np.float64)
+    live = np.isfinite(rel) & ~np.isnan(ref)
+    err = np.abs(got - ref)
+    bound = np.where(live, np.where(live, ref, 0.0) * np.where(live, rel, 0.0), 0.0) + SOFTMAX_FLOOR
+    bad = live & ~(err <= bound)
+    if bad.any():
+        idx = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{what}: probability {got[idx]!r} vs oracle {ref[idx]!r} at {idx}: "
+                             f"error {err[idx]:.3e} above the bound {bound[idx]:.3e}")
+
+
+def softmax_abs_scores(oracle_lib, qkv: torch.Tensor, B: int, T: int, C: int, NH: int,
+                       bht: np.ndarray | None = None) -> np.ndarray:
+    """a(t, u) from the oracle's score of |Q| and |K| (bf16 magnitudes are exact):
+    (B, NH, T, T), or the rows of bht (n x T); NaN above the diagonal."""
+    bits = synth.bf16_bits(qkv).reshape(-1) & np.uint16(0x7FFF)
+    if bht is None:
+        return oracle_lib.trimul(bits, B, T, C, NH)
+    return oracle_lib.trimul_rows(bits, B, T, C, NH, bht)

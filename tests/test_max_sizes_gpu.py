@@ -9,7 +9,8 @@ import torch
 
 import causal_attention_score_gb300 as csa
 from causal_attention_score_gb300 import synth
-from gpu_util import NAN_BITS, POISON_BITS, assert_close, f32_bits, poisoned
+from gpu_util import (NAN_BITS, POISON_BITS, assert_close, assert_softmax_close, f32_bits,
+                      poisoned, softmax_abs_scores, softmax_rel_bound)
 
 pytestmark = pytest.mark.gpu
 
@@ -76,6 +77,10 @@ def test_softmax_sequence_16384(oracle_lib):
     ref = oracle_lib.causal_softmax_rows(synth.bf16_bits(qkv).reshape(-1), 1, T, shape.C, 1, bht)
     got = att[0, 0, torch.tensor(rows, device="cuda")].cpu().numpy()
     assert_close(got, ref, "softmax T=16384 rows")
+    rel = softmax_rel_bound(softmax_abs_scores(oracle_lib, qkv, 1, T, shape.C, 1, bht),
+                            bht[:, 2], shape.HS)
+    rel = np.where(np.arange(T)[None, :] > bht[:, 2:3], np.inf, rel)
+    assert_softmax_close(got, ref, rel, "softmax T=16384 rows (relative bound)")
 
 
 def test_4096_one_tile_heads(oracle_lib):

@@ -8,7 +8,8 @@ import torch
 
 import causal_attention_score_gb300 as csa
 from causal_attention_score_gb300 import synth
-from gpu_util import POISON_BITS, assert_close, f32_bits
+from gpu_util import (POISON_BITS, assert_close, assert_softmax_close, f32_bits,
+                      softmax_abs_scores, softmax_rel_bound)
 
 pytestmark = pytest.mark.gpu
 
@@ -68,6 +69,10 @@ def test_softmax_long_context_full_size(oracle_lib):
     idx = torch.from_numpy(bht).cuda()
     got = att[idx[:, 0], idx[:, 1], idx[:, 2]].cpu().numpy()
     assert_close(got, ref, "long-context softmax rows")
+    rel = softmax_rel_bound(softmax_abs_scores(oracle_lib, qkv, s.B, T, s.C, s.NH, bht),
+                            bht[:, 2], s.HS)
+    rel = np.where(np.arange(T)[None, :] > bht[:, 2:3], np.inf, rel)
+    assert_softmax_close(got, ref, rel, "long-context softmax rows (relative bound)")
 
 
 def test_trimul_f32_long_context_full_size(oracle_lib):
