@@ -485,6 +485,8 @@ def run_ours(args, rank, world, local):
     import torch
 
     import causal_attention_score_gb300 as csa
+    from causal_attention_score_gb300 import build_lib
+    build_lib.build()  # a no-op when the library matches its sources
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)

@@ -22,6 +22,7 @@ CSA_ERR_TIMEOUT = -7
 CSA_ERR_CUDA = -8
 CSA_ERR_CHECK = -9
 CSA_ERR_WORKSPACE = -10
+CSA_ERR_BUSY = -11
 
 CSA_MASK_NAN = 0x7FC00000
 CSA_MASK_NEG_INF = 0xFF800000
@@ -51,6 +52,8 @@ SIGNATURES = {
     "csa_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "csa_get_wait_limit_ns": (ctypes.c_uint64, []),
     "csa_debug_inject": (None, [_i]),
+    "csa_debug_hold_stream": (_i, [_vp]),
+    "csa_debug_release_streams": (None, []),
     "csa_set_dense_fetch": (_i, [_i]),
 }
 
@@ -78,6 +81,11 @@ def load(path: str | None = None):
             if not os.path.exists(p):
                 raise RuntimeError(
                     f"CUDA extension {p} is not built; run causal_attention_score_gb300.build_lib.build()")
+            if path is None and not build_lib.up_to_date(p):
+                raise RuntimeError(
+                    f"CUDA extension {p} was not built from the sources beside it (its "
+                    f"{os.path.basename(build_lib.stamp_path(p))} does not match); run "
+                    "causal_attention_score_gb300.build_lib.build()")
             lib = ctypes.CDLL(p)
             for name, (res, args) in SIGNATURES.items():
                 fn = getattr(lib, name)

@@ -1,5 +1,9 @@
 """Builds libcsa_gb300.so in-tree with nvcc for sm_103a only.
 
+A built library is stamped with a SHA-256 of its sources (``<lib>.sha256``); it is
+rebuilt whenever the sources differ from the stamp, and the binding refuses to
+load a library whose stamp does not match the sources beside it.
+
 Each ``csrc/*.cu`` is compiled to an object in parallel, then linked into a
 shared library with the CUDA runtime linked statically (so loading the
 library needs no GPU and no libcuda; the driver is reached at first use).
@@ -11,6 +15,7 @@ from __future__ import annotations
 
 import concurrent.futures as cf
 import glob
+import hashlib
 import os
 import shutil
 import subprocess
@@ -49,11 +54,29 @@ def _deps():
             + glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)])
 
 
-def up_to_date(path: str = LIBPATH) -> bool:
-    if not os.path.exists(path):
+def source_hash(debug: bool = False) -> str:
+    """SHA-256 of every source the library is built from (csrc/, include/, this file)
+    and of the compiler flags: what a built library is stamped with."""
+    h = hashlib.sha256()
+    for f in sorted(_deps()):
+        h.update(os.path.relpath(f, ROOT).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    h.update(" ".join(ARCH + ["debug" if debug else "release"]).encode())
+    return h.hexdigest()
+
+
+def stamp_path(path: str) -> str:
+    """The file beside a built library that holds the source hash it was built from."""
+    return path + ".sha256"
+
+
+def up_to_date(path: str = LIBPATH, debug: bool = False) -> bool:
+    """True when the library exists and was built from the current sources."""
+    if not os.path.exists(path) or not os.path.exists(stamp_path(path)):
         return False
-    t = os.path.getmtime(path)
-    return all(os.path.getmtime(d) <= t for d in _deps())
+    with open(stamp_path(path)) as f:
+        return f.read().strip() == source_hash(debug)
 
 
 def _compile(src: str, verbose_ptxas: bool, debug: bool = False) -> str:
@@ -73,8 +96,9 @@ def build(force: bool = False, verbose_ptxas: bool = False, debug: bool = False)
     """Compile and link the library (or, with debug=True, its checking variant) if any
     source changed; returns its path."""
     path = DEBUG_LIBPATH if debug else LIBPATH
-    if not force and up_to_date(path):
+    if not force and up_to_date(path, debug):
         return path
+    digest = source_hash(debug)
     os.makedirs(DEBUG_BUILD if debug else BUILD, exist_ok=True)
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
@@ -85,6 +109,9 @@ def build(force: bool = False, verbose_ptxas: bool = False, debug: bool = False)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, path)
+    with open(stamp_path(path) + f".tmp{os.getpid()}", "w") as f:
+        f.write(digest + "\n")
+    os.replace(stamp_path(path) + f".tmp{os.getpid()}", stamp_path(path))
     return path
 
 

@@ -7,6 +7,8 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <chrono>
+#include <condition_variable>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -232,6 +234,117 @@ uint64_t default_wait_limit_ns() {
 uint64_t wait_limit_ns() {
   const uint64_t v = g_wait_limit_ns.load();
   return v ? v : default_wait_limit_ns();
+}
+
+namespace {
+
+struct SlotFamily {
+  bool ready = false;
+  volatile unsigned long long* done_host = nullptr;  // page-locked, mapped: [kDirectSlots]
+  unsigned long long* done_dev = nullptr;
+  unsigned long long stream_id[kDirectSlots] = {};
+  unsigned long long seq[kDirectSlots] = {};
+  bool used[kDirectSlots] = {};
+  int next_capture = 0;
+  int cursor = 0;
+  unsigned long long next_seq = 0;
+};
+
+std::mutex g_slot_mu;
+SlotFamily g_slot_families[2][kMaxDevices];
+
+}  // namespace
+
+int acquire_counter_slot(int family, const DeviceInfo& dev, unsigned int* base, cudaStream_t stream,
+                         CounterSlot& out, std::string& err) {
+  if (family < 0 || family > 1 || dev.device < 0 || dev.device >= kMaxDevices || !base) {
+    err = "counter slots: bad family or device";
+    return CSA_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_slot_mu);
+  SlotFamily& f = g_slot_families[family][dev.device];
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+  if (e != cudaSuccess) {
+    err = std::string("cudaStreamIsCapturing: ") + cudaGetErrorString(e);
+    return CSA_ERR_CUDA;
+  }
+  if (cs != cudaStreamCaptureStatusNone) {
+    if (f.next_capture >= kCaptureSlots) {
+      err = "more than " + std::to_string(kCaptureSlots) +
+            " launches of this kernel captured into CUDA graphs in this process";
+      return CSA_ERR_BUSY;
+    }
+    out.counters = base + kCounterWords * (kDirectSlots + f.next_capture++);
+    out.done = nullptr;
+    out.seq = 0;
+    out.slot = -1;
+    return CSA_OK;
+  }
+  // (made at the first launch outside capture: a captured launch needs none)
+  if (!f.ready) {
+    void* h = nullptr;
+    e = cudaHostAlloc(&h, sizeof(unsigned long long) * kDirectSlots,
+                      cudaHostAllocMapped | cudaHostAllocPortable);
+    if (e != cudaSuccess) {
+      err = std::string("counter slots: page-locked completion words: ") + cudaGetErrorString(e);
+      return CSA_ERR_CUDA;
+    }
+    std::memset(h, 0, sizeof(unsigned long long) * kDirectSlots);
+    void* d = nullptr;
+    e = cudaHostGetDevicePointer(&d, h, 0);
+    if (e != cudaSuccess) {
+      cudaFreeHost(h);
+      err = std::string("counter slots: cudaHostGetDevicePointer: ") + cudaGetErrorString(e);
+      return CSA_ERR_CUDA;
+    }
+    f.done_host = static_cast<volatile unsigned long long*>(h);
+    f.done_dev = static_cast<unsigned long long*>(d);
+    f.ready = true;
+  }
+  unsigned long long sid = 0;
+  e = cudaStreamGetId(stream, &sid);
+  if (e != cudaSuccess) {
+    err = std::string("cudaStreamGetId: ") + cudaGetErrorString(e);
+    return CSA_ERR_CUDA;
+  }
+  int s = -1;
+  for (int i = 0; i < kDirectSlots; ++i)
+    if (f.used[i] && f.stream_id[i] == sid) {
+      s = i;
+      break;
+    }
+  if (s < 0) {
+    for (int k = 0; k < kDirectSlots; ++k) {
+      const int i = (f.cursor + k) % kDirectSlots;
+      if (!f.used[i] || f.done_host[i] == f.seq[i]) {
+        s = i;
+        break;
+      }
+    }
+    if (s < 0) {
+      err = "launches on " + std::to_string(kDirectSlots) +
+            " other streams are still in flight (work-list counter sets exhausted)";
+      return CSA_ERR_BUSY;
+    }
+    f.cursor = (s + 1) % kDirectSlots;
+    f.used[s] = true;
+    f.stream_id[s] = sid;
+  }
+  f.seq[s] = ++f.next_seq;
+  out.counters = base + kCounterWords * s;
+  out.done = f.done_dev + s;
+  out.seq = f.seq[s];
+  out.slot = s;
+  return CSA_OK;
+}
+
+void abandon_counter_slot(int family, const DeviceInfo& dev, const CounterSlot& slot) {
+  if (slot.slot < 0 || family < 0 || family > 1 || dev.device < 0 || dev.device >= kMaxDevices)
+    return;
+  std::lock_guard<std::mutex> lock(g_slot_mu);
+  SlotFamily& f = g_slot_families[family][dev.device];
+  if (f.ready && f.seq[slot.slot] == slot.seq) f.done_host[slot.slot] = slot.seq;
 }
 
 bool take_inject() { return g_inject.exchange(0) != 0; }
@@ -494,6 +607,7 @@ const char* csa_status_string(csa_status s) {
     case CSA_ERR_CUDA: return "CUDA call failed";
     case CSA_ERR_CHECK: return "device-side index check failed (debug build)";
     case CSA_ERR_WORKSPACE: return "workspace missing or too small";
+    case CSA_ERR_BUSY: return "work-list counter sets exhausted";
     default: return "unknown status";
   }
 }
@@ -507,6 +621,47 @@ void csa_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns); }
 uint64_t csa_get_wait_limit_ns(void) { return csa::wait_limit_ns(); }
 
 void csa_debug_inject(int enable) { g_inject.store(enable ? 1 : 0); }
+
+}  // extern "C"
+
+namespace {
+
+// Streams held by csa_debug_hold_stream: each hold is a host function that
+// waits for its release (or 10 s) on the CUDA runtime's callback thread.
+std::mutex g_hold_mu;
+std::condition_variable g_hold_cv;
+unsigned long long g_hold_issued = 0, g_hold_released = 0;
+
+void CUDART_CB hold_stream_fn(void* arg) {
+  const unsigned long long gen = static_cast<unsigned long long>(reinterpret_cast<uintptr_t>(arg));
+  std::unique_lock<std::mutex> lock(g_hold_mu);
+  g_hold_cv.wait_for(lock, std::chrono::seconds(10), [&] { return g_hold_released >= gen; });
+}
+
+}  // namespace
+
+extern "C" {
+
+csa_status csa_debug_hold_stream(void* stream) {
+  t_last_error.clear();
+  unsigned long long gen;
+  {
+    std::lock_guard<std::mutex> lock(g_hold_mu);
+    gen = ++g_hold_issued;
+  }
+  cudaError_t e = cudaLaunchHostFunc(static_cast<cudaStream_t>(stream), hold_stream_fn,
+                                     reinterpret_cast<void*>(static_cast<uintptr_t>(gen)));
+  if (e != cudaSuccess) return cuda_error("csa_debug_hold_stream", e);
+  return CSA_OK;
+}
+
+void csa_debug_release_streams(void) {
+  {
+    std::lock_guard<std::mutex> lock(g_hold_mu);
+    g_hold_released = g_hold_issued;
+  }
+  g_hold_cv.notify_all();
+}
 
 csa_status csa_set_dense_fetch(int mode) {
   if (mode != CSA_DENSE_FETCH_AUTO && mode != CSA_DENSE_FETCH_LOADERS)

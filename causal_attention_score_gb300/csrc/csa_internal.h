@@ -74,6 +74,40 @@ cudaError_t launch_programmatic_cluster(void (*kernel)(KArgs...), unsigned grid,
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
+// ---------------------------------------------------- work-list counter slots --
+//
+// The score and softmax kernels take work-list positions from a set of global
+// counters that the last CTA of each launch resets to zero. Two launches may
+// share a set only if they never run at the same time. Each kernel family keeps
+// kDirectSlots + kCaptureSlots sets per device (a fixed device array) and hands
+// them out as follows:
+//  - a launch outside stream capture uses its stream's set: launches on one
+//    stream run in order. A stream's set is taken from a set whose last launch
+//    has signalled completion (the kernel's last CTA writes the launch's number
+//    into page-locked host memory) or that was never used; when all direct sets
+//    belong to streams with launches in flight, the call fails with CSA_ERR_BUSY;
+//  - a launch captured into a CUDA graph gets a set of its own for good (the
+//    graph may be replayed at any time, next to anything else): at most
+//    kCaptureSlots captured launches per kernel family and process.
+constexpr int kCounterWords = 4;
+constexpr int kDirectSlots = 256;
+constexpr int kCaptureSlots = 1024;
+enum CounterFamily : int { kFamilyScores = 0, kFamilySoftmax = 1 };
+
+struct CounterSlot {
+  unsigned int* counters = nullptr;  // the set (kCounterWords words), zero at launch
+  unsigned long long* done = nullptr;  // device address of its completion word (nullptr: none)
+  unsigned long long seq = 0;          // number the launch writes there when it completes
+  int slot = -1;                       // direct slot index, -1 for a captured set
+};
+
+// The set for a launch on `stream`; `base` is the family's device array of
+// (kDirectSlots + kCaptureSlots) * kCounterWords words.
+int acquire_counter_slot(int family, const DeviceInfo& dev, unsigned int* base, cudaStream_t stream,
+                         CounterSlot& out, std::string& err);
+// A launch given `slot` failed: its set is free again.
+void abandon_counter_slot(int family, const DeviceInfo& dev, const CounterSlot& slot);
+
 // Bound (ns of %globaltimer) on every mbarrier/flag wait in the kernels.
 uint64_t wait_limit_ns();
 // True once after csa_debug_inject armed it: the next launch withholds one arrival.

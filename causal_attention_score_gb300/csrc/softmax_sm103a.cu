@@ -67,14 +67,14 @@ constexpr int kZeroBytes = kZeroCols * kZeroRows * 4;
 constexpr int kStatsBytes = 2 * kEpiWarps * 32 * 8;  // (m, l) per row half, two units
 constexpr int kTmemCols = 2 * kTile;
 constexpr int kRingDepth = 4;
-constexpr int kSlots = 256;
 constexpr unsigned int kEnd = 0xFFFFFFFFu;
 constexpr uint32_t kIdesc = idesc_bf16_f32(kTile, kTile);
 
-// Work-list counters, one set per launch in flight: [0] row-block units,
-// [1] finished CTAs, [2] zero tiles. The last CTA to finish resets its set.
-constexpr int kSchedWords = 4;
-__device__ unsigned int g_softmax_sched[kSlots][kSchedWords];
+// Work-list counters: [0] row-block units, [1] finished CTAs, [2] zero tiles; sets
+// handed out by acquire_counter_slot (one per stream, or one per captured launch).
+// The last CTA to finish resets its set.
+constexpr int kSchedWords = kCounterWords;
+__device__ unsigned int g_softmax_sched[kDirectSlots + kCaptureSlots][kSchedWords];
 constexpr int kPrefetchK = 4;  // K tiles of the next unit prefetched into L2
 // Staging pairs per epilogue warp (at most) and K ring depth (at most).
 #ifndef CSA_SOFTMAX_MAX_PAIRS
@@ -106,6 +106,8 @@ struct SoftmaxArgs {
   int* status;
   unsigned long long wait_limit_ns;
   unsigned int* sched;
+  unsigned long long* done;  // completion word of the counter set
+  unsigned long long seq;    // written there by the last CTA, after the counters' reset
   int inject;  // withhold each CTA's first Q load (watchdog tests)
   uint32_t q_bytes, k_bytes;
   uint32_t off_k, off_staging, off_zero, off_stats, off_bars, off_misc;
@@ -693,6 +695,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       atomicExch(a.sched, 0u);
       atomicExch(a.sched + 2, 0u);
       atomicExch(a.sched + 1, 0u);
+      if (a.done) {
+        // the set is free for another stream once the host sees this
+        __threadfence_system();
+        *reinterpret_cast<volatile unsigned long long*>(a.done) = a.seq;
+      }
     }
   }
 }
@@ -794,27 +801,6 @@ int softmax_launch(float* out, const void* qkv, int B, int T, int C, int NH, cud
     std::memset(&map_zero, 0, sizeof map_zero);
   }
   {
-    static std::mutex mu;
-    static unsigned int* sched_base[64] = {};
-    static std::atomic<unsigned int> launch_seq{0};
-    std::lock_guard<std::mutex> lock(mu);
-    if (dev.device < 0 || dev.device >= 64) {
-      err = "causal_softmax_forward: device ordinal out of range";
-      return CSA_ERR_CUDA;
-    }
-    if (!sched_base[dev.device]) {
-      void* p = nullptr;
-      cudaError_t se = cudaGetSymbolAddress(&p, g_softmax_sched);
-      if (se != cudaSuccess) {
-        err = std::string("causal_softmax_forward: cudaGetSymbolAddress: ") +
-              cudaGetErrorString(se);
-        return CSA_ERR_CUDA;
-      }
-      sched_base[dev.device] = static_cast<unsigned int*>(p);
-    }
-    a.sched = sched_base[dev.device] + kSchedWords * (launch_seq.fetch_add(1) % kSlots);
-  }
-  {
     int rc = set_max_dynamic_smem(reinterpret_cast<const void*>(softmax_sm103a_kernel),
                                   static_cast<int>(smem), dev.device, err);
     if (rc != CSA_OK) {
@@ -822,12 +808,43 @@ int softmax_launch(float* out, const void* qkv, int B, int T, int C, int NH, cud
       return rc;
     }
   }
+  CounterSlot slot;
+  {
+    static std::mutex mu;
+    static unsigned int* sched_base[64] = {};
+    {
+      std::lock_guard<std::mutex> lock(mu);
+      if (dev.device < 0 || dev.device >= 64) {
+        err = "causal_softmax_forward: device ordinal out of range";
+        return CSA_ERR_CUDA;
+      }
+      if (!sched_base[dev.device]) {
+        void* p = nullptr;
+        cudaError_t se = cudaGetSymbolAddress(&p, g_softmax_sched);
+        if (se != cudaSuccess) {
+          err = std::string("causal_softmax_forward: cudaGetSymbolAddress: ") +
+                cudaGetErrorString(se);
+          return CSA_ERR_CUDA;
+        }
+        sched_base[dev.device] = static_cast<unsigned int*>(p);
+      }
+    }
+    int rc = acquire_counter_slot(kFamilySoftmax, dev, sched_base[dev.device], stream, slot, err);
+    if (rc != CSA_OK) {
+      err = "causal_softmax_forward: " + err;
+      return rc;
+    }
+    a.sched = slot.counters;
+    a.done = slot.done;
+    a.seq = slot.seq;
+  }
   cudaError_t e;
   const long long grid = std::min<long long>(a.n_units, dev.sm_count);
   e = launch_programmatic(softmax_sm103a_kernel, static_cast<unsigned>(grid), kThreads, smem,
                           stream, map_qkv, map_out, map_zero, a);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
+    abandon_counter_slot(kFamilySoftmax, dev, slot);
     err = std::string("causal_softmax_forward: launch: ") + cudaGetErrorString(e);
     return CSA_ERR_LAUNCH;
   }

@@ -129,6 +129,8 @@ struct TrimulArgs {
   int per_lower, per_fill;  // lower / fill tiles per (b, h)
   uint32_t dynamic;     // 1: work-list positions from the shared counter; 0: dealt statically
   unsigned int* sched;  // this launch's counters: [0] next position, [1] CTAs done, [2] next fill
+  unsigned long long* done;  // completion word of the counter set (nullptr: none)
+  unsigned long long seq;    // written there by the last CTA, after the counters' reset
   float scale;
   uint32_t mask_bits;
   uint32_t lower_only;
@@ -159,12 +161,11 @@ struct TrimulArgs {
 };
 
 // Counters per launch: [0] work-list position, [1] finished CTAs, [2] fill tile.
-constexpr int kSchedWords = 4;
+constexpr int kSchedWords = kCounterWords;
 
-// Work-list counters, one set per launch in flight (slot chosen by the host);
-// the last CTA of a launch resets its set to zero.
-constexpr int kSchedSlots = 256;
-__device__ unsigned int g_trimul_sched[kSchedSlots][kSchedWords];
+// Work-list counter sets, handed out by acquire_counter_slot (one per stream, or
+// one per captured launch); the last CTA of a launch resets its set to zero.
+__device__ unsigned int g_trimul_sched[kDirectSlots + kCaptureSlots][kSchedWords];
 
 #ifndef CSA_TRIMUL_SCHED_DEPTH
 #define CSA_TRIMUL_SCHED_DEPTH 4
@@ -954,6 +955,11 @@ __global__ void __launch_bounds__(kF32 ? kThreadsF32 : kThreads, 1)
       atomicExch(a.sched, 0u);
       atomicExch(a.sched + 2, 0u);
       atomicExch(a.sched + 1, 0u);
+      if (a.done) {
+        // the set is free for another stream once the host sees this
+        __threadfence_system();
+        *reinterpret_cast<volatile unsigned long long*>(a.done) = a.seq;
+      }
     }
   }
 }
@@ -1082,28 +1088,38 @@ int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& 
     std::memset(&map_fill, 0, sizeof map_fill);
   }
 
+  CounterSlot slot;
   if (counters) {
     a.sched = counters;  // caller-provided counters (zeroed before this launch)
-  } else {
+  } else if (a.dynamic || a.n_fill > 0) {
     static std::mutex mu;
     static unsigned int* sched_base[64] = {};
-    static std::atomic<unsigned int> launch_seq{0};
-    std::lock_guard<std::mutex> lock(mu);
-    if (dev.device < 0 || dev.device >= 64) {
-      err = name + ": device ordinal out of range";
-      return CSA_ERR_CUDA;
-    }
-    if (!sched_base[dev.device]) {
-      void* p = nullptr;
-      cudaError_t se = cudaGetSymbolAddress(&p, g_trimul_sched);
-      if (se != cudaSuccess) {
-        err = name + ": cudaGetSymbolAddress: " + cudaGetErrorString(se);
+    {
+      std::lock_guard<std::mutex> lock(mu);
+      if (dev.device < 0 || dev.device >= 64) {
+        err = name + ": device ordinal out of range";
         return CSA_ERR_CUDA;
       }
-      sched_base[dev.device] = static_cast<unsigned int*>(p);
+      if (!sched_base[dev.device]) {
+        void* p = nullptr;
+        cudaError_t se = cudaGetSymbolAddress(&p, g_trimul_sched);
+        if (se != cudaSuccess) {
+          err = name + ": cudaGetSymbolAddress: " + cudaGetErrorString(se);
+          return CSA_ERR_CUDA;
+        }
+        sched_base[dev.device] = static_cast<unsigned int*>(p);
+      }
     }
-    a.sched = sched_base[dev.device] + kSchedWords * (launch_seq.fetch_add(1) % kSchedSlots);
+    int rc = acquire_counter_slot(kFamilyScores, dev, sched_base[dev.device], stream, slot, err);
+    if (rc != CSA_OK) {
+      err = name + ": " + err;
+      return rc;
+    }
+    a.sched = slot.counters;
+    a.done = slot.done;
+    a.seq = slot.seq;
   }
+  // (a static deal without fill tiles never touches the counters: no set at all)
   auto* kernel = !f32         ? trimul_sm103a_kernel<false, false>
                  : single_box ? trimul_sm103a_kernel<true, true>
                               : trimul_sm103a_kernel<true, false>;
@@ -1111,6 +1127,7 @@ int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& 
     int rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kernel), static_cast<int>(smem),
                                   dev.device, err);
     if (rc != CSA_OK) {
+      abandon_counter_slot(kFamilyScores, dev, slot);
       err = name + ": " + err;
       return rc;
     }
@@ -1122,6 +1139,7 @@ int launch_scores(const char* who, const CUtensorMap& map_a, const CUtensorMap& 
                           stream, map_a, map_b, map_out, map_fill, a);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
+    abandon_counter_slot(kFamilyScores, dev, slot);
     err = name + ": launch: " + cudaGetErrorString(e);
     return CSA_ERR_LAUNCH;
   }
@@ -1288,3 +1306,17 @@ int trimul_launch_noalloc(float* out, const void* qkv, int B, int T, int C, int 
 }
 
 }  // namespace csa
+
+#ifdef CSA_DEBUG
+// Checking build only: fills the allocation-free entry point's scratch with
+// `value` in every word, as an earlier launch that stopped mid-list would leave
+// its counters, so that a test can see each call clear them before its kernel.
+extern "C" csa_status csa_debug_noalloc_scratch_fill(uint32_t value) {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, csa::g_trimul_noalloc_scratch) != cudaSuccess) return CSA_ERR_CUDA;
+  uint32_t words[csa::kNoallocScratchBytes / 4];
+  for (uint32_t& w : words) w = value;
+  return cudaMemcpy(p, words, sizeof words, cudaMemcpyHostToDevice) == cudaSuccess ? CSA_OK
+                                                                                   : CSA_ERR_CUDA;
+}
+#endif

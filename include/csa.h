@@ -33,7 +33,7 @@
  *    scratch space included (dense_xwt_ws); no call allocates device memory.
  *    The library keeps, per device, only fixed arrays in its own image: the
  *    status word, the kernels' work-list counters and the scratch of
- *    trimul_forward_noalloc.
+ *    trimul_forward_noalloc (plus the page-locked completion words below).
  *  - bf16 inputs are passed as `const void*` to raw 16-bit bfloat16 values.
  *  - Outputs are fp32 and fully overwritten (no read-modify-write).
  *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
@@ -41,6 +41,18 @@
  *    returned synchronously before anything is launched.
  *  - Return value: CSA_OK (0) or a negative csa_status. A failed call launches
  *    nothing and leaves the output untouched; csa_last_error() then describes it.
+ *  - Work-list counters (trimul_forward, trimul_forward_ex, trimul_forward_f32,
+ *    causal_softmax_forward): these kernels take work from a set of counters
+ *    that their last CTA resets. A launch outside stream capture uses its
+ *    stream's set (launches on one stream run in order); a stream gets a set
+ *    that was never used or whose last launch has reported completion (through
+ *    a 2 KB page-locked host array per kernel and device, made at the first such
+ *    launch on that device -- make it outside any stream capture). With launches
+ *    still in flight on 256 other streams, the call returns CSA_ERR_BUSY. A
+ *    launch captured into a CUDA graph gets a set of its own for good, at most
+ *    1024 per kernel and process (then CSA_ERR_BUSY); a graph instantiated more
+ *    than once must not have two instances running at once. Launches whose work
+ *    is dealt statically (lower-only scores, batch_matmul_nt) use no set.
  *  - The library keeps one device status word per device. A kernel whose
  *    bounded wait ran out records CSA_ERR_TIMEOUT there and returns early
  *    (its output is then incomplete); csa_get_status() reports and clears it.
@@ -72,6 +84,9 @@ typedef int csa_status;
                                      -DCSA_DEBUG) failed (reported by csa_get_status) */
 #define CSA_ERR_WORKSPACE    -10  /* dense_xwt_ws: workspace missing or smaller than
                                      dense_xwt_workspace_size reports */
+#define CSA_ERR_BUSY         -11  /* no work-list counter set free: score or softmax
+                                     launches in flight on 256 other streams, or more
+                                     than 1024 of them captured into CUDA graphs */
 
 /* Causal mask bit patterns for the upper triangle (t2 > t). The page writes
  * NAN (the float quiet NaN, 0x7FC00000) and notes -inf would also do. */
@@ -318,6 +333,17 @@ const char* csa_version(void);
 void csa_set_wait_limit_ns(uint64_t ns);
 uint64_t csa_get_wait_limit_ns(void);
 void csa_debug_inject(int enable);
+
+/*
+ * Stream holds, for tests of launches that wait on the host (no GPU wait involved).
+ *
+ * csa_debug_hold_stream -- enqueues on `stream` a host function that returns once
+ *   csa_debug_release_streams is called (or after 10 s): work enqueued behind it
+ *   starts only then. CSA_ERR_CUDA if the host function cannot be enqueued.
+ * csa_debug_release_streams -- releases every hold enqueued so far.
+ */
+csa_status csa_debug_hold_stream(void* stream);
+void csa_debug_release_streams(void);
 
 #ifdef __cplusplus
 }

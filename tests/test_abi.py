@@ -45,7 +45,7 @@ def test_checking_build_compiles_and_exports_every_symbol():
 
 
 def test_status_strings(lib):
-    for code in range(-10, 1):
+    for code in range(-11, 1):
         assert lib.csa_status_string(code)
         assert lib.csa_status_string(code) != b"unknown status"
     assert lib.csa_version().decode().endswith("sm_103a")
@@ -274,9 +274,23 @@ def test_library_sources_call_no_device_allocator():
     """Every device buffer belongs to the caller: no source of the library calls a
     device allocator or a memory pool (its only device memory is fixed arrays)."""
     csrc = os.path.join(ROOT, "causal_attention_score_gb300", "csrc")
-    pat = re.compile(r"cuda(Malloc|Free|MemPool|MallocAsync|FreeAsync|MallocFromPoolAsync)"
-                     r"|cuMem(Alloc|Create|Free)")
+    pat = re.compile(r"cuda(Malloc|Free)(?!Host)|cudaMemPool|cuMem(Alloc|Create|Free)")
     for f in sorted(os.listdir(csrc)):
         text = open(os.path.join(csrc, f), encoding="utf-8").read()
         code = re.sub(r"//[^\n]*", "", re.sub(r"/\*.*?\*/", "", text, flags=re.S))
         assert not pat.search(code), f"{f} calls a device allocator"
+
+
+def test_library_is_stamped_with_its_sources(tmp_path, monkeypatch):
+    """build() stamps the library with a hash of its sources; a source edit makes the
+    stamp stale (so build() rebuilds and the binding refuses the old binary)."""
+    path = build_lib.build()
+    assert build_lib.up_to_date(path)
+    with open(build_lib.stamp_path(path)) as f:
+        assert f.read().strip() == build_lib.source_hash()
+    extra = tmp_path / "extra.h"
+    extra.write_text("// one more header\n")
+    deps = build_lib._deps()
+    monkeypatch.setattr(build_lib, "_deps", lambda: deps + [str(extra)])
+    assert not build_lib.up_to_date(path)
+    assert build_lib.source_hash() != build_lib.source_hash(debug=True)

@@ -107,3 +107,21 @@ def test_dense_grouped(dbg):
     torch.cuda.synchronize()
     for g in range(n):
         _same_and_clean(dbg, a[g], b[g], f"grouped problem {g}")
+
+
+def test_noalloc_clears_scratch_left_mid_list(dbg):
+    """trimul_forward_noalloc clears its fixed scratch before each kernel: with the
+    counters left non-zero (as by a launch that stopped mid-list; the checking build
+    can plant that), the call still writes every tile, the release library's bits."""
+    fill = dbg.csa_debug_noalloc_scratch_fill
+    fill.restype, fill.argtypes = ctypes.c_int, [ctypes.c_uint32]
+    shape, qkv = trimul_case(2, 300, 3, 64, seed=41)
+    q = qkv.cuda()
+    a = poisoned(shape.out_shape)
+    csa.trimul_forward(a, q, 2, 300, shape.C, 3)
+    for value in (7, 0x00FFFFFF):
+        assert fill(value) == 0
+        b = poisoned(shape.out_shape)
+        assert dbg.trimul_forward_noalloc(b.data_ptr(), q.data_ptr(), 2, 300, shape.C, 3,
+                                          _lib.CSA_MASK_NAN, 0, _stream()) == 0
+        _same_and_clean(dbg, a, b, f"noalloc after scratch filled with {value:#x}")
