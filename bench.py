@@ -755,24 +755,36 @@ class OracleSample:
                     "a step")
         return "one (b,h) head of trimul GPT-2 (1024 rows) + 64 rows of dense ragged"
 
-    def __call__(self, o, i):
-        """Runs sample i on oracle `o`; returns its useful flops."""
+    def parts(self, i):
+        """What sample i computes: the (b, h, t) rows of the score product and, per dense
+        problem, its rows; with the useful flops of each."""
         np = self.np
         ts = self.ts
         bh = i % (ts.B * ts.NH)
         b, h = divmod(bh, ts.NH)
         bht = np.array([(b, h, t) for t in range(ts.T)], dtype=np.int64)
-        o.trimul_rows(self.qkv, ts.B, ts.T, ts.C, ts.NH, bht)
-        flops = 2 * ts.HS * ts.T * (ts.T + 1) // 2
+        dense = []
         for xb, wb, M, I, H in self.dense:
             if self.sweep:
                 rows = np.arange(i % self.stride, M, self.stride, dtype=np.int64)
             else:
                 rows = (np.arange(64, dtype=np.int64) + 64 * i) % M
+            dense.append((xb, wb, M, I, H, rows))
+        return bht, 2 * ts.HS * ts.T * (ts.T + 1) // 2, dense
+
+    def flops(self, i):
+        _, f, dense = self.parts(i)
+        return f + sum(2 * int(rows.size) * I * H for _, _, _, I, H, rows in dense)
+
+    def __call__(self, o, i):
+        """Runs sample i on oracle `o`; returns its useful flops."""
+        ts = self.ts
+        bht, _, dense = self.parts(i)
+        o.trimul_rows(self.qkv, ts.B, ts.T, ts.C, ts.NH, bht)
+        for xb, wb, M, I, H, rows in dense:
             if rows.size:
                 o.dense_rows(xb, wb, M, I, H, rows)
-                flops += 2 * int(rows.size) * I * H
-        return flops
+        return self.flops(i)
 
 
 ORACLE_SAMPLES = ("step", "step_gpt2")

@@ -67,3 +67,21 @@ def test_step_time_percentiles_match_numpy():
         xs = rng.uniform(0.05, 0.09, size=n).tolist()
         for q in (10, 50, 90):
             assert abs(bench._percentile(xs, q) - float(np.percentile(xs, q))) < 1e-12
+
+
+def test_oracle_samples_cover_one_step():
+    """The default step's CPU baseline samples are 1/32 of a step each: 32 consecutive
+    samples compute every head of the long-context scores once and every row of the 33
+    dense problems once, i.e. exactly one step's useful flops."""
+    from causal_attention_score_gb300 import synth
+    sample = bench.OracleSample("step")
+    tl = synth.TRIMUL_LONG
+    xs, W = synth.dense_sweep_inputs(seed=0)
+    H, I = W.shape
+    step = (bench.trimul_flops(tl.B, tl.T, tl.C, tl.NH)
+            + sum(bench.dense_flops(X.shape[0], I, H) for X in xs)
+            + bench.dense_flops(synth.DENSE_RAGGED.M, synth.DENSE_RAGGED.I, synth.DENSE_RAGGED.H))
+    assert step == 226_755_411_968
+    assert sum(sample.flops(i) for i in range(32)) == step
+    heads = {tuple(sample.parts(i)[0][0, :2]) for i in range(32)}
+    assert len(heads) == tl.B * tl.NH
