@@ -45,6 +45,9 @@ SIGNATURES = {
     "dense_xwt_workspace_size": (_i, [_vp, _vp, _i, _i, _i, ctypes.POINTER(ctypes.c_size_t)]),
     "dense_xwt_ws": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, ctypes.c_size_t, _vp]),
     "dense_xwt_grouped": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp]),
+    "dense_xwt_grouped_workspace_size": (_i, [_vp, _vp, _vp, _i, _i, _i,
+                                              ctypes.POINTER(ctypes.c_size_t)]),
+    "dense_xwt_grouped_ws": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp, ctypes.c_size_t, _vp]),
     "csa_get_status": (_i, [_vp]),
     "csa_status_string": (ctypes.c_char_p, [_i]),
     "csa_last_error": (ctypes.c_char_p, []),

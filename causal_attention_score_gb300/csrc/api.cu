@@ -545,31 +545,72 @@ csa_status dense_xwt(float* Y, const void* X, const void* W, int M, int I, int H
   return dense_xwt_ex(Y, X, W, M, I, H, nullptr);
 }
 
-csa_status dense_xwt_grouped(float* const* Y, const void* const* X, const void* W, const int* M,
-                             int n, int I, int H, void* stream) {
-  t_last_error.clear();
-  if (!Y || !X || !W || !M) return set_error(CSA_ERR_NULL, "dense_xwt_grouped: null pointer");
+// Checks shared by the grouped dense entry points; CSA_OK or the status to return.
+static int grouped_args_ok(const char* who, float* const* Y, const void* const* X, const void* W,
+                           const int* M, int n, int I, int H) {
+  if (!Y || !X || !W || !M) return set_error(CSA_ERR_NULL, std::string(who) + ": null pointer");
   if (n <= 0 || I <= 0 || H <= 0)
-    return set_error(CSA_ERR_SHAPE, "dense_xwt_grouped: n, I, H must be >= 1");
+    return set_error(CSA_ERR_SHAPE, std::string(who) + ": n, I, H must be >= 1");
   if (reinterpret_cast<uintptr_t>(W) % 2)
-    return set_error(CSA_ERR_ALIGN, "dense_xwt_grouped: W needs 2-byte alignment");
+    return set_error(CSA_ERR_ALIGN, std::string(who) + ": W needs 2-byte alignment");
   for (int g = 0; g < n; ++g) {
     if (!Y[g] || !X[g])
-      return set_error(CSA_ERR_NULL, "dense_xwt_grouped: null pointer in problem " +
+      return set_error(CSA_ERR_NULL, std::string(who) + ": null pointer in problem " +
                                          std::to_string(g));
     if (M[g] <= 0)
-      return set_error(CSA_ERR_SHAPE, "dense_xwt_grouped: M[" + std::to_string(g) +
+      return set_error(CSA_ERR_SHAPE, std::string(who) + ": M[" + std::to_string(g) +
                                           "] must be >= 1");
     if (reinterpret_cast<uintptr_t>(X[g]) % 2 || reinterpret_cast<uintptr_t>(Y[g]) % 4)
-      return set_error(CSA_ERR_ALIGN, "dense_xwt_grouped: X[" + std::to_string(g) +
+      return set_error(CSA_ERR_ALIGN, std::string(who) + ": X[" + std::to_string(g) +
                                           "] needs 2-byte and Y 4-byte alignment");
+  }
+  return CSA_OK;
+}
+
+csa_status dense_xwt_grouped_ws(float* const* Y, const void* const* X, const void* W,
+                                const int* M, int n, int I, int H, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  t_last_error.clear();
+  int rc = grouped_args_ok("dense_xwt_grouped", Y, X, W, M, n, I, H);
+  if (rc != CSA_OK) return rc;
+  if (workspace) {
+    const size_t need = dense_grouped_workspace_bytes(X, W, M, n, I, H);
+    if (workspace_bytes < need)
+      return set_error(CSA_ERR_WORKSPACE, "dense_xwt_grouped_ws: " + std::to_string(need) +
+                                              " bytes of workspace needed, " +
+                                              std::to_string(workspace_bytes) + " given");
+    if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
+      return set_error(CSA_ERR_ALIGN, "dense_xwt_grouped_ws: workspace must be 16-byte aligned");
   }
   DeviceInfo dev;
   std::string err;
-  int rc = current_device(dev, err);
+  rc = current_device(dev, err);
   if (rc != CSA_OK) return set_error(rc, err);
-  rc = dense_grouped_launch(Y, X, W, M, n, I, H, static_cast<cudaStream_t>(stream), dev, err);
+  rc = dense_grouped_launch(Y, X, W, M, n, I, H, workspace, workspace_bytes,
+                            static_cast<cudaStream_t>(stream), dev, err);
   if (rc != CSA_OK) return set_error(rc, err);
+  return CSA_OK;
+}
+
+csa_status dense_xwt_grouped(float* const* Y, const void* const* X, const void* W, const int* M,
+                             int n, int I, int H, void* stream) {
+  return dense_xwt_grouped_ws(Y, X, W, M, n, I, H, nullptr, 0, stream);
+}
+
+csa_status dense_xwt_grouped_workspace_size(const void* const* X, const void* W, const int* M,
+                                            int n, int I, int H, size_t* bytes) {
+  t_last_error.clear();
+  if (!bytes) return set_error(CSA_ERR_NULL, "dense_xwt_grouped_workspace_size: null pointer");
+  *bytes = 0;
+  if (!X || !W || !M) return set_error(CSA_ERR_NULL, "dense_xwt_grouped_workspace_size: null pointer");
+  if (n <= 0 || I <= 0 || H <= 0)
+    return set_error(CSA_ERR_SHAPE, "dense_xwt_grouped_workspace_size: n, I, H must be >= 1");
+  for (int g = 0; g < n; ++g) {
+    if (!X[g]) return set_error(CSA_ERR_NULL, "dense_xwt_grouped_workspace_size: null pointer");
+    if (M[g] <= 0)
+      return set_error(CSA_ERR_SHAPE, "dense_xwt_grouped_workspace_size: M[g] must be >= 1");
+  }
+  *bytes = dense_grouped_workspace_bytes(X, W, M, n, I, H);
   return CSA_OK;
 }
 

@@ -145,8 +145,13 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H, vo
 // Workspace bytes dense_launch needs to realign X and W (0 when their rows need none).
 size_t dense_workspace_bytes(const void* X, const void* W, int M, int I, int H);
 
+// Dense layers sharing W. Rows no tensor map can describe are first copied into
+// `workspace` (at least dense_grouped_workspace_bytes), or each problem runs as its
+// own loader-warp dense_launch when workspace is nullptr.
 int dense_grouped_launch(float* const* Y, const void* const* X, const void* W, const int* M, int n,
-                         int I, int H, cudaStream_t stream, const DeviceInfo& dev,
-                         std::string& err);
+                         int I, int H, void* workspace, size_t ws_bytes, cudaStream_t stream,
+                         const DeviceInfo& dev, std::string& err);
+size_t dense_grouped_workspace_bytes(const void* const* X, const void* W, const int* M, int n,
+                                     int I, int H);
 
 }  // namespace csa

@@ -586,6 +586,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 // aligned) and are read as bf16 pairs, else one element at a time.
 constexpr int kRealignThreads = 256;
 
+// One row of I bf16 values copied by one warp into a row of pitch P (zeros in
+// columns I..P-1), one 16-byte destination chunk per lane and step, four
+// steps' loads issued before their stores.
+__device__ __forceinline__ void realign_row(const uint16_t* __restrict__ src,
+                                            uint16_t* __restrict__ dst, int I, int P, int pairs,
+                                            int lane) {
+  const int chunks = P / 8;
+  for (int c0 = lane; c0 < chunks; c0 += 4 * 32) {
+    uint32_t w[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int k = (c0 + 32 * u) * 8;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int e = k + 2 * j;
+        if (pairs) {
+          w[u][j] = e < I ? __ldg(reinterpret_cast<const unsigned int*>(src + e)) : 0u;
+        } else {
+          const uint32_t lo = e < I ? __ldg(reinterpret_cast<const unsigned short*>(src + e)) : 0u;
+          const uint32_t hi =
+              e + 1 < I ? __ldg(reinterpret_cast<const unsigned short*>(src + e + 1)) : 0u;
+          w[u][j] = lo | (hi << 16);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + 32 * u;
+      if (c < chunks)
+        *reinterpret_cast<uint4*>(dst + c * 8) = make_uint4(w[u][0], w[u][1], w[u][2], w[u][3]);
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kRealignThreads)
     realign_rows_kernel(const uint16_t* __restrict__ X, const uint16_t* __restrict__ W,
                         uint16_t* __restrict__ Xp, uint16_t* __restrict__ Wp, int M, int H, int I,
@@ -595,38 +629,41 @@ __global__ void __launch_bounds__(kRealignThreads)
   const long long rows = static_cast<long long>(M) + H;
   const int lane = static_cast<int>(threadIdx.x & 31u);
   const long long warps_per_grid = static_cast<long long>(gridDim.x) * (kRealignThreads / 32);
-  const int chunks = P / 8;
   for (long long r = static_cast<long long>(blockIdx.x) * (kRealignThreads / 32) +
                      (threadIdx.x >> 5);
        r < rows; r += warps_per_grid) {
     const bool is_x = r < M;
     const uint16_t* src = is_x ? X + r * I : W + (r - M) * I;
     uint16_t* dst = is_x ? Xp + r * P : Wp + (r - M) * P;
-    for (int c0 = lane; c0 < chunks; c0 += 4 * 32) {
-      uint32_t w[4][4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int k = (c0 + 32 * u) * 8;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int e = k + 2 * j;
-          if (pairs) {
-            w[u][j] = e < I ? __ldg(reinterpret_cast<const unsigned int*>(src + e)) : 0u;
-          } else {
-            const uint32_t lo = e < I ? __ldg(reinterpret_cast<const unsigned short*>(src + e)) : 0u;
-            const uint32_t hi =
-                e + 1 < I ? __ldg(reinterpret_cast<const unsigned short*>(src + e + 1)) : 0u;
-            w[u][j] = lo | (hi << 16);
-          }
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int c = c0 + 32 * u;
-        if (c < chunks)
-          *reinterpret_cast<uint4*>(dst + c * 8) = make_uint4(w[u][0], w[u][1], w[u][2], w[u][3]);
-      }
+    realign_row(src, dst, I, P, pairs, lane);
+  }
+}
+
+// The same copy for the operands of a grouped call: up to kMaxGroup + 1 row
+// ranges (W's rows and each X[g]'s), copied by one launch.
+struct RealignSegments {
+  const uint16_t* src[kMaxGroup + 1];
+  uint16_t* dst[kMaxGroup + 1];
+  long long first[kMaxGroup + 2];  // first row of range s in the launch's row list; [n] = all
+  int n, I, P, pairs;
+};
+
+__global__ void __launch_bounds__(kRealignThreads)
+    realign_segments_kernel(const __grid_constant__ RealignSegments g) {
+  grid_dependency_wait();
+  const int lane = static_cast<int>(threadIdx.x & 31u);
+  const long long warps_per_grid = static_cast<long long>(gridDim.x) * (kRealignThreads / 32);
+  for (long long r = static_cast<long long>(blockIdx.x) * (kRealignThreads / 32) +
+                     (threadIdx.x >> 5);
+       r < g.first[g.n]; r += warps_per_grid) {
+    int lo = 0, hi = g.n - 1;  // the last range whose first row is <= r
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (g.first[mid] <= r) lo = mid;
+      else hi = mid - 1;
     }
+    const long long row = r - g.first[lo];
+    realign_row(g.src[lo] + row * g.I, g.dst[lo] + row * g.P, g.I, g.P, g.pairs, lane);
   }
 }
 
@@ -815,27 +852,92 @@ namespace csa {
 // Y[g] = X[g] W^T for g < n: launches of up to kMaxGroup problems each when the
 // rows of every X[g] and of W can be described by tensor maps (I * 2 % 16 == 0,
 // 16-byte aligned), else one dense_launch per problem.
+namespace {
+
+bool group_rows_describable(const void* const* X, const void* W, int n, int I) {
+  bool ok = (static_cast<long long>(I) * 2) % 16 == 0 && reinterpret_cast<uintptr_t>(W) % 16 == 0;
+  for (int i = 0; ok && i < n; ++i) ok = reinterpret_cast<uintptr_t>(X[i]) % 16 == 0;
+  return ok;
+}
+
+}  // namespace
+
+size_t dense_grouped_workspace_bytes(const void* const* X, const void* W, const int* M, int n,
+                                     int I, int H) {
+  if (group_rows_describable(X, W, n, I)) return 0;
+  const size_t P = (static_cast<size_t>(I) + 7) / 8 * 8;
+  size_t b = 256 + round256(static_cast<size_t>(H) * P * 2);
+  for (int i = 0; i < n; ++i) b += round256(static_cast<size_t>(M[i]) * P * 2);
+  return b;
+}
+
 int dense_grouped_launch(float* const* Y, const void* const* X, const void* W, const int* M, int n,
-                         int I, int H, cudaStream_t stream, const DeviceInfo& dev,
-                         std::string& err) {
-  bool tma_rows = (static_cast<long long>(I) * 2) % 16 == 0 &&
-                  reinterpret_cast<uintptr_t>(W) % 16 == 0;
+                         int I, int H, void* workspace, size_t ws_bytes, cudaStream_t stream,
+                         const DeviceInfo& dev, std::string& err) {
+  const bool tma_rows = group_rows_describable(X, W, n, I);
   bool tma_store = (static_cast<long long>(H) * 4) % 16 == 0;
-  for (int i = 0; i < n; ++i) {
-    tma_rows = tma_rows && reinterpret_cast<uintptr_t>(X[i]) % 16 == 0;
-    tma_store = tma_store && reinterpret_cast<uintptr_t>(Y[i]) % 16 == 0;
-  }
-  if (!tma_rows) {
+  for (int i = 0; i < n; ++i) tma_store = tma_store && reinterpret_cast<uintptr_t>(Y[i]) % 16 == 0;
+  const bool realign = !tma_rows && workspace && dense_fetch_mode() == CSA_DENSE_FETCH_AUTO;
+  if (!tma_rows && !realign) {
+    // No workspace (or the loader-warp fetch asked for): one dense_xwt per problem.
     for (int i = 0; i < n; ++i) {
       const int rc = dense_launch(Y[i], X[i], W, M[i], I, H, nullptr, 0, stream, dev, err);
       if (rc != CSA_OK) return rc;
     }
     return CSA_OK;
   }
+  // Rows no tensor map can describe: W's and every X[g]'s rows are copied into the
+  // workspace (W first, then the problems in order) as 16-byte-aligned rows of
+  // pitch P, by one copy launch per group of problems, then read from there.
+  long long pitch = I;
+  const void* w_src = W;
+  uint8_t* x_next = nullptr;
+  int pairs = 0;
+  if (realign) {
+    const size_t need = dense_grouped_workspace_bytes(X, W, M, n, I, H);
+    if (ws_bytes < need) {
+      err = "dense_xwt_grouped_ws: " + std::to_string(need) + " bytes of workspace needed, " +
+            std::to_string(ws_bytes) + " given";
+      return CSA_ERR_WORKSPACE;
+    }
+    pitch = (static_cast<long long>(I) + 7) / 8 * 8;
+    uint8_t* p = static_cast<uint8_t*>(workspace);
+    p += (256 - reinterpret_cast<uintptr_t>(p) % 256) % 256;
+    w_src = p;
+    x_next = p + round256(static_cast<size_t>(H) * pitch * 2);
+    pairs = I % 2 == 0 && reinterpret_cast<uintptr_t>(W) % 4 == 0;
+    for (int i = 0; i < n; ++i) pairs = pairs && reinterpret_cast<uintptr_t>(X[i]) % 4 == 0;
+  }
   CUtensorMap map_w;  // W's box depends on BN, chosen per launch below
   static thread_local DenseGroup<true> grp;  // 13 KB: kept off the stack
+  static thread_local RealignSegments seg;
+  const void* x_src[kMaxGroup];
   for (int first = 0; first < n; first += kMaxGroup) {
     const int cnt = std::min(kMaxGroup, n - first);
+    if (realign) {
+      std::memset(&seg, 0, sizeof seg);
+      seg.I = I;
+      seg.P = static_cast<int>(pitch);
+      seg.pairs = pairs;
+      long long rows = 0;
+      if (first == 0) {
+        seg.src[seg.n] = static_cast<const uint16_t*>(W);
+        seg.dst[seg.n] = static_cast<uint16_t*>(const_cast<void*>(w_src));
+        seg.first[seg.n++] = rows;
+        rows += H;
+      }
+      for (int i = 0; i < cnt; ++i) {
+        x_src[i] = x_next;
+        seg.src[seg.n] = static_cast<const uint16_t*>(X[first + i]);
+        seg.dst[seg.n] = reinterpret_cast<uint16_t*>(x_next);
+        seg.first[seg.n++] = rows;
+        rows += M[first + i];
+        x_next += round256(static_cast<size_t>(M[first + i]) * pitch * 2);
+      }
+      seg.first[seg.n] = rows;
+    } else {
+      for (int i = 0; i < cnt; ++i) x_src[i] = X[first + i];
+    }
     std::memset(&grp, 0, sizeof grp);
     grp.n = cnt;
     long long total = 0;
@@ -919,17 +1021,17 @@ int dense_grouped_launch(float* const* Y, const void* const* X, const void* W, c
       }
     }
 
-    const uint64_t st_in[1] = {static_cast<uint64_t>(I) * 2};
+    const uint64_t st_in[1] = {static_cast<uint64_t>(pitch) * 2};
     const uint32_t bx[2] = {kBK, kBM};
     // With pairs, each CTA loads (and multicasts) half of the W tile's rows.
     const uint32_t bw[2] = {kBK, static_cast<uint32_t>(pair ? a.BN / 2 : a.BN)};
     const uint64_t dw[2] = {static_cast<uint64_t>(I), static_cast<uint64_t>(H)};
-    rc = encode_tiled(&map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, dw, st_in, bw,
+    rc = encode_tiled(&map_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_src, dw, st_in, bw,
                       CU_TENSOR_MAP_SWIZZLE_128B, err);
     if (rc != CSA_OK) return rc;
     for (int i = 0; i < cnt; ++i) {
       const uint64_t dx[2] = {static_cast<uint64_t>(I), static_cast<uint64_t>(grp.M[i])};
-      rc = encode_tiled(&grp.x[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X[first + i], dx, st_in,
+      rc = encode_tiled(&grp.x[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x_src[i], dx, st_in,
                         bx, CU_TENSOR_MAP_SWIZZLE_128B, err);
       if (rc != CSA_OK) return rc;
       if (a.tma_store) {
@@ -950,6 +1052,19 @@ int dense_grouped_launch(float* const* Y, const void* const* X, const void* W, c
     CUtensorMap unused;
     std::memset(&unused, 0, sizeof unused);
     cudaError_t e;
+    if (realign) {
+      // The copy, launched last of all the checks so that a failing call launches nothing.
+      const long long rows = seg.first[seg.n];
+      const long long blocks = std::min<long long>(
+          (rows + kRealignThreads / 32 - 1) / (kRealignThreads / 32), 16LL * dev.sm_count);
+      e = launch_programmatic(realign_segments_kernel, static_cast<unsigned>(blocks),
+                              kRealignThreads, 0, stream, seg);
+      if (e == cudaSuccess) e = cudaGetLastError();
+      if (e != cudaSuccess) {
+        err = std::string("dense_xwt_grouped: launch: ") + cudaGetErrorString(e);
+        return CSA_ERR_LAUNCH;
+      }
+    }
     if (pair) {
       const long long grid = 2 * std::min<long long>(a.num_tiles, clusters);
       e = launch_programmatic_cluster(kernel_pair, static_cast<unsigned>(grid), kThreads, smem,

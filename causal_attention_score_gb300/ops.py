@@ -132,6 +132,11 @@ class DenseGroupedPlan:
     one C call plus a check that every tensor still has the storage it was planned
     with, instead of the full per-tensor checks (which take longer than the launch
     itself for a few dozen problems). The plan keeps references to its tensors.
+
+    When no tensor map can describe the rows (I * 2 not a multiple of 16, or a
+    misaligned view), the plan also holds the workspace dense_xwt_grouped_ws copies
+    them into (torch memory, allocated once with the plan), so the batch still runs as
+    one grouped launch; calls of one plan must then not overlap on the GPU.
     """
 
     def __init__(self, Ys, Xs, W: torch.Tensor, I: int, H: int):
@@ -155,12 +160,20 @@ class DenseGroupedPlan:
         self._m = (ctypes.c_int * n)(*Ms)
         self._args = (ctypes.addressof(self._y), ctypes.addressof(self._x), W.data_ptr(),
                       ctypes.addressof(self._m), n, I, H)
+        nbytes = ctypes.c_size_t(0)
+        _lib.check(_lib.load().dense_xwt_grouped_workspace_size(
+            ctypes.addressof(self._x), W.data_ptr(), ctypes.addressof(self._m), n, I, H,
+            ctypes.byref(nbytes)), "dense_xwt_grouped_workspace_size")
+        self._ws = (torch.empty(nbytes.value, dtype=torch.uint8, device=W.device)
+                    if nbytes.value else None)
+        self._ws_args = ((self._ws.data_ptr(), nbytes.value) if self._ws is not None
+                         else (None, 0))
 
     def __call__(self, stream=None) -> None:
         if [t.data_ptr() for t in self._tensors] != self._ptrs:
             raise ValueError("a tensor of this DenseGroupedPlan no longer has the storage it "
                              "was planned with; make a new plan")
-        rc = _lib.load().dense_xwt_grouped(*self._args, _stream_ptr(stream))
+        rc = _lib.load().dense_xwt_grouped_ws(*self._args, *self._ws_args, _stream_ptr(stream))
         _lib.check(rc, "dense_xwt_grouped")
 
 

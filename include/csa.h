@@ -245,13 +245,37 @@ csa_status dense_xwt_ws(float* Y, const void* X, const void* W, int M, int I, in
  *   M  host array of n row counts, each >= 1.
  * The host arrays are read during the call only. Results are bit-identical to n
  * dense_xwt calls. When I * 2 is not a multiple of 16, or W or some X[g] is not
- * 16-byte aligned, the call makes n dense_xwt launches instead. Alignment: X[g]
+ * 16-byte aligned, this call (no workspace) makes n dense_xwt launches instead;
+ * dense_xwt_grouped_ws keeps such a batch in one grouped launch. Alignment: X[g]
  * and W 2-byte, Y[g] 4-byte (Y written by TMA when H * 4 % 16 == 0 and every Y[g]
  * is 16-byte aligned). CSA_ERR_NULL / CSA_ERR_SHAPE / CSA_ERR_ALIGN name the first
  * offending problem; nothing is launched then.
  */
 csa_status dense_xwt_grouped(float* const* Y, const void* const* X, const void* W, const int* M,
                              int n, int I, int H, void* stream);
+
+/*
+ * dense_xwt_grouped_workspace_size -- bytes of device workspace
+ * dense_xwt_grouped_ws needs for these operands, written to *bytes: 0 when
+ * tensor maps describe the rows of W and of every X[g] as they are, else
+ * 256 + ceil256(H*P*2) + sum_g ceil256(M[g]*P*2), P = I rounded up to 8.
+ * CSA_ERR_NULL / CSA_ERR_SHAPE (then *bytes = 0).
+ *
+ * dense_xwt_grouped_ws -- dense_xwt_grouped with caller-owned scratch. Where no
+ * tensor map can describe the rows (e.g. I = 770), one copy launch per 48
+ * problems writes W's and the X[g]'s rows into `workspace` as 16-byte-aligned
+ * rows (W once, then the problems in order), and the grouped launch reads them
+ * from there, instead of one loader-warp dense_xwt per problem. Same bits as n
+ * dense_xwt calls. workspace NULL is dense_xwt_grouped itself; otherwise it
+ * must be 16-byte aligned and at least the size above (else CSA_ERR_ALIGN /
+ * CSA_ERR_WORKSPACE, nothing launched). It is in use until the call's kernels
+ * complete on `stream`. Nothing is allocated.
+ */
+csa_status dense_xwt_grouped_workspace_size(const void* const* X, const void* W, const int* M,
+                                            int n, int I, int H, size_t* bytes);
+csa_status dense_xwt_grouped_ws(float* const* Y, const void* const* X, const void* W,
+                                const int* M, int n, int I, int H, void* workspace,
+                                size_t workspace_bytes, void* stream);
 
 /*
  * csa_set_dense_fetch -- process-wide fetch mode of dense_xwt_ws for rows that

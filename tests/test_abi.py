@@ -294,3 +294,23 @@ def test_library_is_stamped_with_its_sources(tmp_path, monkeypatch):
     monkeypatch.setattr(build_lib, "_deps", lambda: deps + [str(extra)])
     assert not build_lib.up_to_date(path)
     assert build_lib.source_hash() != build_lib.source_hash(debug=True)
+
+
+def test_dense_grouped_workspace_size_and_errors(lib):
+    P = (770 + 7) // 8 * 8
+    r256 = lambda n: (n + 255) // 256 * 256
+    n = ctypes.c_size_t(5)
+    xs = (ctypes.c_void_p * 3)(4096, 8192, 16384)
+    ms = (ctypes.c_int * 3)(10, 300, 1)
+    ys = (ctypes.c_void_p * 3)(1 << 20, 1 << 21, 1 << 22)
+    assert lib.dense_xwt_grouped_workspace_size(xs, 4096, ms, 3, 768, 64, ctypes.byref(n)) == 0
+    assert n.value == 0
+    assert lib.dense_xwt_grouped_workspace_size(xs, 4096, ms, 3, 770, 64, ctypes.byref(n)) == 0
+    assert n.value == 256 + r256(64 * P * 2) + sum(r256(m * P * 2) for m in (10, 300, 1))
+    assert lib.dense_xwt_grouped_workspace_size(xs, 4096, ms, 0, 770, 64, ctypes.byref(n)) == \
+        _lib.CSA_ERR_SHAPE
+    assert lib.dense_xwt_grouped_ws(ys, xs, 4096, ms, 3, 770, 64, 1 << 24, 10, None) == \
+        _lib.CSA_ERR_WORKSPACE
+    need = 256 + r256(64 * P * 2) + sum(r256(m * P * 2) for m in (10, 300, 1))
+    assert lib.dense_xwt_grouped_ws(ys, xs, 4096, ms, 3, 770, 64, (1 << 24) + 8, need, None) == \
+        _lib.CSA_ERR_ALIGN

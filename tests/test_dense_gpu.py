@@ -406,3 +406,56 @@ def test_dense_grouped_plan_repeats_and_notices_new_storage():
     Yp[2].set_(torch.empty_like(Yp[2]))  # the tensor now points at other memory
     with pytest.raises(ValueError):
         plan()
+
+
+@pytest.mark.parametrize("I,H,offset", [(770, 768, 0), (771, 200, 0), (768, 300, 1)])
+def test_dense_grouped_realigned_rows(oracle_lib, I, H, offset):
+    """A grouped call whose rows no tensor map can describe (I = 770 and 771, or views
+    starting 2 bytes into their storage) runs as one copy into the plan's workspace and
+    one grouped launch: the same bits as one dense_xwt per problem, and the oracle's
+    values on sampled rows."""
+    Ms = [45, 300, 17, 128, 1000, 3]
+    rng = np.random.default_rng(I + H)
+    Wb = synth.dense_input(synth.DenseShape(M=1, I=I + offset, H=H), seed=5)[1]
+    Wd = Wb.reshape(-1).cuda()[offset:offset + H * I].reshape(H, I)
+    W = Wb.reshape(-1)[offset:offset + H * I].reshape(H, I).contiguous()
+    Xs, Xd = [], []
+    for k, M in enumerate(Ms):
+        Xb = synth.dense_input(synth.DenseShape(M=M, I=I + offset, H=1), seed=40 + k)[0]
+        Xs.append(Xb.reshape(-1)[offset:offset + M * I].reshape(M, I).contiguous())
+        Xd.append(Xb.reshape(-1).cuda()[offset:offset + M * I].reshape(M, I))
+    Yg = [poisoned((M, H)) for M in Ms]
+    plan = csa.DenseGroupedPlan(Yg, Xd, Wd, I, H)
+    assert plan._ws is not None
+    for _ in range(2):
+        plan()
+    Ys = [poisoned((M, H)) for M in Ms]
+    for Y, X in zip(Ys, Xd):
+        csa.dense_xwt(Y, X, Wd, X.shape[0], I, H)
+    torch.cuda.synchronize()
+    assert csa.get_status() == 0
+    wbits = synth.bf16_bits(W).reshape(-1)
+    for g, (a, b, X) in enumerate(zip(Yg, Ys, Xs)):
+        assert np.array_equal(f32_bits(a), f32_bits(b)), f"problem {g}"
+        M = X.shape[0]
+        rows = np.unique(np.concatenate([[0, M - 1], rng.integers(0, M, size=4)]))
+        ref = oracle_lib.dense_rows(synth.bf16_bits(X).reshape(-1), wbits, M, I, H, rows)
+        assert_close(a[torch.from_numpy(rows).cuda()].cpu().numpy(), ref, f"problem {g}")
+
+
+def test_dense_grouped_realigned_more_than_one_launch():
+    """50 problems with I = 770: two copy + grouped launches (48 + 2), W copied once."""
+    I, H = 770, 136
+    Ms = [16 * (1 + (7 * k) % 23) for k in range(50)]
+    W = synth.dense_input(synth.DenseShape(M=1, I=I, H=H), seed=9)[1].cuda()
+    Xd = [synth.dense_input(synth.DenseShape(M=M, I=I, H=1), seed=200 + k)[0].cuda()
+          for k, M in enumerate(Ms)]
+    Yg = [poisoned((M, H)) for M in Ms]
+    csa.dense_xwt_grouped(Yg, Xd, W, I, H)
+    Ys = [poisoned((M, H)) for M in Ms]
+    for Y, X in zip(Ys, Xd):
+        csa.dense_xwt(Y, X, W, X.shape[0], I, H)
+    torch.cuda.synchronize()
+    assert csa.get_status() == 0
+    for g, (a, b) in enumerate(zip(Yg, Ys)):
+        assert np.array_equal(f32_bits(a), f32_bits(b)), f"problem {g}"
