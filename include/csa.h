@@ -207,8 +207,8 @@ csa_status dense_xwt_ex(float* Y, const void* X, const void* W, int M, int I, in
  * dense_xwt_workspace_size -- bytes of device workspace dense_xwt_ws needs for
  * these operands, written to *bytes: 0 when tensor maps describe the rows of X
  * and W as they are (I*2 % 16 == 0, both 16-byte aligned), else
- * 256 + ceil256(M*P*2) + H*P*2 with P = I rounded up to a multiple of 8 (a
- * copy of X and W whose rows start on 16-byte boundaries, and alignment
+ * 256 + ceil256(M*P*2) + H*P*2 with P = I rounded up to a multiple of 64 (a
+ * copy of X and W whose rows start on 128-byte boundaries, and alignment
  * slack). Depends on the pointers' alignment and the sizes only.
  * CSA_ERR_NULL / CSA_ERR_SHAPE as dense_xwt (then *bytes = 0).
  */
@@ -218,7 +218,7 @@ csa_status dense_xwt_workspace_size(const void* X, const void* W, int M, int I, 
 /*
  * dense_xwt_ws -- dense_xwt with caller-owned scratch, on `stream`. Where no
  * tensor map can describe the rows of X and W, a first kernel copies them into
- * `workspace` as rows of pitch P (16-byte multiples) and the product kernel
+ * `workspace` as rows of pitch P (128-byte multiples) and the product kernel
  * fetches every tile from that copy by TMA, with zero fill past M, H and I --
  * the local padding of "DietCode tests/codegen/test_1_local_padding.py"
  * (bounds handled only where data is fetched and written back).
@@ -258,12 +258,12 @@ csa_status dense_xwt_grouped(float* const* Y, const void* const* X, const void* 
  * dense_xwt_grouped_workspace_size -- bytes of device workspace
  * dense_xwt_grouped_ws needs for these operands, written to *bytes: 0 when
  * tensor maps describe the rows of W and of every X[g] as they are, else
- * 256 + ceil256(H*P*2) + sum_g ceil256(M[g]*P*2), P = I rounded up to 8.
+ * 256 + ceil256(H*P*2) + sum_g ceil256(M[g]*P*2), P = I rounded up to 64.
  * CSA_ERR_NULL / CSA_ERR_SHAPE (then *bytes = 0).
  *
  * dense_xwt_grouped_ws -- dense_xwt_grouped with caller-owned scratch. Where no
  * tensor map can describe the rows (e.g. I = 770), one copy launch per 48
- * problems writes W's and the X[g]'s rows into `workspace` as 16-byte-aligned
+ * problems writes W's and the X[g]'s rows into `workspace` as 128-byte-aligned
  * rows (W once, then the problems in order), and the grouped launch reads them
  * from there, instead of one loader-warp dense_xwt per problem. Same bits as n
  * dense_xwt calls. workspace NULL is dense_xwt_grouped itself; otherwise it

@@ -243,16 +243,16 @@ def _ws_bytes(lib, X, W, M, I, H):
 
 def test_dense_workspace_size(lib):
     """No workspace when tensor maps describe the rows as they are; otherwise the
-    realigned copy (rows padded to 8 elements, X's part 256-byte rounded) and 256
+    realigned copy (rows padded to 64 elements, X's part 256-byte rounded) and 256
     bytes of alignment slack."""
-    P = (770 + 7) // 8 * 8
+    P = (770 + 63) // 64 * 64
     r256 = lambda n: (n + 255) // 256 * 256
     assert _ws_bytes(lib, 4096, 8192, 960, 768, 768) == (0, 0)
     assert _ws_bytes(lib, 4096, 8192, 960, 770, 768) == (
         0, 256 + r256(960 * P * 2) + 768 * P * 2)
     # a misaligned view needs the copy even when I * 2 is a multiple of 16
     rc, n = _ws_bytes(lib, 4098, 8192, 10, 768, 20)
-    assert rc == 0 and n == 256 + r256(10 * 768 * 2) + 20 * 768 * 2
+    assert rc == 0 and n == 256 + r256(10 * 768 * 2) + 20 * 768 * 2  # 768 is a multiple of 64
     assert _ws_bytes(lib, None, 8192, 1, 1, 1)[0] == _lib.CSA_ERR_NULL
     assert _ws_bytes(lib, 16, 16, 0, 1, 1) == (_lib.CSA_ERR_SHAPE, 0)
     assert lib.dense_xwt_workspace_size(16, 16, 1, 1, 1, None) == _lib.CSA_ERR_NULL
@@ -297,7 +297,7 @@ def test_library_is_stamped_with_its_sources(tmp_path, monkeypatch):
 
 
 def test_dense_grouped_workspace_size_and_errors(lib):
-    P = (770 + 7) // 8 * 8
+    P = (770 + 63) // 64 * 64
     r256 = lambda n: (n + 255) // 256 * 256
     n = ctypes.c_size_t(5)
     xs = (ctypes.c_void_p * 3)(4096, 8192, 16384)
