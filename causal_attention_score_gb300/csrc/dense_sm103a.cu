@@ -8,7 +8,7 @@
 // then runs over whole tiles with no predicates at all.
 //
 // Design (one persistent launch, one CTA per SM, 9 warps):
-//  - tiles of 128 x BN outputs (BN = 64, 128 or 256, chosen per shape),
+//  - tiles of 128 x BN outputs (BN = 64, 128, 192 or 256, chosen per shape),
 //    K in blocks of 64; tiles are dealt round-robin to CTAs.
 //  - dense_xwt_grouped: up to 48 problems sharing W in one launch (their tensor
 //    maps in the kernel parameters, m-tiles of all problems in one list); when
@@ -673,7 +673,7 @@ __global__ void __launch_bounds__(kRealignThreads)
 int choose_bn_tiles(long long m_tiles, int H, int sms) {
   int best = 64;
   long long best_cost = -1;
-  for (int bn : {256, 128, 64}) {
+  for (int bn : {256, 192, 128, 64}) {
     const long long tiles = m_tiles * ((H + bn - 1) / bn);
     const long long waves = (tiles + sms - 1) / sms;
     const long long cost = waves * (bn + 32);
@@ -686,6 +686,13 @@ int choose_bn_tiles(long long m_tiles, int H, int sms) {
 }
 
 int choose_bn(int M, int H, int sms) { return choose_bn_tiles((M + kBM - 1) / kBM, H, sms); }
+
+// TMEM columns for two BN-wide accumulators: an allocation is a power of two >= 32.
+uint32_t tmem_cols_for(int BN) {
+  uint32_t c = 32u;
+  while (c < static_cast<uint32_t>(2 * BN)) c *= 2u;
+  return c;
+}
 
 // Shared-memory plan: ring stages of 128 rows of X and b_rows rows of W (BN, or
 // BN / 2 for a CTA pair), then staging, barriers and misc.
@@ -782,7 +789,7 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H, vo
   a.status = dev.status_word;
   a.wait_limit_ns = wait_limit_ns();
   a.inject = take_inject() ? 1 : 0;
-  a.tmem_cols = static_cast<uint32_t>(2 * a.BN);
+  a.tmem_cols = tmem_cols_for(a.BN);
 
   size_t smem = 0;
   {
@@ -981,7 +988,7 @@ int dense_grouped_launch(float* const* Y, const void* const* X, const void* W, c
     a.status = dev.status_word;
     a.wait_limit_ns = wait_limit_ns();
     a.inject = take_inject() ? 1 : 0;
-    a.tmem_cols = static_cast<uint32_t>(2 * a.BN);
+    a.tmem_cols = tmem_cols_for(a.BN);
     size_t smem = 0;
     int rc = plan_smem(a, dev, err, smem, pair ? a.BN / 2 : a.BN);
     if (rc != CSA_OK) return rc;
