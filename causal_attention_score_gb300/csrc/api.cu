@@ -59,6 +59,17 @@ int current_device(DeviceInfo& info, std::string& err) {
     err = "device ordinal out of range";
     return CSA_ERR_CUDA;
   }
+  // cudaGetDevice binds no context, and the tensor-map encoder is a driver
+  // call that needs one: on a host thread that has made no runtime call that
+  // touches the device yet, bind the device's primary context once.
+  thread_local bool t_bound[kMaxDevices] = {};
+  if (!t_bound[dev]) {
+    if ((e = cudaSetDevice(dev)) != cudaSuccess) {
+      err = std::string("cudaSetDevice: ") + cudaGetErrorString(e);
+      return CSA_ERR_CUDA;
+    }
+    t_bound[dev] = true;
+  }
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_dev_ready[dev]) {
     DeviceInfo d;

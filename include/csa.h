@@ -57,7 +57,9 @@
  *    bounded wait ran out records CSA_ERR_TIMEOUT there and returns early
  *    (its output is then incomplete); csa_get_status() reports and clears it.
  *  - Thread safety: entry points may be called from several host threads; the
- *    error string is per thread.
+ *    error string is per thread. Each call works on the calling thread's current
+ *    device (cudaGetDevice); the first call on a thread makes that device's
+ *    primary context current there (cudaSetDevice).
  */
 #ifndef CSA_GB300_H
 #define CSA_GB300_H

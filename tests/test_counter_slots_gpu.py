@@ -105,3 +105,39 @@ def test_graph_replayed_beside_direct_launches(oracle_lib):
     assert csa.get_status() == 0
     _check_scores(out_a, _scores_ref(oracle_lib, qa, sa), "graph replays")
     _check_scores(out_b, _scores_ref(oracle_lib, qb, sb), "direct launches beside them")
+
+
+def test_launches_from_four_host_threads(oracle_lib):
+    """Four host threads, each on its own stream, launch score and softmax kernels at
+    once: the counter sets are handed out under a lock, every result is the oracle's."""
+    import threading
+    cases = [trimul_case(1, 300 + 70 * k, 2, 64, seed=80 + k) for k in range(4)]
+    qs = [q.cuda() for _, q in cases]
+    outs = [poisoned(s.out_shape) for s, _ in cases]
+    atts = [poisoned(s.out_shape) for s, _ in cases]
+    streams = [torch.cuda.Stream() for _ in cases]
+    errors = []
+
+    def work(k):
+        try:
+            s, _ = cases[k]
+            for _ in range(10):
+                csa.trimul_forward(outs[k], qs[k], s.B, s.T, s.C, s.NH, stream=streams[k])
+                csa.causal_softmax_forward(atts[k], qs[k], s.B, s.T, s.C, s.NH, stream=streams[k])
+        except Exception as e:  # reported below, on the main thread
+            errors.append(e)
+
+    torch.cuda.synchronize()
+    threads = [threading.Thread(target=work, args=(k,)) for k in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    assert csa.get_status() == 0
+    from gpu_util import assert_close
+    for k, ((s, q), out, att) in enumerate(zip(cases, outs, atts)):
+        _check_scores(out, _scores_ref(oracle_lib, q, s), f"thread {k}")
+        ref = oracle_lib.causal_softmax(synth.bf16_bits(q).reshape(-1), s.B, s.T, s.C, s.NH)
+        assert_close(att.cpu().numpy(), ref, f"softmax thread {k}")
