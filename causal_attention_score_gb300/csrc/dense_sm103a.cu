@@ -61,6 +61,11 @@ constexpr int kFirstEpiWarp = 5;
 #ifndef CSA_DENSE_PAIR
 #define CSA_DENSE_PAIR 1
 #endif
+// One problem (dense_xwt): CTA pairs when the tiling model prefers them (-1),
+// never (0), always when the rows are fetched by TMA (1).
+#ifndef CSA_DENSE_SINGLE_PAIR
+#define CSA_DENSE_SINGLE_PAIR -1
+#endif
 #ifndef CSA_DENSE_STORE_BUFS
 #define CSA_DENSE_STORE_BUFS 2
 #endif
@@ -157,7 +162,7 @@ __device__ __forceinline__ void issue_block_async(const uint16_t* src, int nrows
   }
 }
 
-// kPair (groups only): clusters of two CTAs compute 256-row tiles as a CTA pair
+// kPair: clusters of two CTAs compute 256-row tiles as a CTA pair
 // (tcgen05 cta_group::2): each CTA loads its own 128 rows of X and half of the W
 // tile's rows, and the pair's first CTA issues M = 256 MMAs that read both CTAs'
 // shared memory, each CTA's TMEM receiving its own rows. Per k-block each SM then
@@ -203,7 +208,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the m-tiles of all problems following one another. One problem is n-major
   // (measured 2 % faster than m-major over the sweep's separate calls).
   auto locate = [&](long long t, int& p, int& mb, int& nb) {
-    if constexpr (kGrouped) {
+    if constexpr (!kGrouped && kPair) {
+      // One problem in pairs: t numbers (pair of m-tiles, n-tile), n-major; the
+      // phantom half of a pair past the last m-tile is zero-filled and not stored.
+      const long long m_pairs = (a.m_tiles + 1) / 2;
+      p = 0;
+      mb = static_cast<int>(2 * (t % m_pairs) + rank);
+      nb = static_cast<int>(t / m_pairs);
+    } else if constexpr (kGrouped) {
       // (pairs: t numbers tile pairs; a pair past the last m-tile has a phantom
       // half, whose rows are past its problem's M: zero-filled and not stored)
       const int mt = kPair ? static_cast<int>(2 * (t / a.n_tiles) + rank)
@@ -230,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int n = 1;
     if constexpr (kGrouped) n = g.n;
     return p >= 0 && p < n && mb >= 0 && nb >= 0 && nb < a.n_tiles &&
-           (kGrouped || mb < a.m_tiles);
+           (kGrouped || mb < a.m_tiles + (kPair ? 1 : 0));
   };
 #endif
   auto map_x = [&](int p) -> const CUtensorMap* {
@@ -667,16 +679,22 @@ __global__ void __launch_bounds__(kRealignThreads)
   }
 }
 
-// Tile width along H: the largest BN whose wave count times tile cost is
-// smallest (tile cost ~ BN plus a fixed per-tile overhead), for m_tiles rows of
-// 128-row tiles.
-int choose_bn_tiles(long long m_tiles, int H, int sms) {
+// Cost of a tiling: waves of `rows` x ceil(H / bn) work units over `slots`
+// concurrent units (SMs, or clusters for CTA pairs), times the cost of one
+// unit (~ bn plus a fixed per-tile overhead; each SM's share of a unit is a
+// 128 x bn output tile in both forms).
+long long tiling_cost(long long rows, int H, int bn, int slots) {
+  const long long tiles = rows * ((H + bn - 1) / bn);
+  return (tiles + slots - 1) / slots * (bn + 32);
+}
+
+// Tile width along H: the largest BN of least tiling cost, for `rows` rows of
+// work units (128-row m-tiles, or pairs of them) over `slots` units at a time.
+int choose_bn_tiles(long long rows, int H, int slots) {
   int best = 64;
   long long best_cost = -1;
   for (int bn : {256, 192, 128, 64}) {
-    const long long tiles = m_tiles * ((H + bn - 1) / bn);
-    const long long waves = (tiles + sms - 1) / sms;
-    const long long cost = waves * (bn + 32);
+    const long long cost = tiling_cost(rows, H, bn, slots);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best = bn;
@@ -685,7 +703,42 @@ int choose_bn_tiles(long long m_tiles, int H, int sms) {
   return best;
 }
 
-int choose_bn(int M, int H, int sms) { return choose_bn_tiles((M + kBM - 1) / kBM, H, sms); }
+// Clusters of two CTAs of `kernel` resident at once with `smem` bytes of
+// dynamic shared memory each (its maximum already raised to that); 0 when none
+// fit or the query fails.
+int pair_clusters(const void* kernel, size_t smem, const DeviceInfo& dev) {
+  struct Entry {
+    const void* fn;
+    int device;
+    size_t smem;
+    int clusters;
+  };
+  static std::mutex mu;
+  static Entry cache[32];
+  static int count = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < count; ++i)
+    if (cache[i].fn == kernel && cache[i].device == dev.device && cache[i].smem == smem)
+      return cache[i].clusters;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  if (count < 32) cache[count++] = Entry{kernel, dev.device, smem, n};
+  return n;
+}
 
 // TMEM columns for two BN-wide accumulators: an allocation is a power of two >= 32.
 uint32_t tmem_cols_for(int BN) {
@@ -750,11 +803,9 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H, vo
   a.M = M;
   a.I = I;
   a.H = H;
-  a.BN = choose_bn(M, H, dev.sm_count);
   a.m_tiles = (M + kBM - 1) / kBM;
-  a.n_tiles = (H + a.BN - 1) / a.BN;
+  a.BN = choose_bn_tiles(a.m_tiles, H, dev.sm_count);
   a.kblocks = (I + kBK - 1) / kBK;
-  a.num_tiles = static_cast<long long>(a.m_tiles) * a.n_tiles;
   a.tma_load = rows_describable(X, W, I) ? 1u : 0u;
   a.tma_store = ((static_cast<long long>(H) * 4) % 16 == 0 && py % 16 == 0) ? 1u : 0u;
   a.vec2 = (I % 2 == 0 && px % 4 == 0 && pw % 4 == 0) ? 1u : 0u;
@@ -782,17 +833,54 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H, vo
     a.tma_load = 1u;
     realign = true;
   }
-  a.idesc = idesc_bf16_f32(kBM, a.BN);
+  // CTA pairs (256-row tiles, each SM loading half of the W tile) when the rows
+  // are fetched by TMA and the pair tiling, counted in clusters of two, costs
+  // less than single CTAs', or as much with three tiles or more per cluster.
+  // (Measured with L2 flushed, I = 768, H = 3072: pairs 4-8 % faster from
+  // M = 6144 up, within 1 us of single CTAs at 2-2.5 tiles per cluster, 2 us
+  // slower where either form takes one wave.)
+  auto* kernel_pair = dense_sm103a_kernel<false, true>;
+  const long long m_pairs = (a.m_tiles + 1) / 2;
+  const int cluster_slots = std::max(1, dev.sm_count / 2);
+  const int bn_pair = choose_bn_tiles(m_pairs, H, cluster_slots);
+  bool pair = false;
+  if (a.tma_load && CSA_DENSE_SINGLE_PAIR != 0) {
+    const long long cost_single = tiling_cost(a.m_tiles, H, a.BN, dev.sm_count);
+    const long long cost_pair = tiling_cost(m_pairs, H, bn_pair, cluster_slots);
+    const long long pair_tiles = m_pairs * ((H + bn_pair - 1) / bn_pair);
+    pair = CSA_DENSE_SINGLE_PAIR == 1 || cost_pair < cost_single ||
+           (cost_pair == cost_single && pair_tiles >= 3LL * cluster_slots);
+  }
   a.X = static_cast<const uint16_t*>(X);
   a.W = static_cast<const uint16_t*>(W);
   a.Y = Y;
   a.status = dev.status_word;
   a.wait_limit_ns = wait_limit_ns();
   a.inject = take_inject() ? 1 : 0;
-  a.tmem_cols = tmem_cols_for(a.BN);
 
   size_t smem = 0;
-  {
+  int clusters = 0;
+  if (pair) {
+    a.BN = bn_pair;
+    int rc = plan_smem(a, dev, err, smem, a.BN / 2);
+    if (rc != CSA_OK) return rc;
+    rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kernel_pair), static_cast<int>(smem),
+                              dev.device, err);
+    if (rc != CSA_OK) {
+      err = "dense_xwt: " + err;
+      return rc;
+    }
+    clusters = pair_clusters(reinterpret_cast<const void*>(kernel_pair), smem, dev);
+    if (clusters < 1) {
+      pair = false;
+      a.BN = choose_bn_tiles(a.m_tiles, H, dev.sm_count);
+    }
+  }
+  a.n_tiles = (H + a.BN - 1) / a.BN;
+  a.num_tiles = (pair ? m_pairs : static_cast<long long>(a.m_tiles)) * a.n_tiles;
+  a.idesc = pair ? idesc_bf16_f32(2 * kBM, a.BN) : idesc_bf16_f32(kBM, a.BN);
+  a.tmem_cols = tmem_cols_for(a.BN);
+  if (!pair) {
     const int rc = plan_smem(a, dev, err, smem, a.BN);
     if (rc != CSA_OK) return rc;
   }
@@ -806,7 +894,8 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H, vo
     const uint64_t dw[2] = {static_cast<uint64_t>(I), static_cast<uint64_t>(H)};
     const uint64_t st[1] = {static_cast<uint64_t>(pitch) * 2};
     const uint32_t bx[2] = {kBK, kBM};
-    const uint32_t bw[2] = {kBK, static_cast<uint32_t>(a.BN)};
+    // (pairs: each CTA loads half of the W tile's rows)
+    const uint32_t bw[2] = {kBK, static_cast<uint32_t>(pair ? a.BN / 2 : a.BN)};
     int rc = encode_tiled(&map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, X_tma, dx, st, bx,
                           CU_TENSOR_MAP_SWIZZLE_128B, err);
     if (rc != CSA_OK) return rc;
@@ -823,7 +912,7 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H, vo
     if (rc != CSA_OK) return rc;
   }
 
-  {
+  if (!pair) {
     int rc = set_max_dynamic_smem(reinterpret_cast<const void*>(dense_sm103a_kernel<false>),
                                   static_cast<int>(smem), dev.device, err);
     if (rc != CSA_OK) {
@@ -848,9 +937,15 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H, vo
       return CSA_ERR_LAUNCH;
     }
   }
-  const long long grid = std::min<long long>(a.num_tiles, dev.sm_count);
-  e = launch_programmatic(dense_sm103a_kernel<false>, static_cast<unsigned>(grid), kThreads, smem,
-                          stream, map_x, map_w, map_y, a, DenseGroup<false>{});
+  if (pair) {
+    const long long grid = 2 * std::min<long long>(a.num_tiles, clusters);
+    e = launch_programmatic_cluster(kernel_pair, static_cast<unsigned>(grid), kThreads, smem,
+                                    stream, 2u, map_x, map_w, map_y, a, DenseGroup<false>{});
+  } else {
+    const long long grid = std::min<long long>(a.num_tiles, dev.sm_count);
+    e = launch_programmatic(dense_sm103a_kernel<false>, static_cast<unsigned>(grid), kThreads,
+                            smem, stream, map_x, map_w, map_y, a, DenseGroup<false>{});
+  }
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     err = std::string("dense_xwt: launch: ") + cudaGetErrorString(e);
@@ -971,12 +1066,14 @@ int dense_grouped_launch(float* const* Y, const void* const* X, const void* W, c
     a.M = 0;  // per problem: grp.M
     a.I = I;
     a.H = H;
-    a.BN = choose_bn_tiles(total, H, dev.sm_count);
+    // Pairs of CTAs (clusters of two) walk tile pairs: adjacent m-tiles, one n-tile;
+    // their tile width is chosen for pairs of m-tiles over clusters.
+    bool pair = CSA_DENSE_PAIR != 0;
+    a.BN = pair ? choose_bn_tiles((total + 1) / 2, H, std::max(1, dev.sm_count / 2))
+                : choose_bn_tiles(total, H, dev.sm_count);
     a.m_tiles = static_cast<int>(total);
     a.n_tiles = (H + a.BN - 1) / a.BN;
     a.kblocks = (I + kBK - 1) / kBK;
-    // Pairs of CTAs (clusters of two) walk tile pairs: adjacent m-tiles, one n-tile.
-    bool pair = CSA_DENSE_PAIR != 0;
     a.num_tiles = pair ? (total + 1) / 2 * a.n_tiles : total * a.n_tiles;
     a.tma_load = 1u;
     a.tma_store = tma_store ? 1u : 0u;
@@ -1001,33 +1098,12 @@ int dense_grouped_launch(float* const* Y, const void* const* X, const void* W, c
       rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kernel_pair), static_cast<int>(smem),
                                 dev.device, err);
       if (rc != CSA_OK) return rc;
-      static std::mutex mu;
-      static int cached_smem[64] = {}, cached_clusters[64] = {};
-      std::lock_guard<std::mutex> lock(mu);
-      const int d = dev.device >= 0 && dev.device < 64 ? dev.device : 0;
-      if (cached_smem[d] != static_cast<int>(smem)) {
-        cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3(2);
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = smem;
-        cudaLaunchAttribute at[1];
-        at[0].id = cudaLaunchAttributeClusterDimension;
-        at[0].val.clusterDim.x = 2;
-        at[0].val.clusterDim.y = 1;
-        at[0].val.clusterDim.z = 1;
-        cfg.attrs = at;
-        cfg.numAttrs = 1;
-        int n_clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&n_clusters, kernel_pair, &cfg) != cudaSuccess) {
-          (void)cudaGetLastError();
-          n_clusters = 0;
-        }
-        cached_smem[d] = static_cast<int>(smem);
-        cached_clusters[d] = n_clusters;
-      }
-      clusters = cached_clusters[d];
+      clusters = pair_clusters(reinterpret_cast<const void*>(kernel_pair), smem, dev);
       if (clusters < 1) {
         pair = false;
+        a.BN = choose_bn_tiles(total, H, dev.sm_count);
+        a.n_tiles = (H + a.BN - 1) / a.BN;
+        a.tmem_cols = tmem_cols_for(a.BN);
         a.num_tiles = total * a.n_tiles;
         a.idesc = idesc_bf16_f32(kBM, a.BN);
         rc = plan_smem(a, dev, err, smem, a.BN);

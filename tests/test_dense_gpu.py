@@ -103,6 +103,41 @@ def test_dense_sweep(oracle_lib):
         assert bool(torch.all(torch.isfinite(Y)))
 
 
+# Single calls that run as CTA pairs on a 152-SM GB300 (the tiling model, counting pairs
+# of m-tiles over 76 clusters, costs no more than single CTAs and gives each cluster
+# three tiles or more): realigned rows (I = 770) with H not a multiple of the tile
+# width; an odd number of m-tiles (the last pair's second half lies past M) with
+# H % 4 != 0 (plain stores); a single k-block; a ragged last k-block (I = 136); and a
+# shape that takes single CTAs, for contrast.
+PAIR_SHAPES = [(5000, 770, 3000), (12345, 768, 3071), (30000, 64, 2304), (6500, 136, 4100),
+               (2049, 768, 3072)]
+
+
+@pytest.mark.parametrize("M,I,H", PAIR_SHAPES)
+def test_dense_large_call_matches_512_row_calls_and_oracle(oracle_lib, M, I, H):
+    """Every row of a large call (CTA pairs, but for the last shape) equals, bit for bit,
+    the same row from calls of 512 rows (single CTAs: the same products summed in the
+    same k order), and sampled rows match the oracle."""
+    X, W = synth.dense_input(synth.DenseShape(M=M, I=I, H=H), seed=M + H)
+    Xd, Wd = X.cuda(), W.cuda()
+    Y = poisoned((M, H))
+    csa.dense_xwt(Y, Xd, Wd, M, I, H)
+    torch.cuda.synchronize()
+    assert csa.get_status() == 0
+    assert bool(torch.all(torch.isfinite(Y)))
+    for r0 in range(0, M, 512):
+        n = min(512, M - r0)
+        Ys = poisoned((n, H))
+        csa.dense_xwt(Ys, Xd[r0:r0 + n], Wd, n, I, H)
+        torch.cuda.synchronize()
+        assert torch.equal(Y[r0:r0 + n], Ys), f"rows {r0}..{r0 + n} of {(M, I, H)}"
+    rng = np.random.default_rng(M)
+    rows = np.unique(np.concatenate([[0, M - 1, (M - 1) // 256 * 256], rng.integers(0, M, size=6)]))
+    ref = oracle_lib.dense_rows(synth.bf16_bits(X).reshape(-1), synth.bf16_bits(W).reshape(-1),
+                                M, I, H, rows)
+    assert_close(Y[torch.from_numpy(rows).cuda()].cpu().numpy(), ref, f"dense{(M, I, H)} rows")
+
+
 @pytest.fixture(params=["auto", "loaders"])
 def fetch_mode(request):
     """Both fetch paths for rows no tensor map can describe: the rows realigned into
