@@ -45,6 +45,12 @@ if ROOT not in sys.path:
 METRIC = "useful TFLOP/s (lower-triangle FLOPs) and % of GB300 bf16 dense peak"
 UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 * 1024 * 1024
+# The default step runs its dense calls on a stream limited to this many SMs,
+# launched first, beside the score kernel on a stream of its own: the score kernel
+# starts on the other SMs and takes the rest as the dense kernels finish (its work
+# list is dynamic). Measured over limits 32-80 on a GB300 (L2 flushed): 56 best,
+# 439 us per step against 467 us with the three calls one after another.
+STEP_DENSE_SMS = 56
 
 
 # --------------------------------------------------------------- work model --
@@ -278,7 +284,8 @@ class Workload:
     that stands for a bounded part of the step on the CPU."""
 
     def __init__(self, name, config, parts, flops, h2d, d2h, dtype="bf16",
-                 data="synthetic (seeded N(0,1) / uniform[-1,1], rounded to bf16)", calls=None):
+                 data="synthetic (seeded N(0,1) / uniform[-1,1], rounded to bf16)", calls=None,
+                 branches=None):
         self.name = name          # human-readable workload string (config.workload)
         self.dtype = dtype        # arithmetic type of the path
         self.data = data
@@ -288,6 +295,10 @@ class Workload:
         self.h2d = h2d            # [(device tensor, host tensor)]
         self.d2h = d2h            # [(host tensor, device tensor)]
         self.calls = calls or []
+        # Concurrent schedule of a timed step: [(sm_limit, [Part])], each branch on a
+        # stream of its own (0: no SM limit), launched in this order after a fork from
+        # the step's stream and joined back into it; None: the parts one after another.
+        self.branches = branches
         self.kernels_per_step = sum(p.kernels for p in parts)
 
 
@@ -364,7 +375,8 @@ def make_workload(name, dev):
              "dense": {"M": ds.M, "I": ds.I, "H": ds.H}},
             [tp, gp, dp],
             trimul_flops(tl.B, tl.T, tl.C, tl.NH) + gflops + dense_flops(ds.M, ds.I, ds.H),
-            th + gh + dh, to + go + do, calls=calls)
+            th + gh + dh, to + go + do, calls=calls,
+            branches=[(STEP_DENSE_SMS, [gp, dp]), (0, [tp])])
     if name == "step_gpt2":
         tp, th, to = trimul_part(ts, traffic="trimul_gpt2")
         dp, dh, do = dense_part(ds)
@@ -491,25 +503,50 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     wl = make_workload(args.workload, dev)
+    if wl.branches and args.dense_sms is not None:
+        wl.branches = [(args.dense_sms if limit else 0, parts) for limit, parts in wl.branches]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     P = len(wl.parts)
 
+    branch_streams = []
+    if wl.branches:
+        branch_streams = [torch.cuda.Stream(dev) for _ in wl.branches]
+        for (limit, _), bs in zip(wl.branches, branch_streams):
+            csa.set_stream_sm_limit(bs, limit)
+
+    def launch(st):
+        if wl.branches:
+            for bs in branch_streams:
+                bs.wait_stream(st)
+            for (_, parts), bs in zip(wl.branches, branch_streams):
+                for part in parts:
+                    part.fn(bs)
+            for bs in branch_streams:
+                st.wait_stream(bs)
+        else:
+            for part in wl.parts:
+                part.fn(st)
+
     def step():
-        for part in wl.parts:
-            part.fn(stream)
+        launch(stream)
 
     graph = None
-    if args.graph:
-        # The step's launches captured once and replayed as one CUDA graph.
+    if args.graph or (wl.branches and not args.direct):
+        # The step's launches captured once and replayed as one CUDA graph. A step
+        # whose parts run on concurrent streams takes this form by default: the graph
+        # holds the fork and the join itself, so the branches overlap however the
+        # streams map onto the GPU's hardware queues (direct launches of the default
+        # step overlapped only with a short queue and CUDA_DEVICE_MAX_CONNECTIONS=32:
+        # 443 us per step; with 200 steps queued they ran one after the other, 635 us;
+        # the graph, 439 us).
         step()
         torch.cuda.synchronize(dev)
         side = torch.cuda.Stream(dev)
         side.wait_stream(stream)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=side):
-            for part in wl.parts:
-                part.fn(side)
+            launch(side)
         torch.cuda.synchronize(dev)
 
     def run_step():
@@ -678,6 +715,12 @@ def run_ours(args, rank, world, local):
     config = {"workload": wl.name, **wl.config,
               "l2": "flushed between timed steps (256 MiB write, outside the timed events)",
               "launch": "one CUDA graph per step" if graph is not None else "direct launches",
+              "schedule": ("; ".join(
+                  f"stream {i}: {' + '.join(p.label for p in parts)}"
+                  + (f" (at most {limit} SMs)" if limit else " (no SM limit)")
+                  for i, (limit, parts) in enumerate(wl.branches))
+                  + "; launched in this order, forked from and joined into the step's stream"
+                  if wl.branches else "the parts one after another on one stream"),
               "parallelism": f"replicas x{world}"}
     clocks = sampler.summary()
     if n_soak:
@@ -894,10 +937,18 @@ def main(argv=None):
     p.add_argument("--workload", choices=WORKLOADS, default="step",
                    help="what a step runs (default: the headline step)")
     p.add_argument("--graph", action="store_true",
-                   help="capture each step's launches as one CUDA graph and replay it")
+                   help="capture each step's launches as one CUDA graph and replay it (the "
+                        "default for a step whose parts run on concurrent streams)")
+    p.add_argument("--dense-sms", type=int, default=None,
+                   help=f"SM limit of the dense stream in the default step (default "
+                        f"{STEP_DENSE_SMS}; 0: none)")
+    p.add_argument("--direct", action="store_true",
+                   help="launch every step's kernels directly, even on concurrent streams")
     args = p.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         p.error("--warmup must be >= 3")
+    if args.graph and args.direct:
+        p.error("--graph and --direct exclude each other")
 
     if args.impl == "reference":
         # The oracle runs on the host of rank 0 only; other ranks have no work.

@@ -58,6 +58,8 @@ SIGNATURES = {
     "csa_debug_hold_stream": (_i, [_vp]),
     "csa_debug_release_streams": (None, []),
     "csa_set_dense_fetch": (_i, [_i]),
+    "csa_set_stream_sm_limit": (_i, [_vp, _i]),
+    "csa_get_stream_sm_limit": (_i, [_vp, ctypes.POINTER(ctypes.c_int)]),
 }
 
 

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <chrono>
 #include <condition_variable>
@@ -112,6 +113,32 @@ int current_device(DeviceInfo& info, std::string& err) {
   info = g_dev[dev];
   return CSA_OK;
 }
+
+namespace {
+
+// Per-stream SM limits (csa_set_stream_sm_limit): launches on a listed stream
+// size their persistent grids and tilings for at most that many SMs.
+struct SmLimit {
+  cudaStream_t stream;
+  int sms;
+};
+constexpr int kMaxSmLimits = 64;
+std::mutex g_limit_mu;
+SmLimit g_limits[kMaxSmLimits];
+int g_limit_count = 0;
+std::atomic<int> g_any_limit{0};
+
+void apply_stream_sm_limit(DeviceInfo& info, cudaStream_t stream) {
+  if (g_any_limit.load(std::memory_order_acquire) == 0) return;
+  std::lock_guard<std::mutex> lock(g_limit_mu);
+  for (int i = 0; i < g_limit_count; ++i)
+    if (g_limits[i].stream == stream) {
+      info.sm_count = std::max(1, std::min(info.sm_count, g_limits[i].sms));
+      return;
+    }
+}
+
+}  // namespace
 
 namespace {
 
@@ -398,6 +425,7 @@ csa_status trimul_forward_ex(float* out, const void* qkv, int B, int T, int C, i
   std::string err;
   int rc = current_device(dev, err);
   if (rc != CSA_OK) return set_error(rc, err);
+  apply_stream_sm_limit(dev, static_cast<cudaStream_t>(stream));
   rc = trimul_launch(out, qkv, B, T, C, NH, mask_bits, flags, static_cast<cudaStream_t>(stream),
                      dev, err);
   if (rc != CSA_OK) return set_error(rc, err);
@@ -423,6 +451,7 @@ csa_status trimul_forward_f32(float* out, const float* qkv, int B, int T, int C,
   std::string err;
   int rc = current_device(dev, err);
   if (rc != CSA_OK) return set_error(rc, err);
+  apply_stream_sm_limit(dev, static_cast<cudaStream_t>(stream));
   rc = trimul_f32_launch(out, qkv, B, T, C, NH, mask_bits, flags,
                          static_cast<cudaStream_t>(stream), dev, err);
   if (rc != CSA_OK) return set_error(rc, err);
@@ -449,6 +478,7 @@ csa_status trimul_forward_noalloc(float* out, const void* qkv, int B, int T, int
   std::string err;
   int rc = current_device(dev, err);
   if (rc != CSA_OK) return set_error(rc, err);
+  apply_stream_sm_limit(dev, static_cast<cudaStream_t>(stream));
   rc = trimul_launch_noalloc(out, qkv, B, T, C, NH, mask_bits, flags,
                              static_cast<cudaStream_t>(stream), dev, err);
   if (rc != CSA_OK) return set_error(rc, err);
@@ -477,6 +507,7 @@ csa_status causal_softmax_forward(float* att, const void* qkv, int B, int T, int
   std::string err;
   int rc = current_device(dev, err);
   if (rc != CSA_OK) return set_error(rc, err);
+  apply_stream_sm_limit(dev, static_cast<cudaStream_t>(stream));
   rc = softmax_launch(att, qkv, B, T, C, NH, static_cast<cudaStream_t>(stream), dev, err);
   if (rc != CSA_OK) return set_error(rc, err);
   return CSA_OK;
@@ -498,6 +529,7 @@ csa_status batch_matmul_nt(float* Y, const void* X, const void* W, int batch, in
   std::string err;
   int rc = current_device(dev, err);
   if (rc != CSA_OK) return set_error(rc, err);
+  apply_stream_sm_limit(dev, static_cast<cudaStream_t>(stream));
   rc = bmm_nt_launch(Y, X, W, batch, T1, T2, D, static_cast<cudaStream_t>(stream), dev, err);
   if (rc != CSA_OK) return set_error(rc, err);
   return CSA_OK;
@@ -512,6 +544,7 @@ csa_status dense_xwt_ex(float* Y, const void* X, const void* W, int M, int I, in
   std::string err;
   rc = current_device(dev, err);
   if (rc != CSA_OK) return set_error(rc, err);
+  apply_stream_sm_limit(dev, static_cast<cudaStream_t>(stream));
   rc = dense_launch(Y, X, W, M, I, H, nullptr, 0, static_cast<cudaStream_t>(stream), dev, err);
   if (rc != CSA_OK) return set_error(rc, err);
   return CSA_OK;
@@ -546,6 +579,7 @@ csa_status dense_xwt_ws(float* Y, const void* X, const void* W, int M, int I, in
   std::string err;
   rc = current_device(dev, err);
   if (rc != CSA_OK) return set_error(rc, err);
+  apply_stream_sm_limit(dev, static_cast<cudaStream_t>(stream));
   rc = dense_launch(Y, X, W, M, I, H, need > 0 ? workspace : nullptr, workspace_bytes,
                     static_cast<cudaStream_t>(stream), dev, err);
   if (rc != CSA_OK) return set_error(rc, err);
@@ -597,6 +631,7 @@ csa_status dense_xwt_grouped_ws(float* const* Y, const void* const* X, const voi
   std::string err;
   rc = current_device(dev, err);
   if (rc != CSA_OK) return set_error(rc, err);
+  apply_stream_sm_limit(dev, static_cast<cudaStream_t>(stream));
   rc = dense_grouped_launch(Y, X, W, M, n, I, H, workspace, workspace_bytes,
                             static_cast<cudaStream_t>(stream), dev, err);
   if (rc != CSA_OK) return set_error(rc, err);
@@ -713,6 +748,41 @@ void csa_debug_release_streams(void) {
     g_hold_released = g_hold_issued;
   }
   g_hold_cv.notify_all();
+}
+
+csa_status csa_set_stream_sm_limit(void* stream, int max_sms) {
+  t_last_error.clear();
+  if (max_sms < 0)
+    return set_error(CSA_ERR_SHAPE, "csa_set_stream_sm_limit: max_sms must be >= 0");
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(g_limit_mu);
+  for (int i = 0; i < g_limit_count; ++i) {
+    if (g_limits[i].stream != s) continue;
+    if (max_sms == 0) {
+      g_limits[i] = g_limits[--g_limit_count];
+    } else {
+      g_limits[i].sms = max_sms;
+    }
+    g_any_limit.store(g_limit_count, std::memory_order_release);
+    return CSA_OK;
+  }
+  if (max_sms == 0) return CSA_OK;
+  if (g_limit_count == kMaxSmLimits)
+    return set_error(CSA_ERR_BUSY, "csa_set_stream_sm_limit: 64 streams already carry a limit");
+  g_limits[g_limit_count++] = SmLimit{s, max_sms};
+  g_any_limit.store(g_limit_count, std::memory_order_release);
+  return CSA_OK;
+}
+
+csa_status csa_get_stream_sm_limit(void* stream, int* max_sms) {
+  t_last_error.clear();
+  if (!max_sms) return set_error(CSA_ERR_NULL, "csa_get_stream_sm_limit: null pointer");
+  *max_sms = 0;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(g_limit_mu);
+  for (int i = 0; i < g_limit_count; ++i)
+    if (g_limits[i].stream == s) *max_sms = g_limits[i].sms;
+  return CSA_OK;
 }
 
 csa_status csa_set_dense_fetch(int mode) {

@@ -870,7 +870,9 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H, vo
       err = "dense_xwt: " + err;
       return rc;
     }
-    clusters = pair_clusters(reinterpret_cast<const void*>(kernel_pair), smem, dev);
+    // (at most one cluster per two of the SMs this call may use)
+    clusters = std::min(pair_clusters(reinterpret_cast<const void*>(kernel_pair), smem, dev),
+                        dev.sm_count / 2);
     if (clusters < 1) {
       pair = false;
       a.BN = choose_bn_tiles(a.m_tiles, H, dev.sm_count);
@@ -1098,7 +1100,8 @@ int dense_grouped_launch(float* const* Y, const void* const* X, const void* W, c
       rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kernel_pair), static_cast<int>(smem),
                                 dev.device, err);
       if (rc != CSA_OK) return rc;
-      clusters = pair_clusters(reinterpret_cast<const void*>(kernel_pair), smem, dev);
+      clusters = std::min(pair_clusters(reinterpret_cast<const void*>(kernel_pair), smem, dev),
+                          dev.sm_count / 2);
       if (clusters < 1) {
         pair = false;
         a.BN = choose_bn_tiles(total, H, dev.sm_count);

@@ -269,5 +269,22 @@ def set_dense_fetch(mode: int) -> None:
     _lib.check(_lib.load().csa_set_dense_fetch(int(mode)), "csa_set_dense_fetch")
 
 
+def set_stream_sm_limit(stream, max_sms: int) -> None:
+    """Later calls on ``stream`` (a torch stream or raw handle) size their grids for at
+    most ``max_sms`` SMs, so that calls on two streams can share the GPU's SMs; 0
+    removes the limit. Same bits under any limit."""
+    _lib.check(_lib.load().csa_set_stream_sm_limit(_stream_ptr(stream), int(max_sms)),
+               "csa_set_stream_sm_limit")
+
+
+def get_stream_sm_limit(stream) -> int:
+    """The SM limit set on ``stream`` (0: none)."""
+    import ctypes
+    v = ctypes.c_int(0)
+    _lib.check(_lib.load().csa_get_stream_sm_limit(_stream_ptr(stream), ctypes.byref(v)),
+               "csa_get_stream_sm_limit")
+    return v.value
+
+
 def version() -> str:
     return _lib.load().csa_version().decode()

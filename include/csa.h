@@ -293,6 +293,26 @@ csa_status dense_xwt_grouped_ws(float* const* Y, const void* const* X, const voi
 csa_status csa_set_dense_fetch(int mode);
 
 /*
+ * csa_set_stream_sm_limit -- later calls of this library on `stream` (a
+ * cudaStream_t; NULL is the legacy default stream) size their grids and tilings for
+ * at most `max_sms` SMs: persistent kernels launch at most that many CTAs (CTA
+ * pairs: max_sms / 2 clusters). Every kernel of this library holds a whole SM per
+ * CTA (its shared memory), so a call limited to S SMs on one stream and a call
+ * limited to the device's SM count minus S on another can run side by side on
+ * disjoint SMs, as long as the first is launched first (clusters need whole pairs
+ * of SMs). max_sms = 0 removes the limit; a limit above the device's SM count has
+ * no effect. Results are the same bits under any limit. Limits are keyed by the
+ * stream's handle value, process-wide, for at most 64 streams at once (then
+ * CSA_ERR_BUSY); a stream destroyed with a limit set should have it removed
+ * first, since a new stream may reuse the handle. Returns CSA_OK, CSA_ERR_SHAPE
+ * for max_sms < 0, or CSA_ERR_BUSY.
+ */
+csa_status csa_set_stream_sm_limit(void* stream, int max_sms);
+
+/* csa_get_stream_sm_limit -- the limit set on `stream` (0: none) into *max_sms. */
+csa_status csa_get_stream_sm_limit(void* stream, int* max_sms);
+
+/*
  * causal_softmax_forward -- the causal score rows of trimul_forward followed by
  * a softmax over t2 <= t, in one kernel (the scores never reach memory):
  *   att[b][h][t][t2] = exp(s[t2] - m) / sum_{u <= t} exp(s[u] - m)  for t2 <= t,

@@ -314,3 +314,35 @@ def test_dense_grouped_workspace_size_and_errors(lib):
     need = 256 + r256(64 * P * 2) + sum(r256(m * P * 2) for m in (10, 300, 1))
     assert lib.dense_xwt_grouped_ws(ys, xs, 4096, ms, 3, 770, 64, (1 << 24) + 8, need, None) == \
         _lib.CSA_ERR_ALIGN
+
+
+def test_stream_sm_limits_on_the_host(lib):
+    """Per-stream SM limits are host state: set, read back, replaced, removed; a
+    negative limit is refused; at most 64 streams carry one (then CSA_ERR_BUSY)."""
+    v = ctypes.c_int(-1)
+    s1, s2 = ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000)
+    assert lib.csa_get_stream_sm_limit(s1, ctypes.byref(v)) == 0 and v.value == 0
+    assert lib.csa_set_stream_sm_limit(s1, 100) == 0
+    assert lib.csa_set_stream_sm_limit(s2, 52) == 0
+    assert lib.csa_get_stream_sm_limit(s1, ctypes.byref(v)) == 0 and v.value == 100
+    assert lib.csa_get_stream_sm_limit(s2, ctypes.byref(v)) == 0 and v.value == 52
+    assert lib.csa_set_stream_sm_limit(s1, 96) == 0
+    assert lib.csa_get_stream_sm_limit(s1, ctypes.byref(v)) == 0 and v.value == 96
+    assert lib.csa_set_stream_sm_limit(s1, -1) == _lib.CSA_ERR_SHAPE
+    assert lib.csa_get_stream_sm_limit(s1, ctypes.byref(v)) == 0 and v.value == 96
+    assert lib.csa_get_stream_sm_limit(s1, None) == _lib.CSA_ERR_NULL
+    for s in (s1, s2):
+        assert lib.csa_set_stream_sm_limit(s, 0) == 0
+        assert lib.csa_get_stream_sm_limit(s, ctypes.byref(v)) == 0 and v.value == 0
+    assert lib.csa_set_stream_sm_limit(s1, 0) == 0  # removing an absent limit is fine
+    handles = [ctypes.c_void_p(0x10000 + 16 * i) for i in range(65)]
+    try:
+        for h in handles[:64]:
+            assert lib.csa_set_stream_sm_limit(h, 8) == 0
+        assert lib.csa_set_stream_sm_limit(handles[64], 8) == _lib.CSA_ERR_BUSY
+        assert lib.csa_set_stream_sm_limit(handles[3], 0) == 0
+        assert lib.csa_set_stream_sm_limit(handles[64], 8) == 0
+        assert lib.csa_get_stream_sm_limit(handles[63], ctypes.byref(v)) == 0 and v.value == 8
+    finally:
+        for h in handles:
+            lib.csa_set_stream_sm_limit(h, 0)
