@@ -504,7 +504,9 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     wl = make_workload(args.workload, dev)
     if wl.branches and args.dense_sms is not None:
-        wl.branches = [(args.dense_sms if limit else 0, parts) for limit, parts in wl.branches]
+        # (the first branch holds the dense calls; a limit of 0 lifts theirs)
+        wl.branches = [(args.dense_sms if i == 0 else limit, parts)
+                       for i, (limit, parts) in enumerate(wl.branches)]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     P = len(wl.parts)
@@ -940,8 +942,8 @@ def main(argv=None):
                    help="capture each step's launches as one CUDA graph and replay it (the "
                         "default for a step whose parts run on concurrent streams)")
     p.add_argument("--dense-sms", type=int, default=None,
-                   help=f"SM limit of the dense stream in the default step (default "
-                        f"{STEP_DENSE_SMS}; 0: none)")
+                   help=f"SM limit of the dense calls' stream in a step with concurrent "
+                        f"streams (default: {STEP_DENSE_SMS} in the default step; 0: none)")
     p.add_argument("--direct", action="store_true",
                    help="launch every step's kernels directly, even on concurrent streams")
     args = p.parse_args(argv)
