@@ -80,7 +80,10 @@ def test_batch_matmul_nt(dbg):
     _same_and_clean(dbg, a, b, "batched NT")
 
 
-@pytest.mark.parametrize("M,I,H", [(960, 770, 768), (300, 768, 136), (2049, 256, 3072)])
+# (the last two run as CTA pairs: an odd number of m-tiles with H % 4 != 0, and a ragged
+# last k-block)
+@pytest.mark.parametrize("M,I,H", [(960, 770, 768), (300, 768, 136), (2049, 256, 3072),
+                                   (12345, 768, 3071), (6500, 136, 4100)])
 def test_dense(dbg, M, I, H):
     X, W = synth.dense_input(synth.DenseShape(M=M, I=I, H=H), seed=M)
     Xd, Wd = X.cuda(), W.cuda()

@@ -106,6 +106,28 @@ def test_withheld_hand_off_dense(oracle_lib, M, I, H, mode):
         csa.set_dense_fetch(csa.DENSE_FETCH_AUTO)
 
 
+@pytest.mark.parametrize("M,I,H", [(6144, 768, 3072), (5000, 770, 3000)])
+def test_withheld_hand_off_dense_pairs(oracle_lib, M, I, H):
+    """A single call large enough to run as CTA pairs (TMA rows, and rows realigned into
+    the workspace): both CTAs of the first pair withhold their first loads, the first
+    CTA's MMA wait runs out, and the next call is correct on sampled rows."""
+    import numpy as np
+    from gpu_util import assert_close
+    X, W = synth.dense_input(synth.DenseShape(M=M, I=I, H=H), seed=7)
+    Xd, Wd = X.cuda(), W.cuda()
+    Y = torch.empty((M, H), dtype=torch.float32, device="cuda")
+
+    def check():
+        rows = np.array([0, 255, 256, M // 2, M - 1])
+        ref = oracle_lib.dense_rows(synth.bf16_bits(X).reshape(-1), synth.bf16_bits(W).reshape(-1),
+                                    M, I, H, rows)
+        assert_close(Y[torch.from_numpy(rows).cuda()].cpu().numpy(), ref,
+                     f"dense {M}x{I}x{H} rows after timeout")
+        assert bool(torch.all(torch.isfinite(Y)))
+
+    _timeout_then_recover(lambda: csa.dense_xwt(Y, Xd, Wd, M, I, H), check)
+
+
 def test_withheld_hand_off_dense_grouped(oracle_lib):
     """The grouped launch's TMA producer withholds its first load: the MMA warp's wait
     runs out, the status reports it, and the next call is correct."""
