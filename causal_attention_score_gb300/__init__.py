@@ -23,7 +23,7 @@ from ._lib import (CSA_ERR_ALIGN, CSA_ERR_ARCH, CSA_ERR_CHECK, CSA_ERR_CUDA, CSA
                    CSA_MASK_NAN, CSA_MASK_NEG_INF, CSA_OK, CsaError)
 from .ops import (DENSE_FETCH_AUTO, DENSE_FETCH_LOADERS, DenseGroupedPlan, batch_matmul_nt,
                   causal_softmax, causal_softmax_forward, debug_inject, dense, dense_workspace_size,
-                  dense_xwt, dense_xwt_ws,
+                  dense_tiling, dense_xwt, dense_xwt_ws,
                   dense_xwt_grouped, get_status, get_stream_sm_limit, get_wait_limit_ns,
                   set_dense_fetch, set_stream_sm_limit, set_wait_limit_ns, trimul, trimul_forward,
                   trimul_forward_f32, version)
@@ -33,7 +33,7 @@ __all__ = [
     "dense_xwt_grouped", "DenseGroupedPlan",
     "batch_matmul_nt", "causal_softmax_forward", "causal_softmax", "trimul", "dense", "get_status",
     "set_wait_limit_ns", "get_wait_limit_ns", "debug_inject", "set_dense_fetch",
-    "set_stream_sm_limit", "get_stream_sm_limit",
+    "set_stream_sm_limit", "get_stream_sm_limit", "dense_tiling",
     "DENSE_FETCH_AUTO", "DENSE_FETCH_LOADERS", "version", "CsaError", "CSA_OK", "CSA_ERR_NULL",
     "CSA_ERR_SHAPE",
     "CSA_ERR_ALIGN", "CSA_ERR_UNSUPPORTED", "CSA_ERR_ARCH", "CSA_ERR_LAUNCH", "CSA_ERR_TIMEOUT",

@@ -58,6 +58,7 @@ SIGNATURES = {
     "csa_debug_hold_stream": (_i, [_vp]),
     "csa_debug_release_streams": (None, []),
     "csa_set_dense_fetch": (_i, [_i]),
+    "csa_dense_tiling": (_i, [_i, _i, _i, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
     "csa_set_stream_sm_limit": (_i, [_vp, _i]),
     "csa_get_stream_sm_limit": (_i, [_vp, ctypes.POINTER(ctypes.c_int)]),
 }

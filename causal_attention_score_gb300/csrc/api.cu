@@ -750,6 +750,19 @@ void csa_debug_release_streams(void) {
   g_hold_cv.notify_all();
 }
 
+csa_status csa_dense_tiling(int M, int H, int sms, int* bn, int* pairs) {
+  t_last_error.clear();
+  if (!bn || !pairs) return set_error(CSA_ERR_NULL, "csa_dense_tiling: null pointer");
+  if (M <= 0 || H <= 0 || sms <= 0)
+    return set_error(CSA_ERR_SHAPE, "csa_dense_tiling: M, H, sms must be >= 1");
+  int b = 0;
+  bool p = false;
+  dense_tiling(M, H, sms, true, b, p);
+  *bn = b;
+  *pairs = p ? 1 : 0;
+  return CSA_OK;
+}
+
 csa_status csa_set_stream_sm_limit(void* stream, int max_sms) {
   t_last_error.clear();
   if (max_sms < 0)

@@ -143,6 +143,11 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H, vo
                  size_t ws_bytes, cudaStream_t stream, const DeviceInfo& dev, std::string& err);
 
 // Workspace bytes dense_launch needs to realign X and W (0 when their rows need none).
+// The tile width (64..256) and form (CTA pairs or single CTAs) that one problem of
+// M rows and H columns takes on `sms` SMs when clusters of two fit; pairs need rows
+// fetched by TMA (tma_rows).
+void dense_tiling(int M, int H, int sms, bool tma_rows, int& bn, bool& pair);
+
 size_t dense_workspace_bytes(const void* X, const void* W, int M, int I, int H);
 
 // Dense layers sharing W. Rows no tensor map can describe are first copied into

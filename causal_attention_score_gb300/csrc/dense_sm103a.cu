@@ -791,6 +791,22 @@ size_t dense_workspace_bytes(const void* X, const void* W, int M, int I, int H) 
   return 256 + round256(static_cast<size_t>(M) * P * 2) + static_cast<size_t>(H) * P * 2;
 }
 
+void dense_tiling(int M, int H, int sms, bool tma_rows, int& bn, bool& pair) {
+  const long long m_tiles = (static_cast<long long>(M) + kBM - 1) / kBM;
+  const long long m_pairs = (m_tiles + 1) / 2;
+  const int cluster_slots = sms / 2;
+  bn = choose_bn_tiles(m_tiles, H, sms);
+  pair = false;
+  if (!tma_rows || cluster_slots < 1 || CSA_DENSE_SINGLE_PAIR == 0) return;
+  const int bn_pair = choose_bn_tiles(m_pairs, H, cluster_slots);
+  const long long cost_single = tiling_cost(m_tiles, H, bn, sms);
+  const long long cost_pair = tiling_cost(m_pairs, H, bn_pair, cluster_slots);
+  const long long pair_tiles = m_pairs * ((H + bn_pair - 1) / bn_pair);
+  pair = CSA_DENSE_SINGLE_PAIR == 1 || cost_pair < cost_single ||
+         (cost_pair == cost_single && pair_tiles >= 3LL * cluster_slots);
+  if (pair) bn = bn_pair;
+}
+
 int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H, void* workspace,
                  size_t ws_bytes, cudaStream_t stream, const DeviceInfo& dev, std::string& err) {
   const uintptr_t px = reinterpret_cast<uintptr_t>(X), pw = reinterpret_cast<uintptr_t>(W),
@@ -841,15 +857,11 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H, vo
   // slower where either form takes one wave.)
   auto* kernel_pair = dense_sm103a_kernel<false, true>;
   const long long m_pairs = (a.m_tiles + 1) / 2;
-  const int cluster_slots = std::max(1, dev.sm_count / 2);
-  const int bn_pair = choose_bn_tiles(m_pairs, H, cluster_slots);
   bool pair = false;
-  if (a.tma_load && CSA_DENSE_SINGLE_PAIR != 0) {
-    const long long cost_single = tiling_cost(a.m_tiles, H, a.BN, dev.sm_count);
-    const long long cost_pair = tiling_cost(m_pairs, H, bn_pair, cluster_slots);
-    const long long pair_tiles = m_pairs * ((H + bn_pair - 1) / bn_pair);
-    pair = CSA_DENSE_SINGLE_PAIR == 1 || cost_pair < cost_single ||
-           (cost_pair == cost_single && pair_tiles >= 3LL * cluster_slots);
+  {
+    int bn = 0;
+    dense_tiling(M, H, dev.sm_count, a.tma_load != 0, bn, pair);
+    if (pair) a.BN = bn;
   }
   a.X = static_cast<const uint16_t*>(X);
   a.W = static_cast<const uint16_t*>(W);
@@ -861,7 +873,6 @@ int dense_launch(float* Y, const void* X, const void* W, int M, int I, int H, vo
   size_t smem = 0;
   int clusters = 0;
   if (pair) {
-    a.BN = bn_pair;
     int rc = plan_smem(a, dev, err, smem, a.BN / 2);
     if (rc != CSA_OK) return rc;
     rc = set_max_dynamic_smem(reinterpret_cast<const void*>(kernel_pair), static_cast<int>(smem),

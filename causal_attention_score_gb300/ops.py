@@ -269,6 +269,16 @@ def set_dense_fetch(mode: int) -> None:
     _lib.check(_lib.load().csa_set_dense_fetch(int(mode)), "csa_set_dense_fetch")
 
 
+def dense_tiling(M: int, H: int, sms: int) -> tuple[int, bool]:
+    """(tile width along H, CTA pairs?) that ``dense_xwt`` picks for one problem of M rows
+    and H columns fetched by TMA on ``sms`` SMs; see csa_dense_tiling in include/csa.h."""
+    import ctypes
+    bn, pairs = ctypes.c_int(0), ctypes.c_int(0)
+    _lib.check(_lib.load().csa_dense_tiling(int(M), int(H), int(sms), ctypes.byref(bn),
+                                            ctypes.byref(pairs)), "csa_dense_tiling")
+    return bn.value, bool(pairs.value)
+
+
 def set_stream_sm_limit(stream, max_sms: int) -> None:
     """Later calls on ``stream`` (a torch stream or raw handle) size their grids for at
     most ``max_sms`` SMs, so that calls on two streams can share the GPU's SMs; 0

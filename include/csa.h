@@ -293,6 +293,18 @@ csa_status dense_xwt_grouped_ws(float* const* Y, const void* const* X, const voi
 csa_status csa_set_dense_fetch(int mode);
 
 /*
+ * csa_dense_tiling -- the tiling dense_xwt / dense_xwt_ws choose for one problem of M
+ * rows and H output columns whose rows are fetched by TMA (I * 2 % 16 == 0 and
+ * 16-byte aligned operands, or rows realigned into a workspace), on a device or
+ * stream with `sms` SMs: *bn = the tile width along H (64, 128, 192 or 256) and
+ * *pairs = 1 when clusters of two CTAs compute 256-row tiles together (tcgen05
+ * cta_group::2), else 0. Informational: a call falls back to single CTAs when no
+ * cluster of two fits, and rows fetched by loader warps always use single CTAs.
+ * Host only; returns CSA_OK, CSA_ERR_NULL or CSA_ERR_SHAPE.
+ */
+csa_status csa_dense_tiling(int M, int H, int sms, int* bn, int* pairs);
+
+/*
  * csa_set_stream_sm_limit -- later calls of this library on `stream` (a
  * cudaStream_t; NULL is the legacy default stream) size their grids and tilings for
  * at most `max_sms` SMs: persistent kernels launch at most that many CTAs (CTA

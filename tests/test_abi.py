@@ -346,3 +346,34 @@ def test_stream_sm_limits_on_the_host(lib):
     finally:
         for h in handles:
             lib.csa_set_stream_sm_limit(h, 0)
+
+
+def test_dense_tiling_rule(lib):
+    """The single-call tiling on a 152-SM GB300, worked by hand from the cost model
+    (waves of 128 x BN units over the SMs, or of 256 x BN pair units over 76 clusters,
+    each wave costing BN + 32; pairs on a strictly lower cost, or an equal one with at
+    least three pair tiles per cluster)."""
+    bn, pairs = ctypes.c_int(0), ctypes.c_int(0)
+
+    def tiling(M, H, sms):
+        assert lib.csa_dense_tiling(M, H, sms, ctypes.byref(bn), ctypes.byref(pairs)) == 0
+        return bn.value, pairs.value
+
+    # M = 1088: 9 m-tiles. Single: BN 192 -> 144 tiles, one wave, cost 224 (BN 256: 288).
+    # Pairs: 5 rows; BN 256 -> 60 tiles, one wave, 288; BN 192 -> 80 > 76, two waves.
+    assert tiling(1088, 3072, 152) == (192, 0)
+    # M = 6144: 48 m-tiles. Single: BN 256 -> 576 tiles, 4 waves, 1152 (192: 6 x 224 =
+    # 1344; 128: 8 x 160 = 1280). Pairs: 24 rows, BN 256 -> 288 tiles, 4 waves, 1152:
+    # equal, and 288 >= 3 x 76.
+    assert tiling(6144, 3072, 152) == (256, 1)
+    # M = 4096: single BN 256, 384 tiles, 3 waves, 864; pairs BN 256, 192 tiles, 3 waves,
+    # 864: equal, but 192 < 228 pair tiles.
+    assert tiling(4096, 3072, 152) == (256, 0)
+    # One SM leaves no cluster of two.
+    assert tiling(32768, 3072, 1)[1] == 0
+    assert tiling(32768, 3072, 152)[1] == 1
+    assert lib.csa_dense_tiling(0, 3072, 152, ctypes.byref(bn), ctypes.byref(pairs)) == \
+        _lib.CSA_ERR_SHAPE
+    assert lib.csa_dense_tiling(64, 64, 0, ctypes.byref(bn), ctypes.byref(pairs)) == \
+        _lib.CSA_ERR_SHAPE
+    assert lib.csa_dense_tiling(64, 64, 152, None, ctypes.byref(pairs)) == _lib.CSA_ERR_NULL

@@ -85,6 +85,8 @@ def test_batch_matmul_nt(dbg):
 @pytest.mark.parametrize("M,I,H", [(960, 770, 768), (300, 768, 136), (2049, 256, 3072),
                                    (12345, 768, 3071), (6500, 136, 4100)])
 def test_dense(dbg, M, I, H):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert csa.dense_tiling(M, H, sms)[1] == (M > 5000)
     X, W = synth.dense_input(synth.DenseShape(M=M, I=I, H=H), seed=M)
     Xd, Wd = X.cuda(), W.cuda()
     a, b = poisoned((M, H)), poisoned((M, H))

@@ -109,15 +109,18 @@ def test_dense_sweep(oracle_lib):
 # width; an odd number of m-tiles (the last pair's second half lies past M) with
 # H % 4 != 0 (plain stores); a single k-block; a ragged last k-block (I = 136); and a
 # shape that takes single CTAs, for contrast.
-PAIR_SHAPES = [(5000, 770, 3000), (12345, 768, 3071), (30000, 64, 2304), (6500, 136, 4100),
-               (2049, 768, 3072)]
+PAIR_SHAPES = [(5000, 770, 3000, True), (12345, 768, 3071, True), (30000, 64, 2304, True),
+               (6500, 136, 4100, True), (2049, 768, 3072, False)]
 
 
-@pytest.mark.parametrize("M,I,H", PAIR_SHAPES)
-def test_dense_large_call_matches_512_row_calls_and_oracle(oracle_lib, M, I, H):
+@pytest.mark.parametrize("M,I,H,pairs", PAIR_SHAPES)
+def test_dense_large_call_matches_512_row_calls_and_oracle(oracle_lib, M, I, H, pairs):
     """Every row of a large call (CTA pairs, but for the last shape) equals, bit for bit,
     the same row from calls of 512 rows (single CTAs: the same products summed in the
     same k order), and sampled rows match the oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert csa.dense_tiling(M, H, sms)[1] == pairs
+    assert not csa.dense_tiling(512, H, sms)[1]
     X, W = synth.dense_input(synth.DenseShape(M=M, I=I, H=H), seed=M + H)
     Xd, Wd = X.cuda(), W.cuda()
     Y = poisoned((M, H))

@@ -113,6 +113,7 @@ def test_withheld_hand_off_dense_pairs(oracle_lib, M, I, H):
     CTA's MMA wait runs out, and the next call is correct on sampled rows."""
     import numpy as np
     from gpu_util import assert_close
+    assert csa.dense_tiling(M, H, torch.cuda.get_device_properties(0).multi_processor_count)[1]
     X, W = synth.dense_input(synth.DenseShape(M=M, I=I, H=H), seed=7)
     Xd, Wd = X.cuda(), W.cuda()
     Y = torch.empty((M, H), dtype=torch.float32, device="cuda")
