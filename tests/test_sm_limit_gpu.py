@@ -145,3 +145,45 @@ def test_side_by_side_streams_equal_one_after_another():
                 _same(a, b, f"output {k}, repetition {rep}")
     finally:
         csa.set_stream_sm_limit(sd, 0)
+
+
+def test_side_by_side_streams_in_a_cuda_graph():
+    """The same schedule captured once into a CUDA graph (the bench's form of the default
+    step: a fork from the capturing stream into the two limited streams and a join) and
+    replayed: every replay equals the calls made one after another."""
+    shape, qkv = trimul_case(1, 1536, 4, 64, seed=64)
+    q = qkv.cuda()
+    xs, W = synth.dense_sweep_inputs(seed=2)
+    Wd = W.cuda()
+    Xs = [x.cuda() for x in xs[:16]]
+    H, I = W.shape
+    out = poisoned(shape.out_shape)
+    Ys = [poisoned((x.shape[0], H)) for x in Xs]
+    plan = csa.DenseGroupedPlan(Ys, Xs, Wd, I, H)
+    main = torch.cuda.current_stream()
+    plan(main)
+    csa.trimul_forward(out, q, shape.B, shape.T, shape.C, shape.NH, stream=main)
+    torch.cuda.synchronize()
+    base = [out.clone()] + [y.clone() for y in Ys]
+
+    sd, ss, cap = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    csa.set_stream_sm_limit(sd, 56)
+    try:
+        graph = torch.cuda.CUDAGraph()
+        cap.wait_stream(main)
+        with torch.cuda.graph(graph, stream=cap):
+            sd.wait_stream(cap)
+            ss.wait_stream(cap)
+            plan(sd)
+            csa.trimul_forward(out, q, shape.B, shape.T, shape.C, shape.NH, stream=ss)
+            cap.wait_stream(sd)
+            cap.wait_stream(ss)
+        for rep in range(3):
+            out.view(torch.int32).fill_(-1)
+            for y in Ys:
+                y.view(torch.int32).fill_(-1)
+            graph.replay()
+            for k, (a, b) in enumerate(zip([out] + Ys, base)):
+                _same(a, b, f"output {k}, replay {rep}")
+    finally:
+        csa.set_stream_sm_limit(sd, 0)
