@@ -66,6 +66,11 @@ def dense_flops(M, I, H):
     return 2 * M * I * H
 
 
+def dense_algorithmic_bytes(M, I, H):
+    """X and W read once (bf16), Y written once (fp32)."""
+    return (M * I + H * I) * 2 + M * H * 4
+
+
 def trimul_algorithmic_bytes(B, T, C, NH, lower_only=False, in_bytes=2):
     """Minimum HBM traffic of one trimul_forward: every output element written once
     (fp32), Q and K read once (bf16, or fp32 with in_bytes=4); V is never touched."""
@@ -267,8 +272,9 @@ class Part:
     the committed DRAM traffic record, if any."""
 
     def __init__(self, label, fn, kernels=1, kernel=None, bound=None, per_launch=None,
-                 traffic=None):
+                 traffic=None, hbm_bytes=None):
         self.label = label
+        self.hbm_bytes = hbm_bytes  # algorithmic HBM bytes of one launch (all parts)
         self.fn = fn
         self.kernels = kernels
         self.kernel = kernel
@@ -314,10 +320,9 @@ def make_workload(name, dev):
         out = torch.empty(shape.out_shape, dtype=torch.float32, device=dev)
         fn = lambda st: csa.trimul_forward(out, qkv, shape.B, shape.T, shape.C, shape.NH,
                                            lower_only=lower_only, stream=st)
+        nbytes = trimul_algorithmic_bytes(shape.B, shape.T, shape.C, shape.NH, lower_only)
         part = Part("trimul", fn, kernel="trimul_sm103a_kernel", bound="hbm",
-                    per_launch=trimul_algorithmic_bytes(shape.B, shape.T, shape.C, shape.NH,
-                                                        lower_only),
-                    traffic=traffic)
+                    per_launch=nbytes, traffic=traffic, hbm_bytes=nbytes)
         return part, [(qkv, qkv_h)], [out]
 
     def dense_part(shape, seed=0, label="dense_ragged"):
@@ -332,7 +337,8 @@ def make_workload(name, dev):
         part = Part(label, fn, kernels=2 if nbytes else 1,
                     kernel="realign_rows_kernel + dense_sm103a_kernel" if nbytes else
                     "dense_sm103a_kernel", bound="tensor",
-                    per_launch=dense_flops(shape.M, shape.I, shape.H), traffic="dense_ragged")
+                    per_launch=dense_flops(shape.M, shape.I, shape.H), traffic="dense_ragged",
+                    hbm_bytes=dense_algorithmic_bytes(shape.M, shape.I, shape.H))
         return part, [(X, X_h), (W, W_h)], [Y]
 
     def sweep_parts():
@@ -345,7 +351,8 @@ def make_workload(name, dev):
         plan = csa.DenseGroupedPlan(Ys, Xs, W, I, H)  # tensors checked once
         part = Part("dense_grouped", lambda st: plan(stream=st),
                     kernel="dense_sm103a_kernel<grouped, CTA pairs>", bound="tensor",
-                    per_launch=flops, traffic="dense_sweep_grouped")
+                    per_launch=flops, traffic="dense_sweep_grouped",
+                    hbm_bytes=H * I * 2 + sum(X.shape[0] * (I * 2 + H * 4) for X in Xs))
         calls = [(f"call{i}_M{X.shape[0]}", int(X.shape[0]), dense_flops(X.shape[0], I, H),
                   (lambda X, Y: lambda st: csa.dense_xwt(Y, X, W, X.shape[0], I, H,
                                                          stream=st))(X, Y))
@@ -757,6 +764,15 @@ def run_ours(args, rank, world, local):
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 4),
     }
+    if wl.parts and all(p.hbm_bytes for p in wl.parts):
+        # The whole step against HBM: every part's algorithmic bytes over the step time.
+        step_bytes = sum(p.hbm_bytes for p in wl.parts)
+        achieved = step_bytes / (total_ms / K * 1e-3) / 1e9
+        result["step_roofline"] = {
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(achieved / hbm_peak, 4), "algorithmic_bytes_per_step": step_bytes,
+            "note": "all parts' algorithmic bytes (inputs read once, outputs written once) "
+                    "over the step time"}
     if P <= 40:
         result["parts"] = {f"{part.label}_us": round(ms * 1e3, 2)
                            for part, ms in zip(wl.parts, part_ms)}
