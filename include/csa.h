@@ -196,8 +196,11 @@ csa_status trimul_forward_noalloc(float* out, const void* qkv, int B, int T, int
  * workspace, fetches them with loader warps; dense_xwt_ws computes the same
  * layer faster with caller workspace. Y is written by TMA when H*4 is a
  * multiple of 16 and Y is 16-byte aligned (4-byte alignment required
- * otherwise). Sums are fp32 accumulations of exact bf16 products, in the same
- * order on every fetch path (results are bit-identical). Nothing is allocated.
+ * otherwise). Tiles are 128 x BN (BN 64..256) per CTA, or, for problems large
+ * enough (csa_dense_tiling), 256 x BN per cluster of two CTAs (tcgen05
+ * cta_group::2) when the rows are fetched by TMA. Sums are fp32 accumulations of
+ * exact bf16 products, in the same order on every fetch path and tiling (results
+ * are bit-identical). Nothing is allocated.
  */
 csa_status dense_xwt(float* Y, const void* X, const void* W, int M, int I, int H);
 
