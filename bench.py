@@ -561,6 +561,7 @@ def run_ours(args, rank, world, local):
         launch(stream)
 
     graph = None
+    graph_error = None
     if args.graph or (wl.branches and not args.direct):
         # The step's launches captured once and replayed as one CUDA graph. A step
         # whose parts run on concurrent streams takes this form by default: the graph
@@ -574,9 +575,16 @@ def run_ours(args, rank, world, local):
         side = torch.cuda.Stream(dev)
         side.wait_stream(stream)
         graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=side):
-            launch(side)
-        torch.cuda.synchronize(dev)
+        try:
+            with torch.cuda.graph(graph, stream=side):
+                launch(side)
+            torch.cuda.synchronize(dev)
+        except Exception as e:  # reported in config.launch; the steps then launch directly
+            if args.graph:
+                raise
+            graph_error = f"{type(e).__name__}: {e}"
+            graph = None
+            torch.cuda.synchronize(dev)
 
     def run_step():
         if graph is not None:
@@ -743,7 +751,9 @@ def run_ours(args, rank, world, local):
     dominant = max(range(P), key=lambda p: part_ms[p])
     config = {"workload": wl.name, **wl.config,
               "l2": "flushed between timed steps (256 MiB write, outside the timed events)",
-              "launch": "one CUDA graph per step" if graph is not None else "direct launches",
+              "launch": ("one CUDA graph per step" if graph is not None else
+                         "direct launches" + (f" (graph capture failed: {graph_error})"
+                                              if graph_error else "")),
               "schedule": ("; ".join(
                   f"stream {i}: {' + '.join(p.label for p in parts)}"
                   + (f" (at most {limit} SMs)" if limit else " (no SM limit)")
